@@ -1,0 +1,135 @@
+"""fp64 CPU oracle of the gate-first sparse gated FFN.
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, the smoke check and the
+benchmark's CPU-baseline leg, never by the library.  It shares no code with the
+CUDA path.  The arithmetic lives in ``sffn_oracle.c`` (plain C99 + OpenMP, fp64)
+and in ``flops.py`` (operation counts); this module only compiles and loads the
+C file and marshals numpy arrays into it.
+
+Formulas followed: "Model casting: compute the gate, then skip most of the FFN"
+(ai.thesatyajit.com), sections "What an FFN actually computes" (y = W2(A(W1x) .*
+W3x)), "Model casting: make sparsity a target" (R-S+), "LoPA Gating: moving the
+ceiling" (W1 = G + UV; the UV part only).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+from . import flops  # noqa: F401  (re-exported)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sffn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+F32, BF16 = 0, 1
+RELU, RSP = 0, 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile sffn_oracle.c into liboracle.so next to it (gcc, OpenMP, -O2)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+               "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    vp, ip = ctypes.c_void_p, ctypes.c_int
+    for name in ("oracle_ffn_dense", "oracle_ffn_gate_first"):
+        f = getattr(lib, name)
+        f.restype = ip
+        f.argtypes = [ip] * 6 + [vp] * 9
+    lib.oracle_num_threads.restype = ip
+    lib.oracle_num_threads.argtypes = []
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(_LIB)
+    return _lib
+
+
+class Variant:
+    """The oracle's entry points bound to another build of the C source.
+
+    Used only by the test that plants mistakes in a copy of the source to check
+    that the pins catch them.
+    """
+
+    def __init__(self, so_path):
+        self._lib = _bind(so_path)
+
+    def ffn_dense(self, *a):
+        return _call("oracle_ffn_dense", *a[:5], *a[5:11],
+                     lambda B: np.zeros((B, a[1]), dtype=np.float64), lib=self._lib)
+
+    def ffn_gate_first(self, *a):
+        return _call("oracle_ffn_gate_first", *a[:5], *a[5:11],
+                     lambda B: np.full((B, a[1]), -1, dtype=np.int32), lib=self._lib)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
+    return int(_load().oracle_num_threads())
+
+
+def _as_input(a, dtype):
+    """Check an input array against the stored dtype: float32, or uint16 bf16 bits."""
+    if a is None:
+        return None
+    want = np.float32 if dtype == F32 else np.uint16
+    a = np.ascontiguousarray(a)
+    if a.dtype != want:
+        raise TypeError(f"oracle input must be {np.dtype(want).name}, got {a.dtype}")
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None):
+    x = _as_input(x, dtype)
+    B = x.size // D
+    if x.size != B * D:
+        raise ValueError("x size is not a multiple of D")
+    arrs = [_as_input(a, dtype) for a in (W1, U, V, W3, W2)]
+    W1, U, V, W3, W2 = arrs
+    if r == 0:
+        assert W1 is not None and W1.size == H * D
+    else:
+        assert U is not None and U.size == H * r and V is not None and V.size == r * D
+    assert W3.size == H * D and W2.size == D * H
+    y = np.zeros((B, D), dtype=np.float64)
+    n_live = np.zeros(B, dtype=np.int32)
+    out = extra(B)
+    rc = getattr(lib or _load(), name)(D, H, r, act, dtype, B, _ptr(W1), _ptr(U), _ptr(V),
+                                _ptr(W3), _ptr(W2), _ptr(x), _ptr(y), _ptr(out), _ptr(n_live))
+    if rc != 0:
+        raise RuntimeError(f"{name} failed with code {rc}")
+    return y, out, n_live
+
+
+def ffn_dense(D, H, r, act, dtype, W1, U, V, W3, W2, x):
+    """Dense definition.  Returns (y[B,D] f64, z[B,H] f64 pre-activations, n_live[B])."""
+    return _call("oracle_ffn_dense", D, H, r, act, dtype, W1, U, V, W3, W2, x,
+                 lambda B: np.zeros((B, H), dtype=np.float64))
+
+
+def ffn_gate_first(D, H, r, act, dtype, W1, U, V, W3, W2, x):
+    """Gate-first evaluation.  Returns (y[B,D] f64, idx[B,H] live set padded with -1, n_live[B])."""
+    return _call("oracle_ffn_gate_first", D, H, r, act, dtype, W1, U, V, W3, W2, x,
+                 lambda B: np.full((B, H), -1, dtype=np.int32))

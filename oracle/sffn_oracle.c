@@ -1,0 +1,264 @@
+/*
+ * sffn_oracle.c -- plain fp64 CPU oracle of the gated FFN forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library.  It shares no code, header,
+ * table or helper with the CUDA library: it is written straight from the
+ * formulas of "Model casting: compute the gate, then skip most of the FFN"
+ * (ai.thesatyajit.com), sections "What an FFN actually computes",
+ * "The 3x ceiling, and why W1 is always on", "Model casting: make sparsity a
+ * target" (R-S+ definition) and "LoPA Gating: moving the ceiling".
+ *
+ * Definitions followed (one token x in R^D, hidden width H):
+ *   z = W1 x                     standard gate,  W1 in R^{H x D}
+ *   z = U (V x)                  low-rank gate,  U in R^{H x r}, V in R^{r x D}
+ *                                (the UV part of W1 = G + UV; G, the RMSNorm
+ *                                 between V and U and the double activation
+ *                                 are not part of this path)
+ *   a = A(z)                     A = ReLU, or R-S+ (x*sigmoid(x) for x >= 0,
+ *                                0 for x < 0)
+ *   u = W3 x                     W3 in R^{H x D}
+ *   y = W2 (a .* u)              W2 in R^{D x H}
+ *
+ * Everything is accumulated in double precision, each sum in ascending index
+ * order, with no blocking, fusion or reordering.  Inputs are the values the
+ * device sees: fp32 arrays, or bf16 bit patterns (uint16, the upper half of an
+ * IEEE binary32), widened exactly to double.
+ *
+ * Two evaluations are provided:
+ *   oracle_ffn_dense      -- the formula above over all H units (the definition)
+ *   oracle_ffn_gate_first -- the gate-first order the pages describe: compute
+ *                            the gate, keep the live set S = {i : z_i > 0},
+ *                            evaluate W3 rows and W2 columns only for i in S.
+ * The pages' claim (skipping dead units leaves y unchanged) says the two agree
+ * exactly; the tests check that.
+ *
+ * Portable C99 + OpenMP; no SIMD intrinsics, no -ffast-math.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_F32 0
+#define OR_BF16 1
+#define OR_RELU 0
+#define OR_RSP 1
+
+/* exact widening of one stored element to double */
+static double elem(const void* p, int dtype, size_t i) {
+  if (dtype == OR_F32) return (double)((const float*)p)[i];
+  uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* widen n consecutive elements starting at element offset off */
+static void widen_row(const void* p, int dtype, size_t off, int n, double* out) {
+  for (int j = 0; j < n; ++j) out[j] = elem(p, dtype, off + (size_t)j);
+}
+
+static double dot(const double* a, const double* b, int n) {
+  double s = 0.0;
+  for (int j = 0; j < n; ++j) s += a[j] * b[j];
+  return s;
+}
+
+/* The activation A.  Both vanish for z <= 0, so the live test is z > 0. */
+static double activation(int act, double z) {
+  if (!(z > 0.0)) return 0.0;
+  if (act == OR_RELU) return z;
+  return z / (1.0 + exp(-z)); /* R-S+ on the positive side: z * sigmoid(z) */
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+static int check_args(int D, int H, int r, int act, int dtype, int B) {
+  if (D <= 0 || H <= 0 || r < 0 || B < 0) return -1;
+  if (act != OR_RELU && act != OR_RSP) return -1;
+  if (dtype != OR_F32 && dtype != OR_BF16) return -1;
+  return 0;
+}
+
+/* Gate pre-activations z[H] for one token xd[D] (already widened). */
+static int gate(int D, int H, int r, int dtype, const void* W1, const void* U,
+                const void* V, const double* xd, double* z) {
+  if (r == 0) {
+    int bad = 0;
+#pragma omp parallel
+    {
+      double* row = (double*)malloc(sizeof(double) * (size_t)D);
+      if (!row) {
+#pragma omp atomic write
+        bad = 1;
+      }
+#pragma omp for schedule(static)
+      for (int i = 0; i < H; ++i) {
+        if (!row) continue;
+        widen_row(W1, dtype, (size_t)i * D, D, row);
+        z[i] = dot(row, xd, D);
+      }
+      free(row);
+    }
+    return bad ? -2 : 0;
+  }
+  /* low-rank gate: t = V x (kept in double, not rounded), z = U t */
+  double* t = (double*)malloc(sizeof(double) * (size_t)r);
+  if (!t) return -2;
+  int bad = 0;
+#pragma omp parallel
+  {
+    double* row = (double*)malloc(sizeof(double) * (size_t)(D > r ? D : r));
+    if (!row) {
+#pragma omp atomic write
+      bad = 1;
+    }
+#pragma omp for schedule(static)
+    for (int k = 0; k < r; ++k) {
+      if (!row) continue;
+      widen_row(V, dtype, (size_t)k * D, D, row);
+      t[k] = dot(row, xd, D);
+    }
+#pragma omp for schedule(static)
+    for (int i = 0; i < H; ++i) {
+      if (!row) continue;
+      widen_row(U, dtype, (size_t)i * r, r, row);
+      z[i] = dot(row, t, r);
+    }
+    free(row);
+  }
+  free(t);
+  return bad ? -2 : 0;
+}
+
+/*
+ * Dense definition.  Per token b (x[b] is row b of x[B,D]):
+ *   y[b] = W2 (A(gate) .* (W3 x[b])), summing over all H units.
+ * Outputs: y[B*D] (double), z[B*H] (double pre-activations, may be NULL),
+ * n_live[B] (= |{i : z_i > 0}|, may be NULL).  Returns 0, or <0 on bad
+ * arguments / allocation failure.
+ */
+int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
+                     const void* W1, const void* U, const void* V,
+                     const void* W3, const void* W2, const void* x,
+                     double* y, double* z, int* n_live) {
+  if (check_args(D, H, r, act, dtype, B)) return -1;
+  double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* zb = (double*)malloc(sizeof(double) * (size_t)H);
+  double* g = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!xd || !zb || !g) {
+    free(xd); free(zb); free(g);
+    return -2;
+  }
+  int rc = 0;
+  for (int b = 0; b < B && rc == 0; ++b) {
+    widen_row(x, dtype, (size_t)b * D, D, xd);
+    rc = gate(D, H, r, dtype, W1, U, V, xd, zb);
+    if (rc) break;
+    int bad = 0;
+#pragma omp parallel
+    {
+      double* row = (double*)malloc(sizeof(double) * (size_t)(D > H ? D : H));
+      if (!row) {
+#pragma omp atomic write
+        bad = 1;
+      }
+      /* up projection and gate product over every unit */
+#pragma omp for schedule(static)
+      for (int i = 0; i < H; ++i) {
+        if (!row) continue;
+        widen_row(W3, dtype, (size_t)i * D, D, row);
+        double u = dot(row, xd, D);
+        g[i] = activation(act, zb[i]) * u;
+      }
+      /* down projection: y_m = sum_i W2[m,i] g_i, i ascending */
+#pragma omp for schedule(static)
+      for (int m = 0; m < D; ++m) {
+        if (!row) continue;
+        widen_row(W2, dtype, (size_t)m * H, H, row);
+        y[(size_t)b * D + m] = dot(row, g, H);
+      }
+      free(row);
+    }
+    if (bad) { rc = -2; break; }
+    int cnt = 0;
+    for (int i = 0; i < H; ++i) cnt += (zb[i] > 0.0);
+    if (n_live) n_live[b] = cnt;
+    if (z) memcpy(z + (size_t)b * H, zb, sizeof(double) * (size_t)H);
+  }
+  free(xd); free(zb); free(g);
+  return rc;
+}
+
+/*
+ * Gate-first evaluation: the gate over all units, then only the live set.
+ *   S = {i : z_i > 0} in ascending order
+ *   h_i = A(z_i) * (W3[i,:] . x)          for i in S
+ *   y_m = sum_{i in S} W2[m,i] h_i       (i ascending)
+ * Same outputs and return codes as oracle_ffn_dense; idx[B*H] (may be NULL)
+ * receives S for each token, padded with -1.
+ */
+int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
+                          const void* W1, const void* U, const void* V,
+                          const void* W3, const void* W2, const void* x,
+                          double* y, int* idx, int* n_live) {
+  if (check_args(D, H, r, act, dtype, B)) return -1;
+  double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* zb = (double*)malloc(sizeof(double) * (size_t)H);
+  double* h = (double*)malloc(sizeof(double) * (size_t)H);
+  int* S = (int*)malloc(sizeof(int) * (size_t)H);
+  if (!xd || !zb || !h || !S) {
+    free(xd); free(zb); free(h); free(S);
+    return -2;
+  }
+  int rc = 0;
+  for (int b = 0; b < B && rc == 0; ++b) {
+    widen_row(x, dtype, (size_t)b * D, D, xd);
+    rc = gate(D, H, r, dtype, W1, U, V, xd, zb);
+    if (rc) break;
+    int k = 0;
+    for (int i = 0; i < H; ++i)
+      if (zb[i] > 0.0) S[k++] = i;
+    int bad = 0;
+#pragma omp parallel
+    {
+      double* row = (double*)malloc(sizeof(double) * (size_t)D);
+      if (!row) {
+#pragma omp atomic write
+        bad = 1;
+      }
+#pragma omp for schedule(static)
+      for (int q = 0; q < k; ++q) {
+        if (!row) continue;
+        int i = S[q];
+        widen_row(W3, dtype, (size_t)i * D, D, row);
+        h[q] = activation(act, zb[i]) * dot(row, xd, D);
+      }
+#pragma omp for schedule(static)
+      for (int m = 0; m < D; ++m) {
+        double s = 0.0;
+        for (int q = 0; q < k; ++q)
+          s += elem(W2, dtype, (size_t)m * H + (size_t)S[q]) * h[q];
+        y[(size_t)b * D + m] = s;
+      }
+      free(row);
+    }
+    if (bad) { rc = -2; break; }
+    if (n_live) n_live[b] = k;
+    if (idx) {
+      for (int q = 0; q < H; ++q) idx[(size_t)b * H + q] = (q < k) ? S[q] : -1;
+    }
+  }
+  free(xd); free(zb); free(h); free(S);
+  return rc;
+}

@@ -1,0 +1,122 @@
+"""The oracle's pins have teeth: plant plausible mistakes in copies of the C
+source, build each copy, and check that at least one pin rejects it.
+
+Every mistake is planted in the oracle (CPU only); nothing here touches the GPU.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "sffn_oracle.c")
+
+MUTANTS = {
+    "w2_transposed": ("widen_row(W2, dtype, (size_t)m * H, H, row);",
+                      "for (int i2 = 0; i2 < H; ++i2) row[i2] = elem(W2, dtype, (size_t)i2 * D + m);"),
+    "w3_dropped": ("g[i] = activation(act, zb[i]) * u;", "g[i] = activation(act, zb[i]);"),
+    "gate_row_off_by_one": ("widen_row(W1, dtype, (size_t)i * D, D, row);",
+                            "widen_row(W1, dtype, (size_t)((i + 1) % H) * D, D, row);"),
+    "live_count_ge": ("cnt += (zb[i] > 0.0);", "cnt += (zb[i] >= 0.0);"),
+    "activation_wrong_side": ("if (!(z > 0.0)) return 0.0;", "if (!(z < 0.0)) return 0.0;"),
+    "rsp_sigmoid_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "rsp_missing_z": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "bf16_widen_shift": ("<< 16;", "<< 15;"),
+    "dot_drops_last_term": ("for (int j = 0; j < n; ++j) s += a[j] * b[j];",
+                            "for (int j = 0; j + 1 < n; ++j) s += a[j] * b[j];"),
+    "u_transposed": ("widen_row(U, dtype, (size_t)i * r, r, row);",
+                     "for (int k2 = 0; k2 < r; ++k2) row[k2] = elem(U, dtype, (size_t)k2 * H + i);"),
+    "gate_first_skips_first_live": ("for (int q = 0; q < k; ++q) {\n        if (!row) continue;",
+                                    "for (int q = 1; q < k; ++q) {\n        if (!row) continue;"),
+}
+
+
+def _bf16_bits(a):
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).bfloat16()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _cast(a, dtype):
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype=np.float32) if dtype == oracle.F32 else _bf16_bits(a)
+
+
+def _pins(mod):
+    """Run a compact set of the pins against `mod`; return the names that fail."""
+    failed = []
+
+    def run(W1, W3, W2, x, act=oracle.RELU, U=None, V=None, r=0, dtype=oracle.F32, fn="ffn_dense"):
+        H, D = W3.shape
+        c = lambda a: _cast(a, dtype)  # noqa: E731
+        return getattr(mod, fn)(D, H, r, act, dtype, c(W1), c(U), c(V), c(W3), c(W2), c(x))
+
+    def check(name, cond):
+        if not cond:
+            failed.append(name)
+
+    # hand-worked case (values derived in test_oracle_pins)
+    X = np.array([[1.0, -2.0, 1.0]])
+    W1 = np.array([[1.0, 0.0, -0.5], [0.0, 1.0, 0.0], [-1.0, -1.0, 0.25], [2.0, 1.0, 0.0]])
+    W3 = np.array([[1.0, 1.0, 3.0], [5.0, 0.0, 0.0], [0.0, -1.0, 1.0], [7.0, 0.0, 0.0]])
+    W2 = np.array([[1.0, 100.0, 2.0, 100.0], [-1.0, 100.0, 0.5, 100.0], [0.0, 100.0, -4.0, 100.0]])
+    for dt in (oracle.F32, oracle.BF16):
+        y, z, n = run(W1, W3, W2, X, dtype=dt)
+        check("hand_relu", y.tolist() == [[8.5, 0.875, -15.0]] and n.tolist() == [2])
+        yg, idx, ng = run(W1, W3, W2, X, dtype=dt, fn="ffn_gate_first")
+        check("hand_gate_first", yg.tolist() == [[8.5, 0.875, -15.0]] and ng.tolist() == [2])
+    s05, s125 = 1 / (1 + math.exp(-0.5)), 1 / (1 + math.exp(-1.25))
+    h0, h2 = 0.5 * s05 * 2.0, 1.25 * s125 * 3.0
+    y, _, _ = run(W1, W3, W2, X, act=oracle.RSP)
+    check("hand_rsp", np.allclose(y[0], [h0 + 2 * h2, -h0 + 0.5 * h2, -4 * h2], rtol=1e-15, atol=1e-15))
+    # all-live bilinear map through numpy
+    rng = np.random.default_rng(3)
+    D, H, B = 24, 40, 3
+    A1 = rng.standard_normal((H, D)).astype(np.float32) / np.float32(5); A1[:, D - 1] = 10.0
+    A3 = rng.standard_normal((H, D)).astype(np.float32)
+    A2 = rng.standard_normal((D, H)).astype(np.float32)
+    xa = rng.standard_normal((B, D)).astype(np.float32); xa[:, D - 1] = 1.0
+    y, z, n = run(A1, A3, A2, xa)
+    d = [a.astype(np.float64) for a in (A1, A3, A2, xa)]
+    want = ((d[3] @ d[0].T) * (d[3] @ d[1].T)) @ d[2].T
+    check("all_live_library", np.allclose(y, want, rtol=1e-12, atol=1e-12))
+    # low-rank gate with integer factors == standard gate with W1 = U V (numpy)
+    rng = np.random.default_rng(13)
+    D, H, r, B = 16, 40, 4, 3
+    U = rng.integers(-3, 4, size=(H, r)).astype(np.float64)
+    V = rng.integers(-3, 4, size=(r, D)).astype(np.float64)
+    L3 = rng.integers(-3, 4, size=(H, D)).astype(np.float64)
+    L2 = rng.integers(-3, 4, size=(D, H)).astype(np.float64)
+    xl = rng.integers(-3, 4, size=(B, D)).astype(np.float64)
+    yl, zl, _ = run(None, L3, L2, xl, U=U, V=V, r=r)
+    check("lopa_materialised", np.array_equal(zl, xl @ (U @ V).T))
+    # bf16 bit patterns 0x3F80 = 1, 0xC000 = -2, 0x3EAB = 0.333984375
+    bits = lambda v: np.array(v, dtype=np.uint16)  # noqa: E731
+    y, z, n = mod.ffn_dense(3, 1, 0, oracle.RELU, oracle.BF16, bits([0x3F80, 0, 0]), None, None,
+                            bits([0xC000, 0, 0]), bits([0x3F80, 0xC000, 0x3EAB]),
+                            bits([0x3EAB, 0x3F80, 0x3F80]))
+    h = 0.333984375 * (-2.0 * 0.333984375)
+    check("bf16_bits", y[0].tolist() == [h, -2.0 * h, 0.333984375 * h])
+    return failed
+
+
+def test_pins_pass_on_the_oracle():
+    assert _pins(oracle) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared", "-o", str(so),
+                    str(mutated), "-lm"], check=True)
+    failed = _pins(oracle.Variant(str(so)))
+    assert failed, f"mutant {name} passed every pin"
