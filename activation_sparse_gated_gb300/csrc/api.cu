@@ -1,0 +1,329 @@
+// api.cu -- the C ABI of include/sffn.h: handles, argument checks, weight
+// repacking (W2 -> W2^T), launch planning and dispatch, error reporting.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sffn.h"
+
+using namespace sffn;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define SFFN_CUDA(call)                                                                        \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return fail(e_ == cudaErrorMemoryAllocation ? SFFN_ERR_NOMEM : SFFN_ERR_CUDA,            \
+                  "%s failed: %s", #call, cudaGetErrorString(e_));                             \
+  } while (0)
+
+constexpr unsigned long long kTimeoutNs = 250000000ull;  // 250 ms per device-side wait
+
+}  // namespace
+
+struct sffn_s {
+  int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
+  int device = 0, num_sms = 0;
+  size_t max_smem = 0;
+  void* gate_w = nullptr;  // W1[H, D] or U[H, r]
+  void* V = nullptr;       // V[r, D]
+  void* W3 = nullptr;      // W3[H, D]
+  void* W2t = nullptr;     // W2^T[H, D]
+  float* yacc = nullptr;   // [SFFN_MAX_BATCH, D]
+  float* tbuf = nullptr;   // [SFFN_MAX_BATCH, r]
+  int* ctrl = nullptr;     // CTRL_INTS
+  int* counts = nullptr;   // [SFFN_MAX_BATCH]
+  uint8_t* mask = nullptr; // [SFFN_MAX_BATCH, H]
+  bool weights_set = false;
+  int last_B = 0;
+  cudaEvent_t ev = nullptr;
+  bool ev_valid = false;
+  int b1_grid = 0, b1_ns1 = 0, b1_ns2 = 0;
+  size_t b1_smem = 0;
+};
+
+namespace {
+
+int gate_k(const sffn_s* h) { return h->r > 0 ? h->r : h->D; }
+
+void release(sffn_s* h) {
+  cudaFree(h->gate_w);
+  cudaFree(h->V);
+  cudaFree(h->W3);
+  cudaFree(h->W2t);
+  cudaFree(h->yacc);
+  cudaFree(h->tbuf);
+  cudaFree(h->ctrl);
+  cudaFree(h->counts);
+  cudaFree(h->mask);
+  if (h->ev) cudaEventDestroy(h->ev);
+}
+
+int plan_b1(sffn_s* h) {
+  const bool lopa = h->r > 0;
+  const int gk = gate_k(h);
+  h->b1_grid = std::min(h->num_sms, h->H);
+  const int rows_max = (h->H + h->b1_grid - 1) / h->b1_grid;
+  const size_t grow = (size_t)gk * h->elt;
+  const int ns2 = 8;  // >= the number of gate warps (slot ownership rule of the kernel)
+  const size_t base = ffn_b1_smem_bytes(h->D, gk, h->elt, lopa, 0, ns2);
+  if (base + 128 + (size_t)B1_NWG * grow > h->max_smem)
+    return fail(SFFN_ERR_DTYPE, "D=%d, gate width %d do not fit the fused kernel's shared memory",
+                h->D, gk);
+  int ns1 = (int)((h->max_smem - base - 128) / grow);
+  ns1 = std::min(ns1, B1_NS1_MAX);
+  ns1 = std::min(ns1, (rows_max + B1_NWG - 1) / B1_NWG * B1_NWG);
+  ns1 = ns1 / B1_NWG * B1_NWG;  // each gate warp owns whole slots
+  if (ns1 < B1_NWG) ns1 = B1_NWG;
+  h->b1_ns1 = ns1;
+  h->b1_ns2 = ns2;
+  h->b1_smem = ffn_b1_smem_bytes(h->D, gk, h->elt, lopa, ns1, ns2);
+  if (h->b1_smem > h->max_smem) return fail(SFFN_ERR_DTYPE, "shared-memory plan exceeds the device limit");
+  return SFFN_OK;
+}
+
+int check_device(const sffn_s* h) {
+  int dev = -1;
+  SFFN_CUDA(cudaGetDevice(&dev));
+  if (dev != h->device)
+    return fail(SFFN_ERR_STATE, "handle belongs to device %d but device %d is current", h->device, dev);
+  return SFFN_OK;
+}
+
+// Wait for the handle's last forward; report and clear a device-side error.
+int sync_and_check(sffn_s* h) {
+  if (h->ev_valid) {
+    SFFN_CUDA(cudaEventSynchronize(h->ev));
+  } else {
+    SFFN_CUDA(cudaDeviceSynchronize());
+  }
+  int err = 0;
+  SFFN_CUDA(cudaMemcpy(&err, h->ctrl + CTRL_ERR, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err != 0) {
+    // the aborted kernel may have left partial sums and counters behind
+    SFFN_CUDA(cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS));
+    SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * h->D));
+    return fail(SFFN_ERR_TIMEOUT, "a device-side wait ran out of time (error word 0x%x); outputs of "
+                "the affected forward are invalid", err);
+  }
+  return SFFN_OK;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sffn_version(void) { return 100; }
+
+const char* sffn_last_error(void) { return g_msg; }
+
+const char* sffn_strerror(int code) {
+  switch (code) {
+    case SFFN_OK: return "success";
+    case SFFN_ERR_ARG: return "invalid argument";
+    case SFFN_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case SFFN_ERR_DTYPE: return "unsupported dtype or shape";
+    case SFFN_ERR_CUDA: return "CUDA runtime error";
+    case SFFN_ERR_TIMEOUT: return "device-side wait timed out";
+    case SFFN_ERR_STATE: return "call out of order";
+    case SFFN_ERR_NOMEM: return "device memory allocation failed";
+    default: return "unknown status";
+  }
+}
+
+sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
+  g_msg[0] = 0;
+  if (dtype != SFFN_F32 && dtype != SFFN_BF16) { fail(SFFN_ERR_ARG, "dtype %d unknown", dtype); return nullptr; }
+  if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP) { fail(SFFN_ERR_ARG, "act %d unknown", act); return nullptr; }
+  const int dmax = dtype == SFFN_BF16 ? SFFN_MAX_D_BF16 : SFFN_MAX_D_F32;
+  if (D < 8 || D % 8 != 0 || D > dmax) { fail(SFFN_ERR_ARG, "D=%d must be a multiple of 8 in [8, %d]", D, dmax); return nullptr; }
+  if (H < 1) { fail(SFFN_ERR_ARG, "H=%d must be >= 1", H); return nullptr; }
+  if (r < 0 || r % 8 != 0 || r > D) { fail(SFFN_ERR_ARG, "r=%d must be 0 or a multiple of 8 <= D", r); return nullptr; }
+
+  sffn_s* h = new (std::nothrow) sffn_s;
+  if (!h) { fail(SFFN_ERR_NOMEM, "host allocation failed"); return nullptr; }
+  h->D = D; h->H = H; h->r = r; h->act = act; h->dtype = dtype;
+  h->elt = dtype == SFFN_BF16 ? 2 : 4;
+
+  auto bail = [&](int code, const char* what, cudaError_t e) -> sffn_t {
+    fail(code, "%s: %s", what, cudaGetErrorString(e));
+    release(h);
+    delete h;
+    return nullptr;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&h->device))) return bail(SFFN_ERR_CUDA, "cudaGetDevice", e);
+  if ((e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device)))
+    return bail(SFFN_ERR_CUDA, "cudaDeviceGetAttribute", e);
+  int optin = 0;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device)))
+    return bail(SFFN_ERR_CUDA, "cudaDeviceGetAttribute", e);
+  h->max_smem = (size_t)optin;
+
+  const size_t elt = h->elt;
+  const size_t gk = (size_t)gate_k(h);
+  struct { void** p; size_t bytes; } allocs[] = {
+      {&h->gate_w, (size_t)H * gk * elt},
+      {&h->V, (size_t)std::max(r, 1) * D * elt},
+      {&h->W3, (size_t)H * D * elt},
+      {&h->W2t, (size_t)H * D * elt},
+      {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * D},
+      {(void**)&h->tbuf, sizeof(float) * SFFN_MAX_BATCH * std::max(r, 8)},
+      {(void**)&h->ctrl, sizeof(int) * CTRL_INTS},
+      {(void**)&h->counts, sizeof(int) * SFFN_MAX_BATCH},
+      {(void**)&h->mask, (size_t)SFFN_MAX_BATCH * H},
+  };
+  for (auto& a : allocs) {
+    if ((e = cudaMalloc(a.p, a.bytes))) return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
+  }
+  if ((e = cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * D)) ||
+      (e = cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS)) ||
+      (e = cudaMemset(h->counts, 0, sizeof(int) * SFFN_MAX_BATCH)) ||
+      (e = cudaMemset(h->mask, 0, (size_t)SFFN_MAX_BATCH * H)))
+    return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+  if ((e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming)))
+    return bail(SFFN_ERR_CUDA, "cudaEventCreate", e);
+  if (plan_b1(h) != SFFN_OK) {
+    char keep[sizeof g_msg];
+    std::memcpy(keep, g_msg, sizeof keep);
+    release(h);
+    delete h;
+    std::memcpy(g_msg, keep, sizeof keep);
+    return nullptr;
+  }
+  if ((e = ffn_b1_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+  if ((e = cudaDeviceSynchronize())) return bail(SFFN_ERR_CUDA, "cudaDeviceSynchronize", e);
+  return h;
+}
+
+int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W3, const void* W2,
+                     void* stream) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (!W1_or_U || !W3 || !W2 || (h->r > 0 && !V)) return fail(SFFN_ERR_ARG, "null weight pointer");
+  if (int rc = check_device(h)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t elt = h->elt, D = h->D, H = h->H, gk = gate_k(h);
+  SFFN_CUDA(cudaMemcpyAsync(h->gate_w, W1_or_U, H * gk * elt, cudaMemcpyDefault, s));
+  if (h->r > 0) SFFN_CUDA(cudaMemcpyAsync(h->V, V, (size_t)h->r * D * elt, cudaMemcpyDefault, s));
+  SFFN_CUDA(cudaMemcpyAsync(h->W3, W3, H * D * elt, cudaMemcpyDefault, s));
+  void* stage = nullptr;
+  SFFN_CUDA(cudaMalloc(&stage, D * H * elt));
+  cudaError_t e = cudaMemcpyAsync(stage, W2, D * H * elt, cudaMemcpyDefault, s);
+  if (!e) e = launch_transpose(stage, h->W2t, (int)D, (int)H, (int)elt, s);
+  if (!e) e = cudaStreamSynchronize(s);
+  cudaFree(stage);
+  if (e) return fail(SFFN_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(e));
+  h->weights_set = true;
+  return SFFN_OK;
+}
+
+int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (!x || !y) return fail(SFFN_ERR_ARG, "null x or y");
+  if (B < 1 || B > SFFN_MAX_BATCH) return fail(SFFN_ERR_ARG, "B=%d outside [1, %d]", B, SFFN_MAX_BATCH);
+  if (((uintptr_t)x & 15) || ((uintptr_t)y & 15)) return fail(SFFN_ERR_ALIGN, "x and y must be 16-byte aligned");
+  const size_t xbytes = (size_t)B * h->D * h->elt;
+  if (ranges_overlap(x, xbytes, y, xbytes)) return fail(SFFN_ERR_ARG, "x and y overlap");
+  if (!h->weights_set) return fail(SFFN_ERR_STATE, "sffn_set_weights has not been called");
+  if (int rc = check_device(h)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool lopa = h->r > 0;
+  const size_t row = (size_t)h->D * h->elt;
+
+  if (lopa) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
+  for (int b = 0; b < B; ++b) {
+    B1Params p;
+    p.gate_w = h->gate_w;
+    p.W3 = h->W3;
+    p.W2t = h->W2t;
+    p.x = static_cast<const uint8_t*>(x) + b * row;
+    p.t = lopa ? h->tbuf + (size_t)b * h->r : nullptr;
+    p.y = static_cast<uint8_t*>(y) + b * row;
+    p.yacc = h->yacc;
+    p.ctrl = h->ctrl;
+    p.counts = h->counts + b;
+    p.mask = h->mask + (size_t)b * h->H;
+    p.D = h->D;
+    p.H = h->H;
+    p.gate_k = gate_k(h);
+    p.ns1 = h->b1_ns1;
+    p.ns2 = h->b1_ns2;
+    p.act = h->act;
+    p.count_slot = b;
+    p.timeout_ns = kTimeoutNs;
+    SFFN_CUDA(launch_ffn_b1(p, h->dtype, lopa, h->b1_grid, h->b1_smem, s));
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  SFFN_CUDA(cudaStreamIsCapturing(s, &cs));
+  if (cs == cudaStreamCaptureStatusNone) {
+    SFFN_CUDA(cudaEventRecord(h->ev, s));
+    h->ev_valid = true;
+  } else {
+    h->ev_valid = false;  // inside a capture: readers fall back to a device-wide sync
+  }
+  h->last_B = B;
+  return SFFN_OK;
+}
+
+int sffn_active_counts(sffn_t h, int* counts_host, int B) {
+  if (!h || !counts_host) return fail(SFFN_ERR_ARG, "null argument");
+  if (h->last_B == 0) return fail(SFFN_ERR_STATE, "no forward has run on this handle");
+  if (B != h->last_B) return fail(SFFN_ERR_ARG, "B=%d but the last forward had B=%d", B, h->last_B);
+  if (int rc = sync_and_check(h)) return rc;
+  SFFN_CUDA(cudaMemcpy(counts_host, h->counts, sizeof(int) * B, cudaMemcpyDeviceToHost));
+  return SFFN_OK;
+}
+
+int sffn_active_mask(sffn_t h, uint8_t* mask_host, int B) {
+  if (!h || !mask_host) return fail(SFFN_ERR_ARG, "null argument");
+  if (h->last_B == 0) return fail(SFFN_ERR_STATE, "no forward has run on this handle");
+  if (B != h->last_B) return fail(SFFN_ERR_ARG, "B=%d but the last forward had B=%d", B, h->last_B);
+  if (int rc = sync_and_check(h)) return rc;
+  SFFN_CUDA(cudaMemcpy(mask_host, h->mask, (size_t)B * h->H, cudaMemcpyDeviceToHost));
+  return SFFN_OK;
+}
+
+int sffn_synchronize(sffn_t h) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  return sync_and_check(h);
+}
+
+int sffn_debug_timeout_probe(sffn_t h, int limit_us, void* stream) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (limit_us < 1 || limit_us > 1000000) return fail(SFFN_ERR_ARG, "limit_us=%d outside [1, 1e6]", limit_us);
+  if (int rc = check_device(h)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SFFN_CUDA(launch_timeout_probe(h->ctrl, (unsigned long long)limit_us * 1000ull, s));
+  SFFN_CUDA(cudaEventRecord(h->ev, s));
+  h->ev_valid = true;
+  return SFFN_OK;
+}
+
+void sffn_destroy(sffn_t h) {
+  if (!h) return;
+  if (h->ev_valid) cudaEventSynchronize(h->ev);
+  release(h);
+  delete h;
+}
+
+}  // extern "C"

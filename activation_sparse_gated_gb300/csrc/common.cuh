@@ -1,0 +1,176 @@
+// common.cuh -- sm_103a device helpers: mbarriers, bulk async copies (TMA
+// engine, non-tensor form), programmatic dependent launch, bounded waits, and
+// bf16/fp32 unpacking for the fp32-accumulating dot products.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sffn {
+
+// device error word bits (the handle's ctrl[CTRL_ERR])
+constexpr int DEV_ERR_TIMEOUT = 1;
+
+// ctrl[] layout: one small int array per handle
+constexpr int CTRL_TICKET = 0;   // blocks finished in the current forward
+constexpr int CTRL_ERR = 1;      // device error word (sticky until read)
+constexpr int CTRL_PROBE = 2;    // flag the timeout probe waits on (never set)
+constexpr int CTRL_COUNT = 4;    // [B_max] live-count accumulators
+constexpr int CTRL_INTS = 4 + 128;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Gives up when `abort` (a shared flag
+// another role raised) becomes non-zero or after `limit_ns`, in which case it
+// raises `abort`, records DEV_ERR_TIMEOUT in `err` and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* err, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort = 1;
+        atomicOr(err, DEV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// One contiguous global -> shared copy on the bulk-copy (TMA) engine,
+// completing `bytes` of transaction count on `bar`.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Programmatic dependent launch: wait for the preceding kernel in the stream
+// (and its memory) / allow the next kernel to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Element traits: a 16-byte chunk holds VPC values; `unpack` widens it to fp32.
+template <typename T>
+struct Elt;
+
+struct bf16_tag {};
+
+template <>
+struct Elt<float> {
+  static constexpr int VPC = 4;
+  static constexpr int BYTES = 4;
+  __device__ __forceinline__ static void unpack(const uint4& c, float (&v)[4]) {
+    v[0] = __uint_as_float(c.x);
+    v[1] = __uint_as_float(c.y);
+    v[2] = __uint_as_float(c.z);
+    v[3] = __uint_as_float(c.w);
+  }
+};
+
+template <>
+struct Elt<bf16_tag> {
+  static constexpr int VPC = 8;
+  static constexpr int BYTES = 2;
+  // a bf16 value is the upper half of a binary32: widening is a shift
+  __device__ __forceinline__ static void unpack(const uint4& c, float (&v)[8]) {
+    v[0] = __uint_as_float(c.x << 16);
+    v[1] = __uint_as_float(c.x & 0xffff0000u);
+    v[2] = __uint_as_float(c.y << 16);
+    v[3] = __uint_as_float(c.y & 0xffff0000u);
+    v[4] = __uint_as_float(c.z << 16);
+    v[5] = __uint_as_float(c.z & 0xffff0000u);
+    v[6] = __uint_as_float(c.w << 16);
+    v[7] = __uint_as_float(c.w & 0xffff0000u);
+  }
+};
+
+// fp32 -> storage type, round to nearest even (bf16 via the CUDA intrinsic)
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The activation A on the gate.  Units with z <= 0 are dead for both.
+// R-S+ on the positive side is z * sigmoid(z) = z / (1 + e^-z).
+__device__ __forceinline__ float activation(int act, float z) {
+  if (!(z > 0.f)) return 0.f;
+  if (act == 0) return z;
+  return z / (1.f + expf(-z));
+}
+
+}  // namespace sffn

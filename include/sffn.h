@@ -1,0 +1,156 @@
+/*
+ * sffn.h -- gate-first sparse gated-FFN forward (C ABI).
+ *
+ * One handle holds one FFN layer.  For each token x in R^D the forward pass
+ * computes the gate first, keeps only the live hidden units and reads only
+ * their rows of W3 and their columns of W2:
+ *
+ *     z = W1 x                (standard gate, W1 in R^{H x D}), or
+ *     z = U (V x)             (low-rank gate, U in R^{H x r}, V in R^{r x D})
+ *     S = { i : z_i > 0 }     (the live units; ReLU and R-S+ vanish for z <= 0)
+ *     y = sum_{i in S} W2[:, i] * A(z_i) * (W3[i, :] . x)
+ *
+ * which equals the dense gated FFN y = W2 (A(W1 x) .* (W3 x)) exactly in real
+ * arithmetic.  Sources: "Model casting: compute the gate, then skip most of
+ * the FFN" (ai.thesatyajit.com), sections "What an FFN actually computes"
+ * (the formula and the skip argument), "The 3x ceiling, and why W1 is always
+ * on" (the gate must run in full), "Model casting: make sparsity a target"
+ * (R-S+), "LoPA Gating: moving the ceiling" (W1 = G + UV; this library
+ * implements the UV part, with no G, no RMSNorm between V and U and the
+ * activation on the gate only).
+ *
+ * Conventions
+ *   - Every call returns SFFN_OK (0) or a negative SFFN_ERR_* code; the
+ *     thread-local sffn_last_error() then holds a one-line message.  No C++
+ *     exception crosses this boundary.
+ *   - Matrices are dense row-major.  x and y are [B, D] row-major.
+ *   - Arithmetic: products and sums in fp32 (FFMA, never TF32); the low-rank
+ *     vector t = V x and the products h_i stay fp32; y is rounded once to the
+ *     handle's dtype (round-to-nearest-even for bf16).
+ *   - The handle owns all library memory (packed weights, accumulators,
+ *     counters).  It is not thread-safe and must not be used by two streams
+ *     at once; concurrent layers need separate handles.
+ *   - Numerical sums over live units are accumulated across thread blocks with
+ *     fp32 atomics, so y can differ from run to run in its last bits; the live
+ *     set and the counts are deterministic.
+ */
+#ifndef SFFN_H
+#define SFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sffn_s* sffn_t;
+
+/* element type of W1/U, V, W3, W2, x and y */
+enum { SFFN_F32 = 0, SFFN_BF16 = 1 };
+
+/* activation A: ReLU, or R-S+ (z * sigmoid(z) for z >= 0, 0 for z < 0;
+   "Model casting: make sparsity a target") */
+enum { SFFN_ACT_RELU = 0, SFFN_ACT_RSP = 1 };
+
+enum {
+  SFFN_OK = 0,
+  SFFN_ERR_ARG = -1,      /* bad size, null pointer, unknown enum value      */
+  SFFN_ERR_ALIGN = -2,    /* a pointer is not 16-byte aligned                */
+  SFFN_ERR_DTYPE = -3,    /* dtype/shape combination not supported           */
+  SFFN_ERR_CUDA = -4,     /* a CUDA runtime call failed (message has details) */
+  SFFN_ERR_TIMEOUT = -5,  /* a device-side wait ran out of time; the kernel
+                             returned early and its outputs are invalid      */
+  SFFN_ERR_STATE = -6,    /* call out of order (e.g. forward before weights) */
+  SFFN_ERR_NOMEM = -7     /* device allocation failed                        */
+};
+
+/* limits of this build */
+#define SFFN_MAX_BATCH 128
+#define SFFN_MAX_D_BF16 4096
+#define SFFN_MAX_D_F32 2048
+
+/*
+ * Create a layer on the current CUDA device.
+ *   D      model width, D % 8 == 0, 8 <= D <= SFFN_MAX_D_BF16 (bf16) or
+ *          SFFN_MAX_D_F32 (f32)
+ *   H      hidden width (H' for the low-rank gate), any H >= 1
+ *   r      0 for the standard gate W1; r > 0 selects the low-rank gate U(Vx)
+ *          with rank r, r % 8 == 0, r <= D
+ *   act    SFFN_ACT_RELU or SFFN_ACT_RSP
+ *   dtype  SFFN_F32 or SFFN_BF16
+ * Returns NULL on error (see sffn_last_error()).  Allocates device memory:
+ * 3*H*D (+ r*D + H*r) elements of weights plus O(B_max * (D + r + H)) bytes of
+ * accumulators.
+ */
+sffn_t sffn_create(int D, int H, int r, int act, int dtype);
+
+/*
+ * Copy the layer's weights into the handle (host or device pointers, any
+ * alignment, dtype of the handle):
+ *   W1_or_U  W1[H, D] when r == 0, else U[H, r]
+ *   V        V[r, D] when r > 0, else ignored (may be NULL)
+ *   W3       W3[H, D]
+ *   W2       W2[D, H]  -- stored transposed (H-major) inside the handle so that
+ *            the column of a live unit is one contiguous row
+ * Work is issued on `stream` (a cudaStream_t, NULL = legacy default) and the
+ * call returns after it has completed.  The caller keeps ownership of its
+ * buffers.  May be called again to replace the weights.
+ */
+int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W3,
+                     const void* W2, void* stream);
+
+/*
+ * y[B, D] = FFN(x[B, D]) for 1 <= B <= SFFN_MAX_BATCH.  x and y are device
+ * pointers of the handle's dtype, 16-byte aligned, and must not overlap.  The
+ * call is asynchronous and stream-ordered on `stream`; y is fully overwritten.
+ * Successive forwards on one stream overlap the weight prefetch of the next
+ * call with the tail of the previous one (programmatic dependent launch); a
+ * forward still observes every write an earlier operation in the stream made
+ * to x.  Device-side failures (SFFN_ERR_TIMEOUT) surface at the next
+ * sffn_synchronize / sffn_active_counts / sffn_active_mask call.
+ */
+int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream);
+
+/*
+ * Number of live units |S_b| per token of the most recent forward, B values
+ * (B must equal that forward's batch).  Waits for that forward to finish.
+ */
+int sffn_active_counts(sffn_t h, int* counts_host, int B);
+
+/*
+ * Live flags of the most recent forward: mask_host[b*H + i] = 1 iff z_i > 0
+ * for token b, else 0 (B*H bytes).  Waits for that forward to finish.
+ */
+int sffn_active_mask(sffn_t h, uint8_t* mask_host, int B);
+
+/*
+ * Wait for all work this handle issued and report any device-side error
+ * recorded since the last check (the error word is cleared).
+ */
+int sffn_synchronize(sffn_t h);
+
+/* Release the handle and its device memory (waits for its pending work). */
+void sffn_destroy(sffn_t h);
+
+/* Static description of a status code. */
+const char* sffn_strerror(int code);
+
+/* The calling thread's message for its most recent failed call ("" if none). */
+const char* sffn_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int sffn_version(void);
+
+/*
+ * Test hook for failure detection: launch one block on `stream` that waits on
+ * a device flag nothing ever sets, with a limit of `limit_us` microseconds
+ * (1..1000000), after which it records SFFN_ERR_TIMEOUT in the handle's error
+ * word and returns.  The next sffn_synchronize reports it.  Faults nothing.
+ */
+int sffn_debug_timeout_probe(sffn_t h, int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SFFN_H */

@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import activation_sparse_gated_gb300 as sffn
+from activation_sparse_gated_gb300 import build as libbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sffn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sffn_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return sffn.load()
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(sffn.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", sffn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (sffn_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_constants_match_header():
+    text = open(HEADER).read()
+    for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
+                 "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
+                 "SFFN_ERR_STATE", "SFFN_ERR_NOMEM"):
+        m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
+        assert m and int(m.group(1)) == getattr(sffn, name), name
+    assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
+
+
+def test_host_only_calls(lib):
+    assert sffn.sffn_version() == 100
+    assert sffn.sffn_strerror(0) == "success"
+    assert "timed out" in sffn.sffn_strerror(sffn.SFFN_ERR_TIMEOUT)
+    assert sffn.sffn_strerror(12345) == "unknown status"
+
+
+def test_null_handle_is_rejected_on_host(lib):
+    # argument checks happen before any CUDA call
+    assert lib.sffn_forward(None, None, None, 1, None) == sffn.SFFN_ERR_ARG
+    assert lib.sffn_set_weights(None, None, None, None, None, None) == sffn.SFFN_ERR_ARG
+    assert lib.sffn_active_counts(None, None, 1) == sffn.SFFN_ERR_ARG
+    assert lib.sffn_synchronize(None) == sffn.SFFN_ERR_ARG
+    lib.sffn_destroy(None)
+
+
+@pytest.mark.parametrize("args", [(0, 64, 0, 0, 1), (12, 64, 0, 0, 1), (8192, 64, 0, 0, 1),
+                                  (4096, 64, 0, 0, 0), (64, 0, 0, 0, 1), (64, 64, 12, 0, 1),
+                                  (64, 64, 128, 0, 1), (64, 64, 0, 2, 1), (64, 64, 0, 0, 7)])
+def test_create_rejects_bad_shapes_before_touching_the_device(lib, args):
+    h = lib.sffn_create(*args)
+    assert not h
+    assert sffn.sffn_last_error()
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(sffn, "_lib", None)
+    with pytest.raises(ImportError):
+        sffn.load(str(tmp_path / "nope.so"))

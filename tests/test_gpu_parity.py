@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bars (from the method's parity contract):
+  * outputs: per token ||y - y*||_2 / ||y*||_2 <= 2e-2 for bf16, <= 1e-5 for fp32
+    (y* the oracle; a token with no live unit must give y == 0 exactly);
+  * live sets: identical to the oracle's {i : z_i > 0} for every unit with
+    |z_i| > 1e-2 (oracle z); counts differ by at most the units inside that band;
+  * integer/byte outputs (masks, counts) are self-consistent and deterministic.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import activation_sparse_gated_gb300 as sffn
+from activation_sparse_gated_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-5}
+BAND = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from activation_sparse_gated_gb300 import build
+    build.build()
+    sffn.load()
+    torch.cuda.set_device(0)
+
+
+def make_ffn(lw, act="relu"):
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, act, lw.dtype)
+    w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
+    ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
+    return ffn
+
+
+def reference(lw, x, act="relu"):
+    v = {k: syn.oracle_view(t) for k, t in lw.tensors().items()}
+    a = oracle.RELU if act == "relu" else oracle.RSP
+    dt = oracle.F32 if lw.dtype == "f32" else oracle.BF16
+    return oracle.ffn_dense(lw.D, lw.H, lw.r, a, dt, v["W1"], v["U"], v["V"], v["W3"], v["W2"],
+                            syn.oracle_view(x))
+
+
+def run_tokens(ffn, x, B=1):
+    """Forward x[n, D] in batches of B; returns y (float64), counts, masks."""
+    xd = x.cuda()
+    ys, counts, masks = [], [], []
+    for s in range(0, x.shape[0], B):
+        xb = xd[s:s + B].contiguous()
+        y = ffn(xb)
+        counts += ffn.active_counts(xb.shape[0])
+        masks.append(ffn.active_mask(xb.shape[0]))
+        ys.append(y.float().cpu().numpy().astype(np.float64))
+    return np.concatenate(ys), np.array(counts), np.concatenate(masks)
+
+
+def check(lw, x, y, counts, masks, act="relu", ref=None):
+    yref, z, n = ref if ref is not None else reference(lw, x, act)
+    tol = TOL[lw.dtype]
+    for b in range(x.shape[0]):
+        den = np.linalg.norm(yref[b])
+        if den == 0:
+            assert (y[b] == 0).all(), f"token {b}: no live unit but y != 0"
+        else:
+            err = np.linalg.norm(y[b] - yref[b]) / den
+            assert err <= tol, f"token {b}: relative L2 {err:.3e} > {tol}"
+        live_ref = z[b] > 0
+        sure = np.abs(z[b]) > BAND
+        gpu = masks[b].astype(bool)
+        bad = np.nonzero(sure & (gpu != live_ref))[0]
+        assert bad.size == 0, f"token {b}: live set differs at units {bad[:10]} (z={z[b][bad[:10]]})"
+        assert counts[b] == gpu.sum(), "count disagrees with the mask"
+        assert abs(int(counts[b]) - int(n[b])) <= int((~sure).sum())
+    return yref, z, n
+
+
+# --------------------------------------------------------------------------- named workloads
+def test_tiny_f32_workload_all_tokens():
+    name = "tiny-f32-D384-H1024"
+    lw = syn.workload_layers(name)[0]
+    x = syn.workload_tokens(name)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    _, _, n = check(lw, x, y, c, m)
+    assert 0.05 < n.mean() / lw.H < 0.15
+
+
+def test_standard_bf16_full_size_sample():
+    name = "std-bf16-D2560-H7168-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, 12)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+
+
+def test_lopa_bf16_full_size_sample():
+    name = "lopa-bf16-D2560-H9787-r400-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, 12)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("gate", ["standard", "lopa"])
+def test_sweep_shape_d4096(gate):
+    name = "sweep-bf16-D4096-H14336"
+    lw = syn.workload_layers(name, sets=1, gate=gate, s=0.75)[0]
+    x = syn.workload_tokens(name, 4)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+
+
+# --------------------------------------------------------------------------- edge cases
+def _dyadic_layer(rng, D, H, shift, dtype="f32", kmax=2):
+    k = lambda shape: torch.from_numpy(rng.integers(-kmax, kmax + 1, size=shape).astype(np.float32) / 8.0)  # noqa: E731
+    W1, W3, W2 = k((H, D)), k((H, D)), k((D, H))
+    W1[:, D - 1] = shift
+    cast = (lambda t: t) if dtype == "f32" else (lambda t: t.bfloat16())
+    return syn.LayerWeights(D, H, 0, dtype, cast(W1), None, None, cast(W3), cast(W2))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_exact_dyadic_case_is_bitwise(dtype):
+    # Weights in {-2..2}/8, x in {-1, 0, 1}, D = 16, H = 600: |z|, |u| <= 4 on a
+    # 1/8 grid, |h| <= 16 on a 1/64 grid, every partial sum of y is <= 600*0.25*16
+    # = 2400 on a 1/512 grid, i.e. < 2^24 grid steps: all fp32 arithmetic is
+    # exact in any order, so the GPU must equal the fp64 oracle bit for bit
+    # (after the one rounding to the output dtype).
+    rng = np.random.default_rng(0)
+    D, H = 16, 600
+    lw = _dyadic_layer(rng, D, H, -0.25, dtype)
+    xr = torch.from_numpy(rng.integers(-1, 2, size=(6, D)).astype(np.float32))
+    xr[:, D - 1] = 1.0
+    x = xr if dtype == "f32" else xr.bfloat16()
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    yref, z, n = reference(lw, x)
+    want = torch.from_numpy(yref).float()
+    if dtype == "bf16":
+        want = want.bfloat16().float()
+    assert np.array_equal(y, want.double().numpy())
+    assert np.array_equal(m.astype(bool), z > 0) and np.array_equal(c, n)
+    assert 0 < n.min() and n.max() < H
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift", [+20.0, -20.0])
+def test_all_live_and_none_live(dtype, shift):
+    rng = np.random.default_rng(1)
+    lw = _dyadic_layer(rng, 128, 500, shift, dtype, kmax=8)
+    x = syn.tokens(3, 128, dtype=dtype, seed=3)
+    x[:, :] = x.clamp(-1, 1)
+    x[:, 127] = 1.0
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+    assert (c == (500 if shift > 0 else 0)).all()
+    if shift < 0:
+        assert (y == 0).all()
+
+
+def test_one_live_unit():
+    D, H, i = 256, 2000, 1234
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=5, shift=-30.0)
+    W1 = lw.W1.clone()
+    W1[i, D - 1] = 30.0
+    lw.W1 = W1
+    x = syn.tokens(2, D, dtype="bf16", seed=6)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    yref, z, n = check(lw, x, y, c, m)
+    assert c.tolist() == [1, 1] and m[:, i].all()
+
+
+@pytest.mark.parametrize("D,H,r", [(8, 1, 0), (8, 37, 0), (64, 151, 0), (64, 152, 0), (64, 153, 0),
+                                   (256, 1000, 0), (1032, 777, 0), (4096, 300, 0),
+                                   (64, 999, 8), (512, 4097, 64), (4096, 3000, 640)])
+def test_ragged_shapes(D, H, r):
+    lw = (syn.standard_layer(D, H, dtype="bf16", seed=D + H, shift=-0.8) if r == 0 else
+          syn.lopa_layer(D, H, r, dtype="bf16", seed=D + H, shift=-0.8))
+    x = syn.tokens(3, D, dtype="bf16", seed=D)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("r", [0, 32])
+def test_rsp_activation(dtype, r):
+    D, H = 384, 1536
+    lw = (syn.standard_layer(D, H, dtype=dtype, seed=21) if r == 0 else
+          syn.lopa_layer(D, H, r, dtype=dtype, seed=21))
+    x = syn.tokens(4, D, dtype=dtype, seed=22)
+    ffn = make_ffn(lw, act="rsp")
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m, act="rsp")
+
+
+@pytest.mark.parametrize("B", [2, 4, 7])
+def test_batched_tokens(B):
+    lw = syn.standard_layer(512, 2048, dtype="bf16", seed=31)
+    x = syn.tokens(2 * B, 512, dtype="bf16", seed=32)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+def test_live_set_is_deterministic():
+    lw = syn.standard_layer(1024, 4096, dtype="bf16", seed=41)
+    x = syn.tokens(3, 1024, dtype="bf16", seed=42)
+    ffn = make_ffn(lw)
+    _, c1, m1 = run_tokens(ffn, x)
+    _, c2, m2 = run_tokens(ffn, x)
+    assert np.array_equal(c1, c2) and np.array_equal(m1, m2)
+
+
+# --------------------------------------------------------------------------- launch configuration of the benchmark
+def test_rotated_sets_in_a_cuda_graph_full_size():
+    """The benchmark's timed loop: rotated full-size layers, one forward each, graph-captured."""
+    name = "std-bf16-D2560-H7168-B1"
+    layers = syn.workload_layers(name, sets=3)
+    ffns = [make_ffn(lw) for lw in layers]
+    n = 6
+    x = syn.workload_tokens(name, n).cuda()
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for t in range(n):  # warm-up, eager
+            sffn.sffn_forward(ffns[t % 3].h, x[t], y[t], 1, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for t in range(n):
+            sffn.sffn_forward(ffns[t % 3].h, x[t], y[t], 1, s)
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    yc = y.float().cpu().numpy().astype(np.float64)
+    for t in range(n):
+        lw = layers[t % 3]
+        yref, z, nref = reference(lw, x[t:t + 1].cpu())
+        err = np.linalg.norm(yc[t] - yref[0]) / np.linalg.norm(yref[0])
+        assert err <= TOL["bf16"], (t, err)
+
+
+# --------------------------------------------------------------------------- failure detection and argument checks
+def test_timeout_probe_reports_and_leaves_the_handle_usable():
+    lw = syn.standard_layer(256, 512, dtype="bf16", seed=51)
+    ffn = make_ffn(lw)
+    sffn.sffn_debug_timeout_probe(ffn.h, 2000)   # 2 ms wait on a flag nothing sets
+    with pytest.raises(sffn.SffnError) as e:
+        ffn.synchronize()
+    assert e.value.code == sffn.SFFN_ERR_TIMEOUT
+    ffn.synchronize()                              # the error word was cleared
+    x = syn.tokens(2, 256, dtype="bf16", seed=52)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m)
+
+
+def test_argument_errors():
+    lw = syn.standard_layer(64, 128, dtype="bf16", seed=61)
+    ffn = sffn.SparseFFN(64, 128, 0, "relu", "bf16")
+    x = torch.zeros(2, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(ffn.h, x, y, 1)
+    assert e.value.code == sffn.SFFN_ERR_STATE
+    w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
+    ffn.set_weights(w["W1"], None, w["W3"], w["W2"])
+    for B in (0, 129):
+        with pytest.raises(sffn.SffnError) as e:
+            sffn.sffn_forward(ffn.h, x, y, B)
+        assert e.value.code == sffn.SFFN_ERR_ARG
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(ffn.h, x.data_ptr() + 2, y, 1)
+    assert e.value.code == sffn.SFFN_ERR_ALIGN
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.sffn_forward(ffn.h, x, x, 1)
+    assert e.value.code == sffn.SFFN_ERR_ARG
+    with pytest.raises(sffn.SffnError) as e:
+        ffn.active_counts(3)
+    assert e.value.code == sffn.SFFN_ERR_STATE
