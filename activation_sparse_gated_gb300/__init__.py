@@ -8,7 +8,7 @@ or fails to load, every entry point raises.
 The functions mirror the C ABI one to one (``sffn_create``, ``sffn_set_weights``,
 ``sffn_forward``, ``sffn_active_counts``, ``sffn_active_mask``,
 ``sffn_synchronize``, ``sffn_destroy``, ``sffn_strerror``, ``sffn_last_error``,
-``sffn_version``, ``sffn_debug_timeout_probe``).  Tensor arguments are passed by
+``sffn_version``, ``sffn_debug_timeout_probe``, ``sffn_forward_noalloc``).  Tensor arguments are passed by
 their data pointer; ``stream`` defaults to the current torch stream.
 ``SparseFFN`` wraps one handle.
 """
@@ -29,7 +29,7 @@ SFFN_MAX_BATCH = 128
 #: every symbol include/sffn.h declares
 EXPORTS = ("sffn_create", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
            "sffn_active_mask", "sffn_synchronize", "sffn_destroy", "sffn_strerror",
-           "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe")
+           "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc")
 
 _lib = None
 
@@ -62,6 +62,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sffn_last_error": (cp, []),
         "sffn_version": (ip, []),
         "sffn_debug_timeout_probe": (ip, [vp, ip, vp]),
+        "sffn_forward_noalloc": (ip, [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -150,6 +151,13 @@ def sffn_destroy(h):
 
 def sffn_debug_timeout_probe(h, limit_us: int, stream=None):
     return _check(load().sffn_debug_timeout_probe(h, limit_us, _stream(stream)))
+
+
+def sffn_forward_noalloc(W1, W3, W2t, x, y, counts, D: int, H: int, B: int, act: int, dtype: int,
+                         stream=None):
+    """Forward that allocates no device memory (see include/sffn.h); W2t is W2 transposed, [H, D]."""
+    return _check(load().sffn_forward_noalloc(_ptr(W1), _ptr(W3), _ptr(W2t), _ptr(x), _ptr(y),
+                                               _ptr(counts), D, H, B, act, dtype, _stream(stream)))
 
 
 class SparseFFN:

@@ -36,6 +36,8 @@ constexpr unsigned long long kTimeoutNs = 250000000ull;  // 250 ms per device-si
 
 }  // namespace
 
+void sffn::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 struct sffn_s {
   int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
   int device = 0, num_sms = 0;

@@ -52,6 +52,9 @@ cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int
 // Wait on a flag nothing sets for at most limit_ns, then record a timeout.
 cudaError_t launch_timeout_probe(int* ctrl, unsigned long long limit_ns, cudaStream_t s);
 
+// Store a message for sffn_last_error() on the calling thread.
+void set_last_error(const char* msg);
+
 // Launch helper: programmatic stream serialization on (the kernel may start
 // before its predecessor finishes and must call griddepcontrol.wait first).
 template <typename... KArgs, typename... Args>

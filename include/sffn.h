@@ -150,6 +150,31 @@ int sffn_version(void);
  */
 int sffn_debug_timeout_probe(sffn_t h, int limit_us, void* stream);
 
+/*
+ * Forward without any device allocation, for callers that cannot call
+ * cudaMalloc (a runtime that owns all device memory through its own arena, code
+ * on a latency path where an allocation would stall the device, a host that
+ * only lends out buffers it owns).  The pages have no counterpart: this is a
+ * packaging of the same standard-gate forward as sffn_forward.
+ *   W1, W3   [H, D] row-major device pointers
+ *   W2t      W2 transposed, [H, D] row-major (row i = column i of W2), device
+ *   x, y     [B, D] device pointers, must not overlap; y fully overwritten
+ *   counts   optional device int[B] receiving |S_b| per token, or NULL
+ *   D, H, B, act, dtype as for sffn_create / sffn_forward (standard gate only)
+ * All pointers 16-byte aligned.  The kernels' scratch (an fp32 accumulator of
+ * D floats, the block ticket, an error word, count accumulators) is one static
+ * device array of 17,664 bytes inside the library, so D is limited to 4096
+ * (bf16) / 2048 (f32); larger D is rejected with SFFN_ERR_ARG and a message.
+ * The first call on a device looks up that array's address and sets kernel
+ * attributes for the device, so make it before any stream capture.  Every
+ * call clears the scratch it needs on `stream` and then launches; calls that
+ * overlap on the GPU (different streams, or several threads) share the one
+ * array and race, so serialise them.  Device-side timeouts are not reported
+ * by this entry point.  Returns SFFN_OK once the work is enqueued.
+ */
+int sffn_forward_noalloc(const void* W1, const void* W3, const void* W2t, const void* x, void* y,
+                         int* counts, int D, int H, int B, int act, int dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,3 +76,12 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sffn, "_lib", None)
     with pytest.raises(ImportError):
         sffn.load(str(tmp_path / "nope.so"))
+
+
+def test_noalloc_rejects_bad_sizes_on_host(lib):
+    # size checks come before any CUDA call, so they work without a GPU
+    for D, H, B, dt in ((8192, 8, 1, 1), (4096, 8, 1, 0), (12, 8, 1, 1), (64, 0, 1, 1), (64, 8, 0, 1),
+                        (64, 8, 129, 1)):
+        rc = lib.sffn_forward_noalloc(16, 16, 16, 16, 4096, None, D, H, B, 0, dt, None)
+        assert rc == sffn.SFFN_ERR_ARG, (D, H, B, dt)
+        assert "sffn_forward_noalloc" in sffn.sffn_last_error()
