@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -57,6 +58,8 @@ struct sffn_s {
   bool ev_valid = false;
   int b1_grid = 0, b1_ns1 = 0, b1_ns2 = 0;
   size_t b1_smem = 0;
+  int stream_grid = 0;  // blocks of the streaming standard-gate kernel
+  int stream_rows_cap = 0, stream_pref_rows = 0;
 };
 
 namespace {
@@ -214,6 +217,19 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
     return nullptr;
   }
   if ((e = ffn_b1_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+  {
+    // blocks per SM of the streaming kernel (1 leaves room for the next call's blocks)
+    int mult = 1;
+    if (const char* env = std::getenv("SFFN_STREAM_BLOCKS_PER_SM")) mult = std::max(1, std::min(4, std::atoi(env)));
+    h->stream_grid = std::min(h->num_sms * mult, H);
+    h->stream_rows_cap = (H + h->stream_grid - 1) / h->stream_grid;
+    // gate rows prefetched into shared memory: about 96 KB per block keeps two
+    // blocks (this call's and the next call's) resident on an SM
+    const size_t row_bytes = (size_t)D * h->elt;
+    h->stream_pref_rows = std::min(h->stream_rows_cap, (int)((96u * 1024u) / row_bytes));
+    if ((e = ffn_b1_stream_prepare(h->max_smem)))
+      return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+  }
   if ((e = cudaDeviceSynchronize())) return bail(SFFN_ERR_CUDA, "cudaDeviceSynchronize", e);
   return h;
 }
@@ -272,8 +288,13 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.ns2 = h->b1_ns2;
     p.act = h->act;
     p.count_slot = b;
+    p.rows_cap = h->stream_rows_cap;
+    p.pref_rows = h->stream_pref_rows;
     p.timeout_ns = kTimeoutNs;
-    SFFN_CUDA(launch_ffn_b1(p, h->dtype, lopa, h->b1_grid, h->b1_smem, s));
+    if (lopa)
+      SFFN_CUDA(launch_ffn_b1(p, h->dtype, true, h->b1_grid, h->b1_smem, s));
+    else
+      SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, h->stream_grid, s));
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SFFN_CUDA(cudaStreamIsCapturing(s, &cs));

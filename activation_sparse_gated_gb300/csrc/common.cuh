@@ -18,6 +18,9 @@ constexpr int CTRL_ERR = 1;      // device error word (sticky until read)
 constexpr int CTRL_PROBE = 2;    // flag the timeout probe waits on (never set)
 constexpr int CTRL_COUNT = 4;    // [B_max] live-count accumulators
 constexpr int CTRL_INTS = 4 + 128;
+// the streaming kernel spreads its cross-block sum over this many fp32 copies
+// of the accumulator (a handle's accumulator holds at least this many rows)
+constexpr int YACC_COPIES = 4;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
