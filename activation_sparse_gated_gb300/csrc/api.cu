@@ -59,7 +59,8 @@ struct sffn_s {
   int b1_grid = 0, b1_ns1 = 0, b1_ns2 = 0;
   size_t b1_smem = 0;
   int stream_grid = 0;  // blocks of the streaming standard-gate kernel
-  int stream_rows_cap = 0, stream_pref_rows = 0;
+  int stream_rows_cap = 0;
+  StreamPlan stream_plan;
 };
 
 namespace {
@@ -223,10 +224,16 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
     if (const char* env = std::getenv("SFFN_STREAM_BLOCKS_PER_SM")) mult = std::max(1, std::min(4, std::atoi(env)));
     h->stream_grid = std::min(h->num_sms * mult, H);
     h->stream_rows_cap = (H + h->stream_grid - 1) / h->stream_grid;
-    // gate rows prefetched into shared memory: about 96 KB per block keeps two
-    // blocks (this call's and the next call's) resident on an SM
-    const size_t row_bytes = (size_t)D * h->elt;
-    h->stream_pref_rows = std::min(h->stream_rows_cap, (int)((96u * 1024u) / row_bytes));
+    h->stream_plan = plan_ffn_b1_stream(D, gate_k(h), h->elt, r > 0, h->stream_rows_cap);
+    if (h->stream_plan.smem > h->max_smem) {
+      fail(SFFN_ERR_DTYPE, "shared-memory plan of the streaming kernel exceeds the device limit");
+      char keep[sizeof g_msg];
+      std::memcpy(keep, g_msg, sizeof keep);
+      release(h);
+      delete h;
+      std::memcpy(g_msg, keep, sizeof keep);
+      return nullptr;
+    }
     if ((e = ffn_b1_stream_prepare(h->max_smem)))
       return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   }
@@ -289,12 +296,10 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.act = h->act;
     p.count_slot = b;
     p.rows_cap = h->stream_rows_cap;
-    p.pref_rows = h->stream_pref_rows;
+    p.pref_rows = h->stream_plan.pref_rows;
+    p.gather_rows = h->stream_plan.gather_rows;
     p.timeout_ns = kTimeoutNs;
-    if (lopa)
-      SFFN_CUDA(launch_ffn_b1(p, h->dtype, true, h->b1_grid, h->b1_smem, s));
-    else
-      SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, h->stream_grid, s));
+    SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, lopa, h->stream_grid, h->stream_plan.smem, s));
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SFFN_CUDA(cudaStreamIsCapturing(s, &cs));

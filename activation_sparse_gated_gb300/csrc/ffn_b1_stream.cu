@@ -1,35 +1,40 @@
-// ffn_b1_stream.cu -- fused single-token gate-first sparse FFN, standard gate,
-// streaming form.
+// ffn_b1_stream.cu -- fused single-token gate-first sparse FFN (standard or
+// low-rank gate), streaming form.
 //
 // The method ("Model casting: compute the gate, then skip most of the FFN",
 // sections "What an FFN actually computes" and "The 3x ceiling, and why W1 is
-// always on"): compute the whole gate z = W1 x, keep S = {i : z_i > 0}, and for
-// those units only read row i of W3 and column i of W2 (row i of W2^T):
+// always on"): compute the whole gate z, keep S = {i : z_i > 0}, and for those
+// units only read row i of W3 and column i of W2 (row i of W2^T):
 //     y = sum_{i in S} W2^T[i, :] * A(z_i) * (W3[i, :] . x).
+// Standard gate: z = W1 x.  Low-rank gate ("LoPA Gating: moving the ceiling"):
+// z = U t with t = V x computed in fp32 by the preceding kernel (lopa_t.cu).
 //
-// GB300 mapping.  A call moves ~44 MB (D=2560, H=7168, 90 % sparsity) in a few
-// microseconds, so fixed costs (launch gap, ramp-up, reduction tail) matter as
-// much as streaming speed.  The kernel is therefore kept light -- 512 threads,
-// at most 64 registers, ~15 KB of shared memory -- so that the next call's
-// blocks (launched early by programmatic dependent launch) sit on the same SMs
-// and start pulling their weights while this call finishes.
-//   * 16 warps per block, each block owning a contiguous slice of units.  A warp
-//     streams its gate rows as half-row pieces through two register buffers
-//     (one piece multiplied with x from shared memory while the next is in
-//     flight), so loads stay outstanding continuously instead of in waves.
-//     The first pieces are requested before the dependency wait: weights
-//     never depend on earlier kernels.
-//   * A live unit never stalls the gate stream: lane 0 appends (unit, A(z)) to
-//     the block's shared list (a shared atomic counter: the compaction) and
-//     asks the copy engine to prefetch the unit's W3 row and W2^T row into L2.
-//   * After the gate stream, warps take list entries and compute
-//     h_i = A(z_i) (W3[i,:] . x) from L2; then every thread owns whole 16-byte
-//     chunks of y and accumulates sum_i h_i W2^T[i, chunk] in registers.
-//   * Blocks add their partial y into a per-handle fp32 accumulator with
-//     128-bit atomics (each block starting at a different offset to spread
-//     same-address traffic); the last block (ticket counter) rounds y, clears
-//     the accumulator and publishes the live count.
+// GB300 mapping.  A call moves tens of MB in a few microseconds and consecutive
+// calls are stream-ordered, so what counts is how much of a call's weight
+// traffic happens before it may start (the dependency wait) and how short the
+// chain of dependent memory round trips after its gate is.
+//   * The kernel is light (512 threads, <= 64 registers, ~100 KB of shared
+//     memory) so the next call's blocks, launched early by programmatic
+//     dependent launch, co-reside with this call's and prefetch their gate
+//     rows while this call finishes.
+//   * Before the wait, a block copies the first rows of its gate slice into
+//     shared memory (16-byte cp.async, ~96 KB, the whole slice for the
+//     low-rank gate) and every warp requests the first two pieces of its
+//     streamed rows into registers.  After the wait, warps stream the rest as
+//     pieces through two register buffers (one multiplied while the next is in
+//     flight), so loads stay outstanding continuously.
+//   * A live unit goes on the block's list (shared atomic counter: the
+//     compaction) and its W3 and W2^T rows are prefetched into L2 at once.
+//   * After the gate: the live units' W3 rows are copied into the now free
+//     shared area while every warp requests its W2^T slices of them -- one
+//     round trip; h_i = A(z_i) (W3[i,:] . x) from shared memory; warp w then
+//     folds its own slice of y over the list in registers (no atomics).
+//   * Blocks add their partial y into one of four fp32 accumulator copies
+//     (fewer blocks per address) with 128-bit atomics; the last block (ticket)
+//     sums the copies, rounds y, clears the copies and publishes the count.
 // There are no spin-waits in this kernel.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -100,6 +105,35 @@ __device__ __forceinline__ float dot_piece(const uint4 (&w)[PIECE], const uint4*
   return a0 + a1;
 }
 
+// One 16-byte gate chunk c dotted with the fp32 low-rank vector t.
+template <typename E>
+__device__ __forceinline__ void dot_chunk_t(const uint4& w, const float* ts, int c, float& a0, float& a1) {
+  constexpr int VPC = E::VPC;
+  float wf[VPC];
+  E::unpack(w, wf);
+  const float4* t4 = reinterpret_cast<const float4*>(ts + c * VPC);
+#pragma unroll
+  for (int v = 0; v < VPC; v += 4) {
+    const float4 tv = t4[v / 4];
+    a0 = fmaf(wf[v], tv.x, a0);
+    a1 = fmaf(wf[v + 1], tv.y, a1);
+    a0 = fmaf(wf[v + 2], tv.z, a0);
+    a1 = fmaf(wf[v + 3], tv.w, a1);
+  }
+}
+
+template <typename E>
+__device__ __forceinline__ float dot_piece_t(const uint4 (&w)[PIECE], const float* ts, int pc, int lane,
+                                             int nch) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < PIECE; ++k) {
+    const int c = pc * 32 * PIECE + lane + 32 * k;
+    if (c < nch) dot_chunk_t<E>(w[k], ts, c, a0, a1);
+  }
+  return a0 + a1;
+}
+
 // u = row . x over all pieces (the first piece already in `w` if `have0`)
 template <typename E>
 __device__ __forceinline__ float row_dot(uint4 (&w)[PIECE], const uint4* row, const uint4* xs, int lane,
@@ -112,27 +146,33 @@ __device__ __forceinline__ float row_dot(uint4 (&w)[PIECE], const uint4* row, co
   return warp_sum(acc);
 }
 
-template <typename T>
+template <typename T, bool LOPA>
 __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) {
   using E = Elt<T>;
   constexpr int VPC = E::VPC;
   extern __shared__ __align__(16) uint8_t smem[];
   const int D = p.D;
-  const int nch = D * E::BYTES / 16;  // 16-byte chunks of a row
-  const int npieces = (nch + 32 * PIECE - 1) / (32 * PIECE);
+  const int nch = D * E::BYTES / 16;          // 16-byte chunks of a D-row (x, W3, W2^T)
+  const int nchg = p.gate_k * E::BYTES / 16;  // ... of a gate row (W1 or U)
+  const int npg = (nchg + 32 * PIECE - 1) / (32 * PIECE);
   const int row0 = (int)(((long long)blockIdx.x * p.H) / gridDim.x);
   const int row1 = (int)(((long long)(blockIdx.x + 1) * p.H) / gridDim.x);
   const int cap = p.rows_cap;  // >= units of this block
-  // shared: x | live list (unit, A(z), h) | counters | prefetched gate rows
-  uint4* xs = reinterpret_cast<uint4*>(smem);
-  int* l_unit = reinterpret_cast<int*>(smem + align16((size_t)nch * 16));  // [cap]
-  float* l_a = reinterpret_cast<float*>(l_unit + cap);                      // [cap]
-  float* l_h = l_a + cap;                                                   // [cap]
+  // shared: x | t (low-rank gate) | live list (unit, A(z), h) | counters | prefetch / gather area
+  uint8_t* sp = smem;
+  uint4* xs = reinterpret_cast<uint4*>(sp);
+  sp += align16((size_t)nch * 16);
+  float* ts = reinterpret_cast<float*>(sp);
+  sp += LOPA ? align16((size_t)p.gate_k * 4) : 0;
+  int* l_unit = reinterpret_cast<int*>(sp);
+  float* l_a = reinterpret_cast<float*>(l_unit + cap);
+  float* l_h = l_a + cap;
   int* misc = reinterpret_cast<int*>(l_h + cap);  // 0: live count, 1: last-block flag
-  uint4* srows = reinterpret_cast<uint4*>(smem + align16((size_t)nch * 16) + align16((size_t)cap * 12 + 16));
+  sp += align16((size_t)cap * 12 + 16);
+  uint4* srows = reinterpret_cast<uint4*>(sp);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint4* W1 = static_cast<const uint4*>(p.gate_w);
+  const uint4* G = static_cast<const uint4*>(p.gate_w);
   const uint4* W3 = static_cast<const uint4*>(p.W3);
   const uint4* W2t = static_cast<const uint4*>(p.W2t);
   float4* ya = reinterpret_cast<float4*>(p.yacc);
@@ -142,30 +182,31 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     misc[0] = 0;
   }
 
-  // ---- prefetch before the dependency wait (weights never depend on earlier
-  // kernels).  The block's first R rows are copied into shared memory with
-  // 16-byte asynchronous copies; the rest are streamed by the warps (rows
-  // row0 + R + warp + SW*k) as pieces, npieces per row, alternating between two
-  // register buffers -- one piece multiplied with x while the next is in flight
-  // -- and the first two pieces are requested now.  x is prefetched into L2,
-  // which is harmless whatever the previous kernel does to it.
+  // ---- before the dependency wait (weights never depend on earlier kernels):
+  // the block's first R gate rows go to shared memory, every warp requests the
+  // first two pieces of its streamed rows (row0 + R + warp + SW*k), and x is
+  // prefetched into L2 (harmless whatever the previous kernel does to it).
   const int nrows = row1 - row0;
   const int R = min(p.pref_rows, nrows);
   {
-    const uint4* src = W1 + (size_t)row0 * nch;
-    for (int i = tid; i < R * nch; i += ST) cp_async16(srows + i, src + i);
+    const uint4* src = G + (size_t)row0 * nchg;
+    for (int i = tid; i < R * nchg; i += ST) cp_async16(srows + i, src + i);
     cp_async_commit();
   }
   const int my_rows = (nrows - R - warp + SW - 1) / SW;
-  const int n_seq = my_rows > 0 ? my_rows * npieces : 0;
-  auto seq_row = [&](int sidx) { return W1 + (size_t)(row0 + R + warp + (sidx / npieces) * SW) * nch; };
+  const int n_seq = my_rows > 0 ? my_rows * npg : 0;
+  auto seq_row = [&](int sidx) { return G + (size_t)(row0 + R + warp + (sidx / npg) * SW) * nchg; };
   uint4 wa[PIECE], wb[PIECE];
-  if (n_seq > 0) load_piece(wa, seq_row(0), 0, lane, nch);
-  if (n_seq > 1) load_piece(wb, seq_row(1), 1 % npieces, lane, nch);
+  if (n_seq > 0) load_piece(wa, seq_row(0), 0, lane, nchg);
+  if (n_seq > 1) load_piece(wb, seq_row(1), 1 % npg, lane, nchg);
   if (tid == 0) prefetch_l2(p.x, (uint32_t)nch * 16u);
 
-  pdl_wait();  // x, the outputs and the accumulators follow stream order
+  pdl_wait();  // x, t, the outputs and the accumulators follow stream order
   for (int i = tid; i < nch; i += ST) xs[i] = __ldcg(static_cast<const uint4*>(p.x) + i);
+  if constexpr (LOPA) {
+    for (int i = tid; i < p.gate_k / 4; i += ST)
+      reinterpret_cast<float4*>(ts)[i] = __ldcg(reinterpret_cast<const float4*>(p.t) + i);
+  }
   cp_async_wait_all();
   __syncthreads();
 
@@ -186,36 +227,43 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   };
   // gate rows already in shared memory
   for (int i = warp; i < R; i += SW) {
-    const uint4* r = srows + (size_t)i * nch;
+    const uint4* r = srows + (size_t)i * nchg;
     float a0 = 0.f, a1 = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      float wf[VPC], xf[VPC];
-      E::unpack(r[c], wf);
-      E::unpack(xs[c], xf);
+    for (int c = lane; c < nchg; c += 32) {
+      if constexpr (LOPA) {
+        dot_chunk_t<E>(r[c], ts, c, a0, a1);
+      } else {
+        float wf[VPC], xf[VPC];
+        E::unpack(r[c], wf);
+        E::unpack(xs[c], xf);
 #pragma unroll
-      for (int v = 0; v < VPC; v += 2) {
-        a0 = fmaf(wf[v], xf[v], a0);
-        a1 = fmaf(wf[v + 1], xf[v + 1], a1);
+        for (int v = 0; v < VPC; v += 2) {
+          a0 = fmaf(wf[v], xf[v], a0);
+          a1 = fmaf(wf[v + 1], xf[v + 1], a1);
+        }
       }
     }
     decide(row0 + i, warp_sum(a0 + a1));
   }
   // streamed gate rows
   float acc = 0.f;
-  auto finish_piece = [&](int sidx) {
-    if (sidx % npieces != npieces - 1) return;
-    const float z = warp_sum(acc);
-    acc = 0.f;
-    decide(row0 + R + warp + (sidx / npieces) * SW, z);
+  auto consume = [&](const uint4(&w)[PIECE], int sidx) {
+    if constexpr (LOPA)
+      acc += dot_piece_t<E>(w, ts, sidx % npg, lane, nchg);
+    else
+      acc += dot_piece<E>(w, xs, sidx % npg, lane, nchg);
+    if (sidx % npg == npg - 1) {
+      const float z = warp_sum(acc);
+      acc = 0.f;
+      decide(row0 + R + warp + (sidx / npg) * SW, z);
+    }
   };
   for (int sidx = 0; sidx < n_seq; sidx += 2) {
-    acc += dot_piece<E>(wa, xs, sidx % npieces, lane, nch);
-    finish_piece(sidx);
-    if (sidx + 2 < n_seq) load_piece(wa, seq_row(sidx + 2), (sidx + 2) % npieces, lane, nch);
+    consume(wa, sidx);
+    if (sidx + 2 < n_seq) load_piece(wa, seq_row(sidx + 2), (sidx + 2) % npg, lane, nchg);
     if (sidx + 1 < n_seq) {
-      acc += dot_piece<E>(wb, xs, (sidx + 1) % npieces, lane, nch);
-      finish_piece(sidx + 1);
-      if (sidx + 3 < n_seq) load_piece(wb, seq_row(sidx + 3), (sidx + 3) % npieces, lane, nch);
+      consume(wb, sidx + 1);
+      if (sidx + 3 < n_seq) load_piece(wb, seq_row(sidx + 3), (sidx + 3) % npg, lane, nchg);
     }
   }
   __syncthreads();
@@ -225,15 +273,15 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   // few round trips as possible.  Warp w owns chunks [cs0, cs0 + cs_n) of y,
   // lane l chunk cs0 + l (a slice has at most 32 chunks because a row has at
   // most 512).  Per batch of up to RB live units: their W3 rows are copied into
-  // the (now free) shared prefetch area while every warp requests its W2^T
-  // slices of the first eight units of the batch; then h = A(z) (W3 . x) from
-  // shared memory, and y_slice += h W2^T[unit, slice] in registers.
+  // the (now free) shared area while every warp requests its W2^T slices of the
+  // first eight units of the batch; then h = A(z) (W3 . x) from shared memory,
+  // and y_slice += h W2^T[unit, slice] in registers.
   const int per = (nch + SW - 1) / SW;
   const int cs0 = warp * per;
   const int cs_n = min(per, nch - cs0);  // may be <= 0 for tiny D
   const bool owns = lane < cs_n;
   const uint4* col = W2t + cs0 + lane;
-  const int RB = max(1, p.pref_rows);
+  const int RB = p.gather_rows;
   float yr[VPC];
 #pragma unroll
   for (int v = 0; v < VPC; ++v) yr[v] = 0.f;
@@ -346,30 +394,39 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 
 }  // namespace
 
-size_t ffn_b1_stream_smem_bytes(int D, int elt_bytes, int rows_cap, int pref_rows) {
-  return align16((size_t)D * elt_bytes) + align16((size_t)rows_cap * 12 + 16) +
-         (size_t)pref_rows * D * elt_bytes;
+StreamPlan plan_ffn_b1_stream(int D, int gate_k, int elt_bytes, bool lopa, int rows_cap) {
+  StreamPlan pl;
+  const size_t grow = (size_t)gate_k * elt_bytes, row = (size_t)D * elt_bytes;
+  // ~96 KB of gate rows per block keeps two blocks resident on an SM
+  pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, (96u * 1024u) / grow);
+  const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 8) * row);
+  pl.gather_rows = (int)std::max<size_t>(1, area / row);
+  pl.smem = align16((size_t)D * elt_bytes) + (lopa ? align16((size_t)gate_k * 4) : 0) +
+            align16((size_t)rows_cap * 12 + 16) + area;
+  return pl;
 }
 
 cudaError_t ffn_b1_stream_prepare(size_t max_smem) {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(ffn_b1_stream_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)max_smem)))
-    return e;
-  if ((e = cudaFuncSetAttribute(ffn_b1_stream_kernel<bf16_tag>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)max_smem)))
-    return e;
-  if ((e = cudaFuncSetAttribute(ffn_b1_stream_kernel<float>, cudaFuncAttributePreferredSharedMemoryCarveout, 100)))
-    return e;
-  return cudaFuncSetAttribute(ffn_b1_stream_kernel<bf16_tag>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  void (*ks[4])(const B1Params) = {ffn_b1_stream_kernel<float, false>, ffn_b1_stream_kernel<float, true>,
+                                   ffn_b1_stream_kernel<bf16_tag, false>, ffn_b1_stream_kernel<bf16_tag, true>};
+  for (auto k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 int ffn_b1_stream_threads() { return ST; }
 
-cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, int grid, cudaStream_t s) {
-  const size_t smem = ffn_b1_stream_smem_bytes(p.D, dtype == 0 ? 4 : 2, p.rows_cap, p.pref_rows);
-  if (dtype == 0) return launch_pdl(ffn_b1_stream_kernel<float>, dim3(grid), dim3(ST), smem, s, p);
-  return launch_pdl(ffn_b1_stream_kernel<bf16_tag>, dim3(grid), dim3(ST), smem, s, p);
+cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
+                                 cudaStream_t s) {
+  const dim3 g(grid), b(ST);
+  if (dtype == 0)
+    return lopa ? launch_pdl(ffn_b1_stream_kernel<float, true>, g, b, smem, s, p)
+                : launch_pdl(ffn_b1_stream_kernel<float, false>, g, b, smem, s, p);
+  return lopa ? launch_pdl(ffn_b1_stream_kernel<bf16_tag, true>, g, b, smem, s, p)
+              : launch_pdl(ffn_b1_stream_kernel<bf16_tag, false>, g, b, smem, s, p);
 }
 
 }  // namespace sffn

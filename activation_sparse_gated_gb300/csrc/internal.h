@@ -26,6 +26,7 @@ struct B1Params {
   int count_slot;         // index of this token's live-count accumulator
   int rows_cap;           // streaming kernel: max units per block (live-list capacity)
   int pref_rows;          // streaming kernel: gate rows per block prefetched into shared memory
+  int gather_rows;        // streaming kernel: W3 rows per gather batch (shared area / row)
   unsigned long long timeout_ns;
 };
 
@@ -43,12 +44,18 @@ cudaError_t ffn_b1_prepare(size_t max_smem);
 cudaError_t launch_ffn_b1(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
                           cudaStream_t s);
 
-// Streaming form of the fused forward for the standard gate (16 warps, no
-// shared ring, no spin-waits); grid = blocks, each owning a slice of units.
-size_t ffn_b1_stream_smem_bytes(int D, int elt_bytes, int rows_cap, int pref_rows);
+// Streaming form of the fused forward (16 warps, no spin-waits); grid =
+// blocks, each owning a slice of units.  The plan fixes the shared-memory
+// prefetch depth, the gather batch and the dynamic shared-memory size.
+struct StreamPlan {
+  int pref_rows = 0, gather_rows = 1;
+  size_t smem = 0;
+};
+StreamPlan plan_ffn_b1_stream(int D, int gate_k, int elt_bytes, bool lopa, int rows_cap);
 cudaError_t ffn_b1_stream_prepare(size_t max_smem);
 int ffn_b1_stream_threads();
-cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, int grid, cudaStream_t s);
+cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
+                                 cudaStream_t s);
 
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,

@@ -18,7 +18,7 @@ namespace sffn {
 namespace {
 
 constexpr int T_WARPS = 8;
-constexpr int T_PF = 16;  // 16-byte chunks of the V row prefetched per lane
+constexpr int T_PF = 10;  // 16-byte chunks of the V row prefetched per lane (a whole bf16 row at D=2560)
 
 template <typename T>
 __global__ void __launch_bounds__(T_WARPS * 32) lopa_t_kernel(const void* __restrict__ V,

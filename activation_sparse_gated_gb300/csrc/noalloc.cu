@@ -153,6 +153,7 @@ extern "C" int sffn_forward_noalloc(const void* W1, const void* W3, const void* 
     p.count_slot = b;
     p.rows_cap = 0;
     p.pref_rows = 0;
+    p.gather_rows = 1;
     p.timeout_ns = 250000000ull;
     if ((e = launch_ffn_b1(p, dtype, false, grid, smem, s)) != cudaSuccess)
       return fail(SFFN_ERR_CUDA, "kernel launch", e);
