@@ -61,6 +61,7 @@ struct sffn_s {
   int stream_grid = 0;  // blocks of the streaming standard-gate kernel
   int stream_rows_cap = 0;
   StreamPlan stream_plan;
+  BatchPlan batch_plan;  // groups of up to 8 tokens
 };
 
 namespace {
@@ -234,6 +235,17 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
       std::memcpy(g_msg, keep, sizeof keep);
       return nullptr;
     }
+    h->batch_plan = plan_ffn_batch(D, gate_k(h), h->elt, r > 0, h->stream_rows_cap, 8);
+    if (h->batch_plan.smem > h->max_smem) {
+      fail(SFFN_ERR_DTYPE, "shared-memory plan of the batched kernel exceeds the device limit");
+      char keep[sizeof g_msg];
+      std::memcpy(keep, g_msg, sizeof keep);
+      release(h);
+      delete h;
+      std::memcpy(g_msg, keep, sizeof keep);
+      return nullptr;
+    }
+    if ((e = ffn_batch_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     if ((e = ffn_b1_stream_prepare(h->max_smem)))
       return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   }
@@ -276,7 +288,9 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   const size_t row = (size_t)h->D * h->elt;
 
   if (lopa) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
-  for (int b = 0; b < B; ++b) {
+  // tokens in groups of up to 8: one pass over the weights per group
+  for (int b = 0; b < B;) {
+    const int nb = std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;
     p.W3 = h->W3;
@@ -296,10 +310,17 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.act = h->act;
     p.count_slot = b;
     p.rows_cap = h->stream_rows_cap;
-    p.pref_rows = h->stream_plan.pref_rows;
-    p.gather_rows = h->stream_plan.gather_rows;
     p.timeout_ns = kTimeoutNs;
-    SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, lopa, h->stream_grid, h->stream_plan.smem, s));
+    if (nb == 1) {
+      p.pref_rows = h->stream_plan.pref_rows;
+      p.gather_rows = h->stream_plan.gather_rows;
+      SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, lopa, h->stream_grid, h->stream_plan.smem, s));
+    } else {
+      p.pref_rows = h->batch_plan.pref_rows;
+      p.gather_rows = h->batch_plan.gather_rows;
+      SFFN_CUDA(launch_ffn_batch(p, nb, h->dtype, lopa, h->stream_grid, h->batch_plan.smem, s));
+    }
+    b += nb;
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   SFFN_CUDA(cudaStreamIsCapturing(s, &cs));

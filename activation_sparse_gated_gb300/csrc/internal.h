@@ -57,6 +57,17 @@ int ffn_b1_stream_threads();
 cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
                                  cudaStream_t s);
 
+// Small-batch form (2..8 tokens per launch, CUDA cores): one pass over the
+// gate slice serves every token; gathers follow the union of live sets.
+struct BatchPlan {
+  int pref_rows = 0, gather_rows = 1;
+  size_t smem = 0;
+};
+BatchPlan plan_ffn_batch(int D, int gate_k, int elt_bytes, bool lopa, int rows_cap, int nb_max);
+cudaError_t ffn_batch_prepare(size_t max_smem);
+cudaError_t launch_ffn_batch(const B1Params& p, int nb, int dtype, bool lopa, int grid, size_t smem,
+                             cudaStream_t s);
+
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,
                           cudaStream_t s);

@@ -204,12 +204,50 @@ def test_rsp_activation(dtype, r):
     check(lw, x, y, c, m, act="rsp")
 
 
-@pytest.mark.parametrize("B", [2, 4, 7])
+@pytest.mark.parametrize("B", [2, 4, 7, 8, 9, 17])
 def test_batched_tokens(B):
     lw = syn.standard_layer(512, 2048, dtype="bf16", seed=31)
     x = syn.tokens(2 * B, 512, dtype="bf16", seed=32)
     ffn = make_ffn(lw)
     y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("B", [3, 8, 11])
+def test_batched_lopa(B):
+    lw = syn.lopa_layer(768, 2600, 96, dtype="bf16", seed=33)
+    x = syn.tokens(B, 768, dtype="bf16", seed=34)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("act", ["relu", "rsp"])
+def test_batched_f32(act):
+    lw = syn.standard_layer(384, 1024, dtype="f32", seed=35)
+    x = syn.tokens(6, 384, dtype="f32", seed=36)
+    ffn = make_ffn(lw, act=act)
+    y, c, m = run_tokens(ffn, x, B=6)
+    check(lw, x, y, c, m, act=act)
+
+
+@pytest.mark.parametrize("B", [16, 64])
+def test_batched_workload_full_size(B):
+    name = "std-bf16-D2560-H7168-batched"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, B)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("gate", ["standard", "lopa"])
+def test_sweep_batch8_d4096(gate):
+    name = "sweep-bf16-D4096-H14336"
+    lw = syn.workload_layers(name, sets=1, gate=gate, s=0.5)[0]
+    x = syn.workload_tokens(name, 8)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=8)
     check(lw, x, y, c, m)
 
 
