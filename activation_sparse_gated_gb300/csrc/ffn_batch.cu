@@ -260,15 +260,25 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
     }
     __syncthreads();
     if (owns) {
-      for (int j = 0; j < nbat; ++j) {
-        float wf[VPC];
-        E::unpack(ldnc(col + (size_t)l_unit[b0 + j] * nch), wf);
-        const float* hj = l_h + (size_t)(b0 + j) * NB;
+      // eight slice loads in flight, then their FMAs
+      for (int j0 = 0; j0 < nbat; j0 += 8) {
+        uint4 r[8];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float h = hj[b];
+        for (int m = 0; m < 8; ++m)
+          r[m] = (j0 + m < nbat) ? ldnc(col + (size_t)l_unit[b0 + j0 + m] * nch) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int v = 0; v < VPC; ++v) yr[b][v] = fmaf(h, wf[v], yr[b][v]);
+        for (int m = 0; m < 8; ++m) {
+          if (j0 + m < nbat) {
+            float wf[VPC];
+            E::unpack(r[m], wf);
+            const float* hj = l_h + (size_t)(b0 + j0 + m) * NB;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              const float h = hj[b];
+#pragma unroll
+              for (int v = 0; v < VPC; ++v) yr[b][v] = fmaf(h, wf[v], yr[b][v]);
+            }
+          }
         }
       }
     }
@@ -301,24 +311,37 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   __syncthreads();
   if (misc[1]) {
     __threadfence();
-    for (int idx = tid; idx < nb * n4; idx += BT) {
-      const int b = idx / n4, i = idx - b * n4;
-      float4 c[YACC_COPIES];
+    // all loads of a round before its stores: ceil(nb * n4 / (4 * BT)) L2 round trips
+    for (int base = 0; base < nb * n4; base += 4 * BT) {
+      float4 c[4][YACC_COPIES];
 #pragma unroll
-      for (int r = 0; r < YACC_COPIES; ++r) c[r] = __ldcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i);
-      float4 v = c[0];
+      for (int k = 0; k < 4; ++k) {
+        const int idx = base + tid + k * BT;
+        const int b = idx / n4, i = idx - b * n4;
 #pragma unroll
-      for (int r = 1; r < YACC_COPIES; ++r) {
-        v.x += c[r].x; v.y += c[r].y; v.z += c[r].z; v.w += c[r].w;
+        for (int r = 0; r < YACC_COPIES; ++r)
+          c[k][r] = idx < nb * n4 ? __ldcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int r = 0; r < YACC_COPIES; ++r)
-        __stcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
-      if constexpr (VPC == 4) {
-        reinterpret_cast<float4*>(p.y)[(size_t)b * n4 + i] = v;
-      } else {
-        reinterpret_cast<uint2*>(p.y)[(size_t)b * n4 + i] =
-            make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+      for (int k = 0; k < 4; ++k) {
+        const int idx = base + tid + k * BT;
+        if (idx >= nb * n4) continue;
+        const int b = idx / n4, i = idx - b * n4;
+        float4 v = c[k][0];
+#pragma unroll
+        for (int r = 1; r < YACC_COPIES; ++r) {
+          v.x += c[k][r].x; v.y += c[k][r].y; v.z += c[k][r].z; v.w += c[k][r].w;
+        }
+#pragma unroll
+        for (int r = 0; r < YACC_COPIES; ++r)
+          __stcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
+        if constexpr (VPC == 4) {
+          reinterpret_cast<float4*>(p.y)[(size_t)b * n4 + i] = v;
+        } else {
+          reinterpret_cast<uint2*>(p.y)[(size_t)b * n4 + i] =
+              make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+        }
       }
     }
     if (tid < nb) {

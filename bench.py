@@ -276,6 +276,59 @@ def dense_graphs(layers_dev, x, y, stream):
     return graphs
 
 
+def batched_extras(ffns, layers, x, stream, args, peak):
+    """Batched decode of the same layer sets: B tokens per call, token group t through set t mod 8."""
+    import torch
+    import torch.nn.functional as F
+    import activation_sparse_gated_gb300 as sffn
+    D, H = layers[0].D, layers[0].H
+    dev = x.device
+    n_sets = len(ffns)
+    ld = [{"W1": lw.W1.to(dev), "W3": lw.W3.to(dev), "W2": lw.W2.to(dev)} for lw in layers]
+    out = {}
+    for B in (4, 16, 64):
+        calls = x.shape[0] // B
+        y = torch.empty_like(x)
+        # union of the tokens' live sets per call (untimed)
+        unions = []
+        with torch.cuda.stream(stream):
+            for t in range(min(calls, 64)):
+                f = ffns[t % n_sets]
+                sffn.sffn_forward(f.h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+                unions.append(int(f.active_mask(B).any(axis=0).sum()))
+        stream.synchronize()
+        mean_union = sum(unions) / len(unions)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(calls):
+                sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+        tt = time_graph(g, stream, args.steps, args.warmup)
+        us = 1e6 * tt / (args.steps * calls)
+        bytes_call = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
+        yd = torch.empty_like(x)
+
+        def body():
+            for t in range(calls):
+                L = ld[t % n_sets]
+                xt = x[t * B:(t + 1) * B]
+                yd[t * B:(t + 1) * B] = F.linear(F.relu(F.linear(xt, L["W1"])) * F.linear(xt, L["W3"]), L["W2"])
+        with torch.cuda.stream(stream):
+            body()
+        stream.synchronize()
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd, stream=stream):
+            body()
+        td = time_graph(gd, stream, args.steps, args.warmup)
+        usd = 1e6 * td / (args.steps * calls)
+        out[f"B{B}"] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,
+                        "union_fraction": mean_union / H, "gbs": bytes_call / (us * 1e3),
+                        "frac_of_measured": bytes_call / (us * 1e3) / peak,
+                        "dense_bf16_us_per_call": usd, "speedup_vs_dense_bf16": usd / us,
+                        "gpu_launches_per_call": (B + 7) // 8}
+        del g, gd
+    return out
+
+
 def run_gpu(args):
     import torch
     import activation_sparse_gated_gb300 as sffn
@@ -392,6 +445,7 @@ def run_gpu(args):
                           "flop_ratio_eq4": flops.dense_macs(D, H) /
                           flops.lopa_macs(D, Hp, r, sum(lcounts) / len(lcounts))}
         del lffns, lg
+        extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
 
     cpu = None
     if rank == 0 and not args.no_cpu:
