@@ -320,6 +320,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       p.gather_rows = h->batch_plan.gather_rows;
       SFFN_CUDA(launch_ffn_batch(p, nb, h->dtype, lopa, h->stream_grid, h->batch_plan.smem, s));
     }
+    SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, nb, h->dtype, s));
     b += nb;
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -13,7 +13,7 @@
 // calls are stream-ordered, so what counts is how much of a call's weight
 // traffic happens before it may start (the dependency wait) and how short the
 // chain of dependent memory round trips after its gate is.
-//   * The kernel is light (512 threads, <= 64 registers, ~100 KB of shared
+//   * The kernel is light (384 threads, <= 64 registers, ~100 KB of shared
 //     memory) so the next call's blocks, launched early by programmatic
 //     dependent launch, co-reside with this call's and prefetch their gate
 //     rows while this call finishes.
@@ -30,8 +30,10 @@
 //     round trip; h_i = A(z_i) (W3[i,:] . x) from shared memory; warp w then
 //     folds its own slice of y over the list in registers (no atomics).
 //   * Blocks add their partial y into one of four fp32 accumulator copies
-//     (fewer blocks per address) with 128-bit atomics; the last block (ticket)
-//     sums the copies, rounds y, clears the copies and publishes the count.
+//     (fewer blocks per address) with 128-bit atomics and end; a small
+//     finalize kernel chained behind (finalize.cu) sums the copies, rounds y,
+//     clears the copies and publishes the count.  That is one kernel boundary
+//     instead of a fence, a ticket and a serial last block.
 // There are no spin-waits in this kernel.
 #include <algorithm>
 
@@ -42,7 +44,7 @@ namespace sffn {
 
 namespace {
 
-constexpr int SW = 16;          // warps per block
+constexpr int SW = 12;          // warps per block (two blocks and a finalize block fit an SM)
 constexpr int ST = SW * 32;     // threads per block
 constexpr int PIECE = 5;        // 16-byte chunks per lane per piece (2.5 KB per warp for bf16)
 
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   int* l_unit = reinterpret_cast<int*>(sp);
   float* l_a = reinterpret_cast<float*>(l_unit + cap);
   float* l_h = l_a + cap;
-  int* misc = reinterpret_cast<int*>(l_h + cap);  // 0: live count, 1: last-block flag
+  int* misc = reinterpret_cast<int*>(l_h + cap);  // 0: live count
   sp += align16((size_t)cap * 12 + 16);
   uint4* srows = reinterpret_cast<uint4*>(sp);
 
@@ -175,7 +177,6 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   const uint4* G = static_cast<const uint4*>(p.gate_w);
   const uint4* W3 = static_cast<const uint4*>(p.W3);
   const uint4* W2t = static_cast<const uint4*>(p.W2t);
-  float4* ya = reinterpret_cast<float4*>(p.yacc);
 
   if (tid == 0) {
     pdl_launch_dependents();
@@ -271,8 +272,9 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 
   // ---- gathers (both rows of every live unit were prefetched into L2), in as
   // few round trips as possible.  Warp w owns chunks [cs0, cs0 + cs_n) of y,
-  // lane l chunk cs0 + l (a slice has at most 32 chunks because a row has at
-  // most 512).  Per batch of up to RB live units: their W3 rows are copied into
+  // lane l chunk cs0 + l and, when a slice is wider than 32 chunks (a row has
+  // at most 512 chunks, so a slice at most 43), chunk cs0 + 32 + l in a second
+  // pass.  Per batch of up to RB live units: their W3 rows are copied into
   // the (now free) shared area while every warp requests its W2^T slices of the
   // first eight units of the batch; then h = A(z) (W3 . x) from shared memory,
   // and y_slice += h W2^T[unit, slice] in registers.
@@ -337,59 +339,37 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     }
     __syncthreads();  // the shared area is reused by the next batch
   }
+  // into accumulator copy (block mod YACC_COPIES): fewer blocks per address
+  float* yc = p.yacc + (size_t)(blockIdx.x % YACC_COPIES) * D;
   if (n_live > 0 && owns) {
-    // into accumulator copy (block mod YACC_COPIES): fewer blocks per address
-    float* yc = p.yacc + (size_t)(blockIdx.x % YACC_COPIES) * D + (size_t)(cs0 + lane) * VPC;
 #pragma unroll
     for (int v = 0; v < VPC; v += 4)
-      atomicAdd(reinterpret_cast<float4*>(yc + v), make_float4(yr[v], yr[v + 1], yr[v + 2], yr[v + 3]));
+      atomicAdd(reinterpret_cast<float4*>(yc + (size_t)(cs0 + lane) * VPC + v),
+                make_float4(yr[v], yr[v + 1], yr[v + 2], yr[v + 3]));
   }
-  __threadfence();
-  __syncthreads();
-  const int n4 = D / 4;
-  if (tid == 0) {
-    if (n_live > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot, n_live);
-    __threadfence();
-    const int ticket = atomicAdd(p.ctrl + CTRL_TICKET, 1);
-    misc[1] = (ticket == (int)gridDim.x - 1);
+  // second chunk of the lane when the slice is wider than 32 chunks (every h is known now)
+  if (n_live > 0 && lane + 32 < cs_n) {
+#pragma unroll
+    for (int v = 0; v < VPC; ++v) yr[v] = 0.f;
+    const uint4* col2 = col + 32;
+    int j = 0;
+    for (; j + 4 <= n_live; j += 4) {
+      uint4 r[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) r[m] = ld_stream(col2 + (size_t)l_unit[j + m] * nch);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) fma_slice(r[m], l_h[j + m]);
+    }
+    for (; j < n_live; ++j) fma_slice(ld_stream(col2 + (size_t)l_unit[j] * nch), l_h[j]);
+#pragma unroll
+    for (int v = 0; v < VPC; v += 4)
+      atomicAdd(reinterpret_cast<float4*>(yc + (size_t)(cs0 + 32 + lane) * VPC + v),
+                make_float4(yr[v], yr[v + 1], yr[v + 2], yr[v + 3]));
   }
-  __syncthreads();
-  if (misc[1]) {
-    // every other block has added its partial and taken its ticket
-    __threadfence();
-    // every load before any store: one L2 round trip (n4 <= 2 * ST)
-    float4 c[2][YACC_COPIES];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + k * ST;
-#pragma unroll
-      for (int r = 0; r < YACC_COPIES; ++r)
-        c[k][r] = i < n4 ? __ldcg(ya + (size_t)r * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = tid + k * ST;
-      if (i >= n4) continue;
-      float4 v = c[k][0];
-#pragma unroll
-      for (int r = 1; r < YACC_COPIES; ++r) {
-        v.x += c[k][r].x; v.y += c[k][r].y; v.z += c[k][r].z; v.w += c[k][r].w;
-      }
-#pragma unroll
-      for (int r = 0; r < YACC_COPIES; ++r) __stcg(ya + (size_t)r * n4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
-      if constexpr (VPC == 4) {
-        reinterpret_cast<float4*>(p.y)[i] = v;
-      } else {
-        reinterpret_cast<uint2*>(p.y)[i] = make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
-      }
-    }
-    if (tid == 0) {
-      // no other block touches these any more: plain loads and stores
-      p.counts[0] = __ldcg(p.ctrl + CTRL_COUNT + p.count_slot);
-      __stcg(p.ctrl + CTRL_COUNT + p.count_slot, 0);
-      __stcg(p.ctrl + CTRL_TICKET, 0);
-    }
-  }
+  // the block's live count; the finalize kernel that follows in the stream
+  // sums the accumulator copies once every block has finished (kernel
+  // completion orders all of these atomics before it)
+  if (tid == 0 && n_live > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot, n_live);
 }
 
 }  // namespace

@@ -16,8 +16,8 @@
 // per-token A(z) (zero where the token's gate is dead), their W3 rows gathered
 // through shared memory and their W2^T slices folded by the warp that owns the
 // slice, per token, in registers.  Per-token partial sums go to four fp32
-// accumulator copies; the last block sums them, rounds y and publishes the
-// per-token live counts.  CUDA cores only: up to 8 tokens the gate is cheap
+// accumulator copies; the finalize kernel chained behind sums them, rounds y
+// and publishes the per-token live counts.  CUDA cores only: up to 8 tokens the gate is cheap
 // next to its weight stream.
 #include <algorithm>
 
@@ -121,7 +121,6 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   const uint4* G = static_cast<const uint4*>(p.gate_w);
   const uint4* W3 = static_cast<const uint4*>(p.W3);
   const uint4* W2t = static_cast<const uint4*>(p.W2t);
-  float4* ya = reinterpret_cast<float4*>(p.yacc);
 
   if (tid == 0) pdl_launch_dependents();
   if (tid < 2 + NB) misc[tid] = 0;
@@ -298,58 +297,8 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
       }
     }
   }
-  __threadfence();
-  __syncthreads();
-  const int n4 = D / 4;
-  if (tid == 0) {
-    for (int b = 0; b < nb; ++b)
-      if (misc[2 + b] > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot + b, misc[2 + b]);
-    __threadfence();
-    const int ticket = atomicAdd(p.ctrl + CTRL_TICKET, 1);
-    misc[1] = (ticket == (int)gridDim.x - 1);
-  }
-  __syncthreads();
-  if (misc[1]) {
-    __threadfence();
-    // all loads of a round before its stores: ceil(nb * n4 / (4 * BT)) L2 round trips
-    for (int base = 0; base < nb * n4; base += 4 * BT) {
-      float4 c[4][YACC_COPIES];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int idx = base + tid + k * BT;
-        const int b = idx / n4, i = idx - b * n4;
-#pragma unroll
-        for (int r = 0; r < YACC_COPIES; ++r)
-          c[k][r] = idx < nb * n4 ? __ldcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int idx = base + tid + k * BT;
-        if (idx >= nb * n4) continue;
-        const int b = idx / n4, i = idx - b * n4;
-        float4 v = c[k][0];
-#pragma unroll
-        for (int r = 1; r < YACC_COPIES; ++r) {
-          v.x += c[k][r].x; v.y += c[k][r].y; v.z += c[k][r].z; v.w += c[k][r].w;
-        }
-#pragma unroll
-        for (int r = 0; r < YACC_COPIES; ++r)
-          __stcg(ya + ((size_t)b * YACC_COPIES + r) * n4 + i, make_float4(0.f, 0.f, 0.f, 0.f));
-        if constexpr (VPC == 4) {
-          reinterpret_cast<float4*>(p.y)[(size_t)b * n4 + i] = v;
-        } else {
-          reinterpret_cast<uint2*>(p.y)[(size_t)b * n4 + i] =
-              make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
-        }
-      }
-    }
-    if (tid < nb) {
-      p.counts[tid] = __ldcg(p.ctrl + CTRL_COUNT + p.count_slot + tid);
-      __stcg(p.ctrl + CTRL_COUNT + p.count_slot + tid, 0);
-    }
-    if (tid == 0) __stcg(p.ctrl + CTRL_TICKET, 0);
-  }
+  // per-token live counts; the finalize kernel chained behind sums the copies
+  if (tid < nb && misc[2 + tid] > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot + tid, misc[2 + tid]);
 }
 
 template <typename T, bool LOPA, int NB>

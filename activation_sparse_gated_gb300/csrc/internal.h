@@ -68,6 +68,11 @@ cudaError_t ffn_batch_prepare(size_t max_smem);
 cudaError_t launch_ffn_batch(const B1Params& p, int nb, int dtype, bool lopa, int grid, size_t smem,
                              cudaStream_t s);
 
+// y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the
+// copies and publishes the nb live counts (chained behind a forward kernel).
+cudaError_t launch_finalize(float* yacc, void* y, int* ctrl, int* counts, int count_slot, int D, int nb,
+                            int dtype, cudaStream_t s);
+
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,
                           cudaStream_t s);
