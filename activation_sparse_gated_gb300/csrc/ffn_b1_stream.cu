@@ -19,10 +19,10 @@
 //     rows while this call finishes.
 //   * Before the wait, a block copies the first rows of its gate slice into
 //     shared memory (16-byte cp.async, ~96 KB, the whole slice for the
-//     low-rank gate) and every warp requests the first two pieces of its
-//     streamed rows into registers.  After the wait, warps stream the rest as
-//     pieces through two register buffers (one multiplied while the next is in
-//     flight), so loads stay outstanding continuously.
+//     low-rank gate) and every warp requests the first pieces of one more row
+//     into registers.  After the wait, once the shared rows are consumed, the
+//     rest of the slice is copied into the freed area in as few batches as
+//     possible (one round trip each) while warps finish their register rows.
 //   * A live unit goes on the block's list (shared atomic counter: the
 //     compaction) and its W3 and W2^T rows are prefetched into L2 at once.
 //   * After the gate: the live units' W3 rows are copied into the now free
@@ -183,23 +183,29 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     misc[0] = 0;
   }
 
-  // ---- before the dependency wait (weights never depend on earlier kernels):
-  // the block's first R gate rows go to shared memory, every warp requests the
-  // first two pieces of its streamed rows (row0 + R + warp + SW*k), and x is
-  // prefetched into L2 (harmless whatever the previous kernel does to it).
+  // ---- Gate rows of the block, in three parts:
+  //   [0, R)             copied into the shared area before the dependency wait;
+  //   [R, R + nreg)      one row per warp, streamed as pieces through two
+  //                      register buffers, the first two requested before the wait;
+  //   [R + nreg, nrows)  copied into the shared area in batches of up to R rows
+  //                      once the first part has been consumed (one round trip
+  //                      per batch instead of one per piece).
+  // Weights never depend on earlier kernels; x is prefetched into L2, which is
+  // harmless whatever the previous kernel does to it.
   const int nrows = row1 - row0;
   const int R = min(p.pref_rows, nrows);
-  {
-    const uint4* src = G + (size_t)row0 * nchg;
-    for (int i = tid; i < R * nchg; i += ST) cp_async16(srows + i, src + i);
+  const int nreg = max(0, min(SW, nrows - R));
+  auto copy_rows = [&](int first, int n) {  // rows [first, first + n) of the slice -> shared area
+    const uint4* src = G + (size_t)(row0 + first) * nchg;
+    for (int i = tid; i < n * nchg; i += ST) cp_async16(srows + i, src + i);
     cp_async_commit();
-  }
-  const int my_rows = (nrows - R - warp + SW - 1) / SW;
-  const int n_seq = my_rows > 0 ? my_rows * npg : 0;
-  auto seq_row = [&](int sidx) { return G + (size_t)(row0 + R + warp + (sidx / npg) * SW) * nchg; };
+  };
+  copy_rows(0, R);
+  const int n_seq = warp < nreg ? npg : 0;
+  const uint4* my_row = G + (size_t)(row0 + R + warp) * nchg;
   uint4 wa[PIECE], wb[PIECE];
-  if (n_seq > 0) load_piece(wa, seq_row(0), 0, lane, nchg);
-  if (n_seq > 1) load_piece(wb, seq_row(1), 1 % npg, lane, nchg);
+  if (n_seq > 0) load_piece(wa, my_row, 0, lane, nchg);
+  if (n_seq > 1) load_piece(wb, my_row, 1, lane, nchg);
   if (tid == 0) prefetch_l2(p.x, (uint32_t)nch * 16u);
 
   pdl_wait();  // x, t, the outputs and the accumulators follow stream order
@@ -226,46 +232,64 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       prefetch_row_l2(W2t + (size_t)q * nch, (uint32_t)nch * 16u, lane);
     }
   };
-  // gate rows already in shared memory
-  for (int i = warp; i < R; i += SW) {
-    const uint4* r = srows + (size_t)i * nchg;
-    float a0 = 0.f, a1 = 0.f;
-    for (int c = lane; c < nchg; c += 32) {
-      if constexpr (LOPA) {
-        dot_chunk_t<E>(r[c], ts, c, a0, a1);
-      } else {
-        float wf[VPC], xf[VPC];
-        E::unpack(r[c], wf);
-        E::unpack(xs[c], xf);
+  // z for n rows of the shared area, the first being slice row `first`
+  auto shared_rows = [&](int first, int n) {
+    for (int i = warp; i < n; i += SW) {
+      const uint4* r = srows + (size_t)i * nchg;
+      float a0 = 0.f, a1 = 0.f;
+      for (int c = lane; c < nchg; c += 32) {
+        if constexpr (LOPA) {
+          dot_chunk_t<E>(r[c], ts, c, a0, a1);
+        } else {
+          float wf[VPC], xf[VPC];
+          E::unpack(r[c], wf);
+          E::unpack(xs[c], xf);
 #pragma unroll
-        for (int v = 0; v < VPC; v += 2) {
-          a0 = fmaf(wf[v], xf[v], a0);
-          a1 = fmaf(wf[v + 1], xf[v + 1], a1);
+          for (int v = 0; v < VPC; v += 2) {
+            a0 = fmaf(wf[v], xf[v], a0);
+            a1 = fmaf(wf[v + 1], xf[v + 1], a1);
+          }
         }
       }
-    }
-    decide(row0 + i, warp_sum(a0 + a1));
-  }
-  // streamed gate rows
-  float acc = 0.f;
-  auto consume = [&](const uint4(&w)[PIECE], int sidx) {
-    if constexpr (LOPA)
-      acc += dot_piece_t<E>(w, ts, sidx % npg, lane, nchg);
-    else
-      acc += dot_piece<E>(w, xs, sidx % npg, lane, nchg);
-    if (sidx % npg == npg - 1) {
-      const float z = warp_sum(acc);
-      acc = 0.f;
-      decide(row0 + R + warp + (sidx / npg) * SW, z);
+      decide(row0 + first + i, warp_sum(a0 + a1));
     }
   };
-  for (int sidx = 0; sidx < n_seq; sidx += 2) {
-    consume(wa, sidx);
-    if (sidx + 2 < n_seq) load_piece(wa, seq_row(sidx + 2), (sidx + 2) % npg, lane, nchg);
-    if (sidx + 1 < n_seq) {
-      consume(wb, sidx + 1);
-      if (sidx + 3 < n_seq) load_piece(wb, seq_row(sidx + 3), (sidx + 3) % npg, lane, nchg);
+  shared_rows(0, R);
+  __syncthreads();  // the shared area is free again
+  int next = R + nreg;
+  int nb1 = min(R, nrows - next);
+  if (nb1 > 0) copy_rows(next, nb1);
+
+  // the register-streamed row of this warp (its first pieces landed before the wait)
+  float acc = 0.f;
+  auto consume = [&](const uint4(&w)[PIECE], int pc) {
+    if constexpr (LOPA)
+      acc += dot_piece_t<E>(w, ts, pc, lane, nchg);
+    else
+      acc += dot_piece<E>(w, xs, pc, lane, nchg);
+    if (pc == npg - 1) {
+      const float z = warp_sum(acc);
+      acc = 0.f;
+      decide(row0 + R + warp, z);
     }
+  };
+  for (int pc = 0; pc < n_seq; pc += 2) {
+    consume(wa, pc);
+    if (pc + 2 < n_seq) load_piece(wa, my_row, pc + 2, lane, nchg);
+    if (pc + 1 < n_seq) {
+      consume(wb, pc + 1);
+      if (pc + 3 < n_seq) load_piece(wb, my_row, pc + 3, lane, nchg);
+    }
+  }
+  // the remaining rows, a shared-area batch at a time
+  while (nb1 > 0) {
+    cp_async_wait_all();
+    __syncthreads();
+    shared_rows(next, nb1);
+    __syncthreads();
+    next += nb1;
+    nb1 = min(R, nrows - next);
+    if (nb1 > 0) copy_rows(next, nb1);
   }
   __syncthreads();
   const int n_live = misc[0];
