@@ -47,7 +47,7 @@ struct sffn_s {
   void* V = nullptr;       // V[r, D]
   void* W3 = nullptr;      // W3[H, D]
   void* W2t = nullptr;     // W2^T[H, D]
-  float* yacc = nullptr;   // [SFFN_MAX_BATCH, D]
+  float* yacc = nullptr;   // [SFFN_MAX_BATCH * YACC_COPIES, D]
   float* tbuf = nullptr;   // [SFFN_MAX_BATCH, r]
   int* ctrl = nullptr;     // CTRL_INTS
   int* counts = nullptr;   // [SFFN_MAX_BATCH]
@@ -62,6 +62,13 @@ struct sffn_s {
   int stream_rows_cap = 0;
   StreamPlan stream_plan;
   BatchPlan batch_plan;  // groups of up to 8 tokens
+  // tensor-core batched path (bf16, standard gate)
+  TcPlan tc;
+  TcMaps tcm;
+  bool tc_ready = false;
+  int tc_min_batch = 2;    // batches of at least this many tokens take the tensor-core path
+  uint16_t* hbuf = nullptr;
+  int* tickets = nullptr;
 };
 
 namespace {
@@ -78,6 +85,8 @@ void release(sffn_s* h) {
   cudaFree(h->ctrl);
   cudaFree(h->counts);
   cudaFree(h->mask);
+  cudaFree(h->hbuf);
+  cudaFree(h->tickets);
   if (h->ev) cudaEventDestroy(h->ev);
 }
 
@@ -124,7 +133,8 @@ int sync_and_check(sffn_s* h) {
   if (err != 0) {
     // the aborted kernel may have left partial sums and counters behind
     SFFN_CUDA(cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS));
-    SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * h->D));
+    SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * h->D));
+    if (h->tickets) SFFN_CUDA(cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS));
     return fail(SFFN_ERR_TIMEOUT, "a device-side wait ran out of time (error word 0x%x); outputs of "
                 "the affected forward are invalid", err);
   }
@@ -194,7 +204,7 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
       {&h->V, (size_t)std::max(r, 1) * D * elt},
       {&h->W3, (size_t)H * D * elt},
       {&h->W2t, (size_t)H * D * elt},
-      {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * D},
+      {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * D},
       {(void**)&h->tbuf, sizeof(float) * SFFN_MAX_BATCH * std::max(r, 8)},
       {(void**)&h->ctrl, sizeof(int) * CTRL_INTS},
       {(void**)&h->counts, sizeof(int) * SFFN_MAX_BATCH},
@@ -203,7 +213,7 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
   for (auto& a : allocs) {
     if ((e = cudaMalloc(a.p, a.bytes))) return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
   }
-  if ((e = cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * D)) ||
+  if ((e = cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * D)) ||
       (e = cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS)) ||
       (e = cudaMemset(h->counts, 0, sizeof(int) * SFFN_MAX_BATCH)) ||
       (e = cudaMemset(h->mask, 0, (size_t)SFFN_MAX_BATCH * H)))
@@ -249,6 +259,21 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
     if ((e = ffn_b1_stream_prepare(h->max_smem)))
       return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   }
+  if (dtype == SFFN_BF16 && r == 0) {
+    h->tc = plan_ffn_tc(D, H, h->num_sms);
+    if (h->tc.ok) {
+      if ((e = cudaMalloc(&h->hbuf, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))) ||
+          (e = cudaMalloc(&h->tickets, sizeof(int) * TC_TICKETS)))
+        return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
+      if ((e = cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+      if (const char* env = std::getenv("SFFN_TC_GATE_KB")) h->tc.gate_smem_budget = (size_t)std::atoi(env) * 1024;
+      if (const char* env = std::getenv("SFFN_TC_DOWN_KB")) h->tc.down_smem_budget = (size_t)std::atoi(env) * 1024;
+      if ((e = cudaMemset(h->hbuf, 0, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))))
+        return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+      if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if (const char* env = std::getenv("SFFN_TC_MIN_BATCH")) h->tc_min_batch = std::max(1, std::atoi(env));
+    }
+  }
   if ((e = cudaDeviceSynchronize())) return bail(SFFN_ERR_CUDA, "cudaDeviceSynchronize", e);
   return h;
 }
@@ -270,6 +295,11 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
   if (!e) e = cudaStreamSynchronize(s);
   cudaFree(stage);
   if (e) return fail(SFFN_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(e));
+  if (h->tc.ok) {
+    if (int rc = encode_tc_maps(&h->tcm, h->tc, h->gate_w, h->W3, h->W2t, h->hbuf, h->D, h->H))
+      return fail(SFFN_ERR_CUDA, "tensor-map encoding of the weights failed (status %d)", rc);
+    h->tc_ready = true;
+  }
   h->weights_set = true;
   return SFFN_OK;
 }
@@ -287,9 +317,17 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   const bool lopa = h->r > 0;
   const size_t row = (size_t)h->D * h->elt;
 
+  if (h->tc_ready && B >= h->tc_min_batch) {
+    // whole batch on the tensor cores: gate kernel, down kernel, finalize
+    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets};
+    cudaError_t ce = cudaSuccess;
+    if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, kTimeoutNs, h->max_smem, s, &ce))
+      return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
+    SFFN_CUDA(ce);
+  }
   if (lopa) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
-  for (int b = 0; b < B;) {
+  for (int b = 0; b < B && !(h->tc_ready && B >= h->tc_min_batch);) {
     const int nb = std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;

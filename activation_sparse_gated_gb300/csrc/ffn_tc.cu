@@ -1,0 +1,603 @@
+// ffn_tc.cu -- gate-first FFN for a batch of tokens on the tensor cores (bf16
+// weights and tokens, fp32 accumulation, standard gate).
+//
+// Per token b the method is unchanged ("Model casting: compute the gate, then
+// skip most of the FFN", section "What an FFN actually computes"):
+//     y_b = sum_{i : z_bi > 0} W2[:, i] * A(z_bi) * (W3[i, :] . x_b),  z_b = W1 x_b.
+// With B tokens a unit's W3 row and W2 column are needed when ANY token keeps
+// it -- the union of the live sets, which the pages warn grows with the batch
+// (at 90 % sparsity it holds 57 % of the units at B = 8 and 82 % at B = 16).
+// From a handful of tokens up, this path therefore streams every unit slice
+// and lets the gate decide, per token and unit, what reaches y:
+//
+//   gate-up kernel, one block per slice of NU units:
+//     [Z ; P][slice, :] = [W1 ; W3][slice, :] X^T   one pass; the W1 and W3 rows
+//                                                   of a K chunk sit back to back,
+//                                                   so one M = 128 MMA per K step
+//                                                   serves both products (NU <= 64;
+//                                                   two MMAs otherwise)
+//     epilogue: live = z > 0, per-token counts and flags, and
+//               h = A(z) * p where live, else exactly 0, stored as a bf16 pair
+//               (h_hi + h_lo = h to about 16 bits): hbuf rows b (h_hi) and
+//               NB + b (h_lo), so one TMA box of 2 NB rows fetches both
+//   down kernel, one block per (128-wide slice of y, range of units):
+//     y^T[d-slice, :] += W2^T[units, d-slice]^T [h_hi ; h_lo]   MN-major A
+//               (W2^T rows as stored); h_hi and h_lo sit back to back as one
+//               N = 2 NB operand, the epilogue adds the two column halves;
+//               fp32 atomics into an accumulator; the last block of a y slice
+//               (a ticket per slice) rounds it into y and clears it, and block
+//               0 publishes the per-token live counts.
+//
+// All operands move by 2D TMA tiles with 128-byte swizzle, several tiles per
+// pipeline stage (one lane of a producer warp issues them, one lane of an MMA
+// warp issues tcgen05.mma; the stage is released by tcgen05.commit).  The
+// weights of the first stages are requested before the dependency wait.  The
+// K steps of a product go round-robin over `nacc` TMEM accumulators (summed
+// by the epilogue): small MMAs into one accumulator form a serial chain whose
+// latency, not the tensor pipe, would set the pace.
+// Ragged edges (units past H, y past D, K past D) are zero-filled by the TMA
+// unit; MMA rows past NU read neighbouring shared memory and land in TMEM
+// lanes the epilogue never reads.  Every wait is bounded (error word + early
+// exit), and a block drains its copies and MMAs before it releases TMEM.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "tc.cuh"
+
+namespace sffn {
+
+namespace {
+
+constexpr int TC_THREADS = 192;  // down kernel: warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+// gate-up kernel: warps 0-3 epilogue, 4 TMA producer, 5-8 MMA issuers.  An MMA
+// costs its issuing thread on the order of 150 cycles however small it is, so
+// the K steps of a chunk are split over up to four issuing warps, each into its
+// own TMEM accumulator.
+constexpr int TC_GATE_THREADS = 288;
+constexpr int TC_GATE_MMA_WARP0 = 5;
+constexpr int TC_PRODUCER_WARP = 4;
+constexpr int TC_MMA_WARP = 5;
+constexpr int TC_DTILE = 128;    // y values per down-kernel block (MMA M)
+constexpr int TC_UCH = 64;       // units per down-kernel K chunk (one TMA box)
+constexpr int TC_DC = 2;         // unit chunks per down-kernel stage
+constexpr size_t TC_SMEM_BUDGET = 200 * 1024;
+constexpr int TC_NS_MAX = 8;
+
+struct TcGateArgs {
+  int D, H, B, NB, NU, KC, C, NCG, NS, act, Hs, nacc;
+  uint32_t tmem_cols;
+  int* ctrl;
+  uint8_t* mask;
+  uint16_t* hbuf;  // [256][Hs] bf16 bits: h_hi in rows [0, NB), h_lo in rows [NB, 2 NB)
+  unsigned long long timeout_ns;
+};
+
+struct TcDownArgs {
+  int D, B, NB, nch, ndt, nsplit, NS, nacc;
+  uint32_t tmem_cols;
+  float* yacc;  // [B_max * YACC_COPIES, D]; this path uses copy 0, zero between calls
+  void* y;      // [B, D] bf16
+  int* ctrl;
+  int* counts;  // [B] published live counts
+  int* tickets; // [ndt] blocks of a y slice done, zero between calls
+  unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr uint32_t gate_stage_bytes(int C, int NU, int NB) {
+  return (uint32_t)C * 128u * (uint32_t)(2 * NU + NB);
+}
+__host__ __device__ constexpr uint32_t down_chunk_bytes(int NB) { return 2u * TC_UCH * 128u + 2u * (uint32_t)NB * 128u; }
+
+size_t gate_smem_bytes(int C, int MT, int NU, int NB, int NS) {
+  return 1024 + (size_t)NS * gate_stage_bytes(C, NU, NB) + 128 * 128 + 8 * (2 * NS + 2) + 8 + 4 * NB + 64;
+}
+size_t down_smem_bytes(int NB, int NS) {
+  return 1024 + (size_t)NS * TC_DC * down_chunk_bytes(NB) + 8 * (2 * NS + 2) + 8 + 64;
+}
+
+uint32_t tmem_cols_for(int n) {
+  uint32_t c = 32;
+  while (c < (uint32_t)n) c <<= 1;
+  return c;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// --------------------------------------------------------------------------- gate-up kernel
+// Stage layout: per 64-wide K chunk c, W1 rows [NU x 128 B] then W3 rows
+// [NU x 128 B]; then X regions [C][NB x 128 B].  K chunk group q covers chunks
+// q*C .. q*C+C-1.  TMEM: fused (2 NU <= 128): lanes [0, NU) = Z, [NU, 2 NU) =
+// P, NB columns; otherwise lanes [0, NU), Z in columns [0, NB), P in [NB, 2 NB).
+template <int MT>
+__global__ void __launch_bounds__(TC_GATE_THREADS, 1)
+    ffn_tc_gateup_kernel(const __grid_constant__ CUtensorMap mW1, const __grid_constant__ CUtensorMap mW3,
+                         const __grid_constant__ CUtensorMap mX, const TcGateArgs p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  const int NS = p.NS, NB = p.NB, C = p.C;
+  const uint32_t wreg = (uint32_t)p.NU * 128u, xreg = (uint32_t)NB * 128u;
+  const uint32_t st_bytes = gate_stage_bytes(C, p.NU, NB);
+  // stages, then 128 rows of slack: an MMA reads 128 (or MT) rows from the start of a
+  // chunk that holds 2 NU
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes + 128 * 128);
+  uint64_t* empty = full + NS;
+  uint64_t* done = empty + NS;  // every MMA complete (one commit per MMA warp)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  int* s_cnt = reinterpret_cast<int*>(tslot + 2);  // [NB] live counts of this slice
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u0 = blockIdx.x * p.NU;
+  int* err = p.ctrl + CTRL_ERR;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], p.nacc);  // one commit per MMA warp
+    }
+    mbar_init(done, p.nacc);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (tid < NB) s_cnt[tid] = 0;
+  if (warp == TC_GATE_MMA_WARP0) tmem_alloc(tslot, p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  // Let the next kernel launch only once this block holds its TMEM: a later
+  // kernel's blocks then never take the columns an earlier one still needs.
+  if (tid == 0) pdl_launch_dependents();
+
+  if (warp == TC_PRODUCER_WARP) {
+    // One TMA copy costs the issuing thread on the order of 100 ns, so the
+    // copies of a stage are spread over the warp's lanes: lane l issues copy l.
+    if (lane == 0) {
+      tma_prefetch_map(&mW1);
+      tma_prefetch_map(&mW3);
+      tma_prefetch_map(&mX);
+    }
+    auto nchunks = [&](int q) { return min(C, p.KC - q * C); };
+    const int npre = min(NS, p.NCG);
+    // the weights do not depend on the previous kernel: request them first
+    for (int q = 0; q < npre; ++q) {
+      uint8_t* st = sm + (size_t)q * st_bytes;
+      const int nc = nchunks(q);
+      if (lane == 0) mbar_arrive_expect_tx(&full[q], (uint32_t)nc * (2 * wreg + xreg));
+      __syncwarp();
+      if (lane < 2 * nc)
+        tma_tile_2d(st + lane * wreg, (lane & 1) ? &mW3 : &mW1, (q * C + (lane >> 1)) * 64, u0, &full[q]);
+    }
+    pdl_wait();
+    for (int q = 0; q < npre; ++q)
+      if (lane < nchunks(q))
+        tma_tile_2d(sm + (size_t)q * st_bytes + 2 * C * wreg + lane * xreg, &mX, (q * C + lane) * 64, 0, &full[q]);
+    int issued = npre;
+    for (int q = npre; q < p.NCG; ++q) {
+      const int s = q % NS;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&empty[s], ((q / NS) - 1) & 1, abort_flag, err, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t* st = sm + (size_t)s * st_bytes;
+      const int nc = nchunks(q);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nc * (2 * wreg + xreg));
+      __syncwarp();
+      if (lane < 3 * nc) {
+        const int c = lane / 3, k = lane - 3 * c;  // k: 0 W1, 1 W3, 2 x
+        if (k < 2)
+          tma_tile_2d(st + (2 * c + k) * wreg, k ? &mW3 : &mW1, (q * C + c) * 64, u0, &full[s]);
+        else
+          tma_tile_2d(st + 2 * C * wreg + c * xreg, &mX, (q * C + c) * 64, 0, &full[s]);
+      }
+      issued = q + 1;
+    }
+    if (lane == 0)
+      for (int q = max(0, issued - NS); q < issued; ++q) mbar_wait_drain(&full[q % NS], (q / NS) & 1, p.timeout_ns);
+    __syncwarp();
+  } else if (warp >= TC_GATE_MMA_WARP0) {
+    const int mw = warp - TC_GATE_MMA_WARP0;  // this warp issues K steps kk = mw (mod nacc) into accumulator mw
+    if (mw < p.nacc && lane == 0) {
+      const bool fused = 2 * p.NU <= 128;
+      const uint32_t idesc = idesc_bf16_f32(fused ? 128 : MT, NB, false, false);
+      const uint32_t acc_cols = fused ? (uint32_t)NB : 2u * NB;  // columns of one accumulator
+      const uint32_t da = tmem + (uint32_t)mw * acc_cols;
+      bool started = false;
+      for (int q = 0; q < p.NCG; ++q) {
+        const int s = q % NS;
+        if (!mbar_wait(&full[s], (q / NS) & 1, abort_flag, err, p.timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(sm + (size_t)s * st_bytes);
+        const uint64_t a0 = smem_desc(sa, 16, 1024, SMEM_LAYOUT_SW128);
+        const uint64_t b0 = smem_desc(sa + 2 * C * wreg, 16, 1024, SMEM_LAYOUT_SW128);
+        const int nc = min(C, p.KC - q * C);
+        for (int c = 0; c < nc; ++c) {
+          // descriptors advance by adds (16-byte units): no divisions on the issue path
+          const uint64_t ac = a0 + ((2 * c * wreg) >> 4), bc = b0 + ((c * xreg) >> 4);
+          for (int kk = mw; kk < 4; kk += p.nacc) {
+            tc_mma(da, ac + 2 * kk, bc + 2 * kk, idesc, started);
+            if (!fused) tc_mma(da + (uint32_t)NB, ac + (wreg >> 4) + 2 * kk, bc + 2 * kk, idesc, started);
+            started = true;
+          }
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(done);
+      mbar_wait_drain(done, 0, p.timeout_ns);  // every MMA warp's work complete before TMEM is released
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps 0..3: warp q reads TMEM lanes 32q..32q+31 (summing
+    // the accumulators) into a shared [128 lanes][ncol] copy -- the stages are
+    // free once every MMA is done -- then thread (unit r, token group g) takes
+    // tokens g, g + 2, ... (units in rounds of 64): a warp shares each token, so
+    // counts are ballots.
+    pdl_wait();  // the outputs below may still be read by the previous forward
+    const bool fused = 2 * p.NU <= 128;
+    const int ncol = fused ? NB : 2 * NB, ldc = ncol + 1;
+    float* s_acc = reinterpret_cast<float*>(sm);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+      float* row = s_acc + (size_t)(32 * warp + lane) * ldc;
+      for (int c0 = 0; c0 < ncol; c0 += 16) {
+        float v[16];
+        tmem_ld_sum(tl + c0, ncol, p.nacc, v);
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) row[c0 + jj] = v[jj];
+      }
+    }
+    named_barrier(1, 128);
+    for (int r0 = 0; ok && r0 < p.NU; r0 += 64) {
+      const int r = r0 + (tid & 63), g = tid >> 6;
+      const bool valid = r < p.NU && u0 + r < p.H;
+      const int u = u0 + r;
+      for (int b = g; b < p.B; b += 2) {
+        const float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
+        const float pv = !valid ? 0.f : fused ? s_acc[(size_t)(p.NU + r) * ldc + b] : s_acc[(size_t)r * ldc + NB + b];
+        const bool lv = valid && z > 0.f;
+        const unsigned bal = __ballot_sync(0xffffffffu, lv);
+        if (lane == 0 && bal) atomicAdd(&s_cnt[b], __popc(bal));
+        if (valid) {
+          if (p.mask) p.mask[(size_t)b * p.H + u] = lv ? 1 : 0;
+          const float hv = lv ? activation(p.act, z) * pv : 0.f;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
+          p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(hi);
+          p.hbuf[(size_t)(NB + b) * p.Hs + u] = __bfloat16_as_ushort(lo);
+        }
+      }
+    }
+    named_barrier(1, 128);
+    if (tid < p.B && s_cnt[tid]) atomicAdd(p.ctrl + CTRL_COUNT + tid, s_cnt[tid]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == TC_GATE_MMA_WARP0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// --------------------------------------------------------------------------- down kernel
+// Stage layout, per unit chunk (64 units): W2^T rows for y values d0..d0+63
+// and d0+64..d0+127 (two 8 KB MN-major atom columns), then h_hi and h_lo
+// ([NB rows x 128 B] each).
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    ffn_tc_down_kernel(const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mH,
+                       const TcDownArgs p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  const int NS = p.NS, NB = p.NB;
+  const uint32_t half = TC_UCH * 128u, hreg = (uint32_t)NB * 128u, chb = down_chunk_bytes(NB);
+  const uint32_t st_bytes = TC_DC * chb;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes);
+  uint64_t* empty = full + NS;
+  uint64_t* done = empty + NS;
+  uint64_t* mdone = done + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int dt = blockIdx.x % p.ndt, sp = blockIdx.x / p.ndt, d0 = dt * TC_DTILE;
+  const int c0 = (int)((long long)sp * p.nch / p.nsplit), c1 = (int)((long long)(sp + 1) * p.nch / p.nsplit);
+  const int nst = (c1 - c0 + TC_DC - 1) / TC_DC;
+  int* err = p.ctrl + CTRL_ERR;
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    mbar_init(mdone, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == TC_MMA_WARP) tmem_alloc(tslot, p.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) pdl_launch_dependents();  // after the TMEM allocation (see the gate-up kernel)
+
+  if (warp == TC_PRODUCER_WARP) {
+    // copies of a stage spread over the lanes (see the gate-up kernel)
+    if (lane == 0) {
+      tma_prefetch_map(&mW2);
+      tma_prefetch_map(&mH);
+    }
+    auto nchunks = [&](int q) { return min(TC_DC, c1 - c0 - q * TC_DC); };
+    const int npre = min(NS, nst);
+    for (int q = 0; q < npre; ++q) {  // W2^T is constant: request it before the dependency wait
+      uint8_t* st = sm + (size_t)q * st_bytes;
+      const int nc = nchunks(q);
+      if (lane == 0) mbar_arrive_expect_tx(&full[q], (uint32_t)nc * chb);
+      __syncwarp();
+      if (lane < 2 * nc) {
+        const int c = lane >> 1, mh = lane & 1;
+        tma_tile_2d(st + c * chb + mh * half, &mW2, d0 + 64 * mh, (c0 + q * TC_DC + c) * TC_UCH, &full[q]);
+      }
+    }
+    pdl_wait();  // h comes from the gate-up kernel
+    for (int q = 0; q < npre; ++q)
+      if (lane < nchunks(q))
+        tma_tile_2d(sm + (size_t)q * st_bytes + lane * chb + 2 * half, &mH, (c0 + q * TC_DC + lane) * TC_UCH, 0,
+                    &full[q]);
+    int issued = npre;
+    for (int q = npre; q < nst; ++q) {
+      const int s = q % NS;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&empty[s], ((q / NS) - 1) & 1, abort_flag, err, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      const int nc = nchunks(q);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)nc * chb);
+      __syncwarp();
+      if (lane < 3 * nc) {
+        const int c = lane / 3, k = lane - 3 * c;  // k: 0, 1 the two y halves of W2^T, 2 the h rows
+        uint8_t* cb = sm + (size_t)s * st_bytes + c * chb;
+        const int u = (c0 + q * TC_DC + c) * TC_UCH;
+        if (k < 2)
+          tma_tile_2d(cb + k * half, &mW2, d0 + 64 * k, u, &full[s]);
+        else
+          tma_tile_2d(cb + 2 * half, &mH, u, 0, &full[s]);
+      }
+      issued = q + 1;
+    }
+    if (lane == 0)
+      for (int q = max(0, issued - NS); q < issued; ++q) mbar_wait_drain(&full[q % NS], (q / NS) & 1, p.timeout_ns);
+    __syncwarp();
+  } else if (warp == TC_MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(TC_DTILE, 2 * NB, true, false);  // N = [h_hi ; h_lo]
+      int gk = 0;  // K step over the block's units
+      for (int q = 0; q < nst; ++q) {
+        const int s = q % NS;
+        if (!mbar_wait(&full[s], (q / NS) & 1, abort_flag, err, p.timeout_ns)) break;
+        tc_fence_after();
+        const int nc = min(TC_DC, c1 - c0 - q * TC_DC);
+        for (int c = 0; c < nc; ++c) {
+          const uint32_t cb = smem_u32(sm + (size_t)s * st_bytes + c * chb);
+          // 16 units per K step: two 8-unit K groups of 1 KB; the y halves are `half` bytes apart
+          const uint64_t ad0 = smem_desc(cb, half, 1024, SMEM_LAYOUT_SW128);
+          const uint64_t bd0 = smem_desc(cb + 2 * half, 16, 1024, SMEM_LAYOUT_SW128);
+#pragma unroll
+          for (int k = 0; k < TC_UCH / 16; ++k, ++gk)
+            tc_mma(tmem + (uint32_t)(gk & (p.nacc - 1)) * (2u * NB), ad0 + (k * 2048 >> 4), bd0 + 2 * k, idesc,
+                   gk >= p.nacc);
+        }
+        tc_commit(&empty[s]);
+      }
+      tc_commit(done);
+      tc_commit(mdone);
+      mbar_wait_drain(mdone, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue warps 0..3: lane = one y value of the slice
+    pdl_wait();
+    int* s_last = reinterpret_cast<int*>(tslot + 2);
+    if (blockIdx.x == 0 && tid < p.B) {  // the gate-up kernel is complete: publish the live counts
+      p.counts[tid] = __ldcg(p.ctrl + CTRL_COUNT + tid);
+      __stcg(p.ctrl + CTRL_COUNT + tid, 0);
+    }
+    const int d = d0 + 32 * warp + lane;
+    const int used = min(p.nacc, (c1 - c0) * (TC_UCH / 16));  // accumulators that received a K step
+    const bool ok = nst > 0 && __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+      float* ya = p.yacc + d;
+      for (int cc = 0; cc < NB; cc += 16) {
+        float v[16], v2[16];
+        tmem_ld_sum(tl + cc, 2 * NB, used, v);
+        tmem_ld_sum(tl + (uint32_t)NB + cc, 2 * NB, used, v2);  // the h_lo half
+        if (d < p.D) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * p.D, v[jj] + v2[jj]);
+        }
+      }
+    }
+    // the last block of this y slice rounds the sum into y and clears the accumulator
+    __threadfence();
+    named_barrier(1, 128);
+    if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
+    named_barrier(1, 128);
+    if (*s_last) {
+      __threadfence();
+      if (d < p.D) {
+        float* ya = p.yacc + d;
+        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + d;
+        for (int b0 = 0; b0 < p.B; b0 += 16) {  // 16 loads in flight, then the stores
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            v[j] = b0 + j < p.B ? __ldcg(ya + (size_t)(b0 + j) * YACC_COPIES * p.D) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (b0 + j < p.B) {
+              __stcg(ya + (size_t)(b0 + j) * YACC_COPIES * p.D, 0.f);
+              y[(size_t)(b0 + j) * p.D] = __float2bfloat16_rn(v[j]);
+            }
+        }
+      }
+      if (tid == 0) p.tickets[dt] = 0;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == TC_MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// --------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// bf16 matrix [rows, cols] (row stride in bytes), boxes of 64 columns x box_rows, 128-byte swizzle
+int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride_bytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return -1;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {stride_bytes};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
+}  // namespace
+
+TcPlan plan_ffn_tc(int D, int H, int num_sms) {
+  TcPlan p;
+  if (D % 8 != 0 || num_sms < 1) return p;
+  const int per = (H + num_sms - 1) / num_sms;
+  p.NU = std::max(8, (per + 7) / 8 * 8);
+  if (p.NU > 128) return p;  // more than 128 units per block: not planned
+  p.MT = p.NU <= 64 ? 64 : 128;
+  p.ntiles = (H + p.NU - 1) / p.NU;
+  p.KC = (D + 63) / 64;
+  p.ndt = (D + TC_DTILE - 1) / TC_DTILE;
+  p.nch = (H + TC_UCH - 1) / TC_UCH;
+  p.nsplit = std::max(1, std::min(p.nch, num_sms / p.ndt));
+  p.Hs = (H + 7) / 8 * 8;
+  p.gate_smem_budget = TC_SMEM_BUDGET;
+  p.down_smem_budget = TC_SMEM_BUDGET;
+  p.ok = true;
+  return p;
+}
+
+size_t ffn_tc_hbuf_elems(const TcPlan& p) { return (size_t)2 * 128 * p.Hs; }
+
+int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, const void* W2t, uint16_t* hbuf,
+                   int D, int H) {
+  int rc = encode_2d(&m->w1, W1, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NU);
+  if (!rc) rc = encode_2d(&m->w3, W3, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NU);
+  if (!rc) rc = encode_2d(&m->w2, W2t, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, TC_UCH);
+  for (int i = 0; i < 8 && !rc; ++i)  // h boxes of 2 NB rows, NB = 16 (i + 1)
+    rc = encode_2d(&m->h[i], hbuf, 256, (uint64_t)H, (uint64_t)p.Hs * 2, (uint32_t)(32 * (i + 1)));
+  return rc;
+}
+
+cudaError_t ffn_tc_prepare(size_t max_smem) {
+  cudaError_t e =
+      cudaFuncSetAttribute(ffn_tc_gateup_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  if (!e)
+    e = cudaFuncSetAttribute(ffn_tc_gateup_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  if (!e) e = cudaFuncSetAttribute(ffn_tc_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  return e;
+}
+
+int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
+                  int B, int act, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err) {
+  *cuda_err = cudaSuccess;
+  if (!plan.ok || B < 1 || B > 128) return -1;
+  const int NB = (B + 15) / 16 * 16;
+  CUtensorMap mx;
+  if (int rc = encode_2d(&mx, x, (uint64_t)B, (uint64_t)D, (uint64_t)D * 2, (uint32_t)NB)) return rc;
+
+  TcGateArgs g;
+  g.D = D;
+  g.H = H;
+  g.B = B;
+  g.NB = NB;
+  g.NU = plan.NU;
+  g.KC = plan.KC;
+  g.C = 4;
+  while (g.C > 1 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, 2) > std::min(max_smem, (size_t)TC_SMEM_BUDGET)) g.C >>= 1;
+  g.NCG = (plan.KC + g.C - 1) / g.C;
+  g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.gate_smem_budget / gate_stage_bytes(g.C, plan.NU, NB)));
+  while (g.NS > 2 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS) > max_smem) --g.NS;
+  g.act = act;
+  g.Hs = plan.Hs;
+  {
+    const int cols = 2 * plan.NU <= 128 ? NB : 2 * NB;  // one accumulator
+    g.nacc = cols <= 128 ? 4 : 2;  // MMA warps = accumulators, nacc * cols <= 512
+    g.tmem_cols = tmem_cols_for(g.nacc * cols);
+  }
+  g.ctrl = buf.ctrl;
+  g.mask = buf.mask;
+  g.hbuf = buf.hbuf;
+  g.timeout_ns = timeout_ns;
+  const size_t smem1 = gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS);
+  // the epilogue stages the accumulator [128][2 NB + 1] fp32 over the pipeline stages
+  if ((size_t)g.NS * gate_stage_bytes(g.C, plan.NU, NB) < (size_t)128 * (2 * NB + 1) * 4 || smem1 > max_smem) {
+    *cuda_err = cudaErrorInvalidConfiguration;
+    return 0;
+  }
+  cudaError_t e =
+      plan.MT == 64
+          ? launch_pdl(ffn_tc_gateup_kernel<64>, dim3(plan.ntiles), dim3(TC_GATE_THREADS), smem1, s, maps.w1, maps.w3,
+                       mx, g)
+          : launch_pdl(ffn_tc_gateup_kernel<128>, dim3(plan.ntiles), dim3(TC_GATE_THREADS), smem1, s, maps.w1, maps.w3, mx,
+                       g);
+  if (e) {
+    *cuda_err = e;
+    return 0;
+  }
+
+  TcDownArgs d;
+  d.D = D;
+  d.B = B;
+  d.NB = NB;
+  d.nch = plan.nch;
+  d.ndt = plan.ndt;
+  d.nsplit = plan.nsplit;
+  d.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.down_smem_budget / (TC_DC * down_chunk_bytes(NB))));
+  while (d.NS > 2 && down_smem_bytes(NB, d.NS) > max_smem) --d.NS;
+  d.nacc = NB <= 64 ? 4 : 2;  // a power of two, nacc * 2 NB <= 512
+  d.tmem_cols = tmem_cols_for(d.nacc * 2 * NB);
+  d.y = y;
+  d.counts = buf.counts;
+  d.tickets = buf.tickets;
+  d.yacc = buf.yacc;
+  d.ctrl = buf.ctrl;
+  d.timeout_ns = timeout_ns;
+  const size_t smem2 = down_smem_bytes(NB, d.NS);
+  if (smem2 > max_smem) {
+    *cuda_err = cudaErrorInvalidConfiguration;
+    return 0;
+  }
+  *cuda_err = launch_pdl(ffn_tc_down_kernel, dim3(plan.ndt * plan.nsplit), dim3(TC_THREADS), smem2, s, maps.w2,
+                         maps.h[NB / 16 - 1], d);
+  return 0;
+}
+
+}  // namespace sffn

@@ -1,6 +1,7 @@
 // internal.h -- kernel launchers shared by the C-ABI host code (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -67,6 +68,44 @@ BatchPlan plan_ffn_batch(int D, int gate_k, int elt_bytes, bool lopa, int rows_c
 cudaError_t ffn_batch_prepare(size_t max_smem);
 cudaError_t launch_ffn_batch(const B1Params& p, int nb, int dtype, bool lopa, int grid, size_t smem,
                              cudaStream_t s);
+
+// Batched forward on the tensor cores (bf16, standard gate): a gate-up kernel
+// ([Z | P] = [W1 | W3] X^T, live flags and counts, h = A(z) * p where z > 0)
+// and a down kernel (y^T += W2^T[units]^T h into the accumulator copies); the
+// finalize kernel follows.  Gate-up: one block per slice of NU units, MT = MMA
+// rows (64 or 128).  Down: ndt slices of 128 y values x nsplit ranges of the
+// nch 64-unit chunks.
+struct TcPlan {
+  bool ok = false;
+  int NU = 0, MT = 0, ntiles = 0, KC = 0;
+  int ndt = 0, nch = 0, nsplit = 0;
+  int Hs = 0;  // row stride (elements) of the h buffer
+  size_t gate_smem_budget = 0, down_smem_budget = 0;  // pipeline-stage bytes per block
+};
+struct TcMaps {
+  CUtensorMap w1, w3;  // W1, W3 [H, D]: boxes of 64 columns x NU rows
+  CUtensorMap w2;      // W2^T [H, D]: boxes of 64 columns x 64 rows
+  CUtensorMap h[8];    // h buffer [256, H]: boxes of 64 columns x 2 NB rows, NB = 16 (i + 1)
+};
+struct TcBuffers {
+  uint16_t* hbuf;  // ffn_tc_hbuf_elems(plan) bf16 values
+  float* yacc;     // [B_max * YACC_COPIES, D]
+  int* ctrl;
+  uint8_t* mask;   // [B_max, H]
+  int* counts;     // [B_max] published live counts
+  int* tickets;    // [TC_TICKETS] zero between calls
+};
+constexpr int TC_TICKETS = 64;  // >= slices of 128 y values (D <= 8192)
+TcPlan plan_ffn_tc(int D, int H, int num_sms);
+size_t ffn_tc_hbuf_elems(const TcPlan& p);
+// 0 on success, else a driver status (or -1: tensor-map encoder unavailable)
+int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, const void* W2t, uint16_t* hbuf,
+                   int D, int H);
+cudaError_t ffn_tc_prepare(size_t max_smem);
+// Whole forward (y and counts written; no finalize kernel).  Returns 0 and sets
+// *cuda_err to the launch status, or a non-zero encode status.
+int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
+                  int B, int act, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
 
 // y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the
 // copies and publishes the nb live counts (chained behind a forward kernel).

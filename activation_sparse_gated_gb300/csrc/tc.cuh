@@ -1,0 +1,125 @@
+// tc.cuh -- sm_103a tensor-core helpers for the batched path: tcgen05 MMA
+// descriptors and issue, TMEM allocation and loads, 2D TMA tile loads.
+// Inline PTX only.
+//
+// Operand layouts used by the kernels (all bf16, 16-byte chunks):
+//   * K-major, 128-byte swizzle: a region of R rows x 64 K-values is R rows
+//     of 128 bytes, 8-row atoms of 1024 bytes (SBO = 1024); the 16-byte chunk
+//     j of row r sits in slot j ^ (r & 7) of its row; successive 16-value K
+//     steps inside the atom start 32 bytes apart.  A 2D TMA tile with a
+//     64-wide box and CU_TENSOR_MAP_SWIZZLE_128B writes exactly this.
+//   * MN-major, 128-byte swizzle: atoms of 8 K-rows x 64 M-values (1024
+//     bytes, chunk slots swizzled the same way), M-atoms LBO apart, 8-row K
+//     groups SBO apart: a TMA tile whose rows are K and whose 64-wide box
+//     runs along M.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace sffn {
+
+constexpr uint32_t SMEM_LAYOUT_NONE = 0;
+constexpr uint32_t SMEM_LAYOUT_SW128 = 2;
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), the fixed version field of this descriptor format
+// (bit 46), and the layout (swizzle) mode in bits 61..63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5),
+// bf16 A and B (bits 7-9, 10-12), A / B major-ness (bits 15, 16; 1 = MN-major),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// TMEM allocation (whole warp): the column base is written to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (whole warp; the
+// warp's lane quarter is encoded in bits 16.. of taddr).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Sum of n accumulators (stride `stride` columns) at 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld_sum(uint32_t taddr, int stride, int n, float (&v)[16]) {
+  tmem_ld16(taddr, v);
+  for (int a = 1; a < n; ++a) {
+    float w[16];
+    tmem_ld16(taddr + (uint32_t)(a * stride), w);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += w[i];
+  }
+}
+
+// 2D TMA tile load: box at (x = column, y = row) of the tensor map; the bytes
+// complete on `bar`.  x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_tile_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// Wait for an mbarrier phase for at most limit_ns, with no abort flag (used
+// to drain copies still in flight before a block exits).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+}  // namespace sffn

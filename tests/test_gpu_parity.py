@@ -326,3 +326,55 @@ def test_argument_errors():
     with pytest.raises(sffn.SffnError) as e:
         ffn.active_counts(3)
     assert e.value.code == sffn.SFFN_ERR_STATE
+
+
+# --------------------------------------------------------------------------- tensor-core batched path
+# bf16 standard-gate batches of >= 2 tokens run on the tensor cores (gate-up and
+# down kernels); these cases cover both unit-slice layouts (2 NU <= 128 stacks
+# W1 and W3 in one MMA, larger slices take two), ragged D and H, and every
+# padding of the token count to a multiple of 16.
+@pytest.mark.parametrize("D,H,B", [
+    (512, 2048, 2),      # slices of 16 units
+    (384, 1000, 16),     # ragged H, D not a multiple of 128
+    (520, 1500, 17),     # D not a multiple of 64: zero-filled K tail
+    (256, 10000, 33),    # slices of 72 units: W1 and W3 in separate MMAs
+    (256, 4000, 100),
+    (128, 3000, 128),
+])
+def test_tc_batched_shapes(D, H, B):
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=51)
+    x = syn.tokens(B, D, dtype="bf16", seed=52)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+def test_tc_batched_rsp_and_changing_batch():
+    """R-S+ activation, and consecutive calls whose token count changes the padded width."""
+    lw = syn.standard_layer(512, 3000, dtype="bf16", seed=53)
+    x = syn.tokens(64, 512, dtype="bf16", seed=54)
+    ffn = make_ffn(lw, act="rsp")
+    ref = reference(lw, x, act="rsp")
+    for B in (40, 3, 64, 17, 2):
+        y, c, m = run_tokens(ffn, x[:B], B=B)
+        sub = tuple(a[:B] for a in ref)
+        check(lw, x[:B], y, c, m, act="rsp", ref=sub)
+
+
+def test_tc_matches_cuda_core_batched_kernel(monkeypatch):
+    """The tensor-core path and the CUDA-core batched kernel agree on the same inputs."""
+    lw = syn.standard_layer(768, 2600, dtype="bf16", seed=55)
+    x = syn.tokens(12, 768, dtype="bf16", seed=56)
+    tc = make_ffn(lw)
+    y_tc, c_tc, m_tc = run_tokens(tc, x, B=12)
+    monkeypatch.setenv("SFFN_TC_MIN_BATCH", "1000")  # read when a handle is created
+    cc = make_ffn(lw)
+    y_cc, c_cc, m_cc = run_tokens(cc, x, B=12)
+    ref = check(lw, x, y_tc, c_tc, m_tc)
+    check(lw, x, y_cc, c_cc, m_cc, ref=ref)
+    z = ref[1]
+    sure = np.abs(z) > BAND
+    assert np.array_equal(m_tc[sure], m_cc[sure])
+    for b in range(12):
+        den = np.linalg.norm(ref[0][b])
+        assert np.linalg.norm(y_tc[b] - y_cc[b]) <= 2 * TOL["bf16"] * max(den, 1e-30)
