@@ -268,6 +268,7 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
       if ((e = cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if (const char* env = std::getenv("SFFN_TC_GATE_KB")) h->tc.gate_smem_budget = (size_t)std::atoi(env) * 1024;
       if (const char* env = std::getenv("SFFN_TC_DOWN_KB")) h->tc.down_smem_budget = (size_t)std::atoi(env) * 1024;
+      if (const char* env = std::getenv("SFFN_TC_GATE_CHUNKS")) h->tc.gate_chunks = std::max(1, std::min(4, std::atoi(env)));
       if ((e = cudaMemset(h->hbuf, 0, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))))
         return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);

@@ -90,8 +90,17 @@ __host__ __device__ constexpr uint32_t gate_stage_bytes(int C, int NU, int NB) {
 }
 __host__ __device__ constexpr uint32_t down_chunk_bytes(int NB) { return 2u * TC_UCH * 128u + 2u * (uint32_t)NB * 128u; }
 
+// Bytes an MMA may read past the last A region of the last stage: it reads
+// 128 rows (2 NU <= 128, W1 and W3 stacked) or MT rows from a chunk's start,
+// and what follows the last A region is the stage's x regions.
+__host__ __device__ inline uint32_t gate_slack_bytes(int C, int MT, int NU, int NB) {
+  const int rows = 2 * NU <= 128 ? 128 - 2 * NU : MT - NU;
+  const int over = rows * 128 - C * NB * 128;
+  return over > 0 ? (uint32_t)(over + 1023) / 1024 * 1024 : 0u;
+}
 size_t gate_smem_bytes(int C, int MT, int NU, int NB, int NS) {
-  return 1024 + (size_t)NS * gate_stage_bytes(C, NU, NB) + 128 * 128 + 8 * (2 * NS + 2) + 8 + 4 * NB + 64;
+  return 1024 + (size_t)NS * gate_stage_bytes(C, NU, NB) + gate_slack_bytes(C, MT, NU, NB) + 8 * (2 * NS + 2) + 8 +
+         4 * NB + 64;
 }
 size_t down_smem_bytes(int NB, int NS) {
   return 1024 + (size_t)NS * TC_DC * down_chunk_bytes(NB) + 8 * (2 * NS + 2) + 8 + 64;
@@ -121,9 +130,8 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   const int NS = p.NS, NB = p.NB, C = p.C;
   const uint32_t wreg = (uint32_t)p.NU * 128u, xreg = (uint32_t)NB * 128u;
   const uint32_t st_bytes = gate_stage_bytes(C, p.NU, NB);
-  // stages, then 128 rows of slack: an MMA reads 128 (or MT) rows from the start of a
-  // chunk that holds 2 NU
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes + 128 * 128);
+  // stages, then slack for the rows an MMA reads past the last A region
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes + gate_slack_bytes(C, MT, p.NU, NB));
   uint64_t* empty = full + NS;
   uint64_t* done = empty + NS;  // every MMA complete (one commit per MMA warp)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 2);
@@ -151,6 +159,10 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // Let the next kernel launch only once this block holds its TMEM: a later
   // kernel's blocks then never take the columns an earlier one still needs.
   if (tid == 0) pdl_launch_dependents();
+  const bool fused = 2 * p.NU <= 128;
+  const int ncol = fused ? NB : 2 * NB, ldc = ncol + 1;  // epilogue copy of the accumulator
+  float* s_acc = reinterpret_cast<float*>(sm);
+  int stage_ok = 1;
 
   if (warp == TC_PRODUCER_WARP) {
     // One TMA copy costs the issuing thread on the order of 100 ns, so the
@@ -200,7 +212,6 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   } else if (warp >= TC_GATE_MMA_WARP0) {
     const int mw = warp - TC_GATE_MMA_WARP0;  // this warp issues K steps kk = mw (mod nacc) into accumulator mw
     if (mw < p.nacc && lane == 0) {
-      const bool fused = 2 * p.NU <= 128;
       const uint32_t idesc = idesc_bf16_f32(fused ? 128 : MT, NB, false, false);
       const uint32_t acc_cols = fused ? (uint32_t)NB : 2u * NB;  // columns of one accumulator
       const uint32_t da = tmem + (uint32_t)mw * acc_cols;
@@ -229,17 +240,12 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ---- epilogue warps 0..3: warp q reads TMEM lanes 32q..32q+31 (summing
-    // the accumulators) into a shared [128 lanes][ncol] copy -- the stages are
-    // free once every MMA is done -- then thread (unit r, token group g) takes
-    // tokens g, g + 2, ... (units in rounds of 64): a warp shares each token, so
-    // counts are ballots.
+    // ---- warps 0..3: warp q copies TMEM lanes 32q..32q+31 (summing the
+    // accumulators) into a shared [128 lanes][ncol] array; the stages are free
+    // once every MMA is done
     pdl_wait();  // the outputs below may still be read by the previous forward
-    const bool fused = 2 * p.NU <= 128;
-    const int ncol = fused ? NB : 2 * NB, ldc = ncol + 1;
-    float* s_acc = reinterpret_cast<float*>(sm);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
-    if (ok) {
+    stage_ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
+    if (stage_ok) {
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
       float* row = s_acc + (size_t)(32 * warp + lane) * ldc;
@@ -250,12 +256,16 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
         for (int jj = 0; jj < 16; ++jj) row[c0 + jj] = v[jj];
       }
     }
-    named_barrier(1, 128);
-    for (int r0 = 0; ok && r0 < p.NU; r0 += 64) {
+  }
+  // ---- epilogue on warps 0..7: thread (unit r, token group g = tid / 64) takes
+  // tokens g, g + 4, ... (units in rounds of 64); a warp shares each token, so
+  // the counts are ballots
+  if (__syncthreads_and(stage_ok) && warp < 8) {
+    for (int r0 = 0; r0 < p.NU; r0 += 64) {
       const int r = r0 + (tid & 63), g = tid >> 6;
       const bool valid = r < p.NU && u0 + r < p.H;
       const int u = u0 + r;
-      for (int b = g; b < p.B; b += 2) {
+      for (int b = g; b < p.B; b += 4) {
         const float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
         const float pv = !valid ? 0.f : fused ? s_acc[(size_t)(p.NU + r) * ldc + b] : s_acc[(size_t)r * ldc + NB + b];
         const bool lv = valid && z > 0.f;
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
         }
       }
     }
-    named_barrier(1, 128);
+    named_barrier(1, 256);
     if (tid < p.B && s_cnt[tid]) atomicAdd(p.ctrl + CTRL_COUNT + tid, s_cnt[tid]);
   }
   tc_fence_before();
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int NS = p.NS, NB = p.NB;
-  const uint32_t half = TC_UCH * 128u, hreg = (uint32_t)NB * 128u, chb = down_chunk_bytes(NB);
+  const uint32_t half = TC_UCH * 128u, chb = down_chunk_bytes(NB);
   const uint32_t st_bytes = TC_DC * chb;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes);
   uint64_t* empty = full + NS;
@@ -499,6 +509,7 @@ TcPlan plan_ffn_tc(int D, int H, int num_sms) {
   p.nsplit = std::max(1, std::min(p.nch, num_sms / p.ndt));
   p.Hs = (H + 7) / 8 * 8;
   p.gate_smem_budget = TC_SMEM_BUDGET;
+  p.gate_chunks = 0;
   p.down_smem_budget = TC_SMEM_BUDGET;
   p.ok = true;
   return p;
@@ -540,7 +551,8 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   g.NB = NB;
   g.NU = plan.NU;
   g.KC = plan.KC;
-  g.C = 4;
+  // four K chunks per stage; two once x makes up a large part of a stage (measured)
+  g.C = plan.gate_chunks > 0 ? plan.gate_chunks : (NB >= 48 ? 2 : 4);
   while (g.C > 1 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, 2) > std::min(max_smem, (size_t)TC_SMEM_BUDGET)) g.C >>= 1;
   g.NCG = (plan.KC + g.C - 1) / g.C;
   g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.gate_smem_budget / gate_stage_bytes(g.C, plan.NU, NB)));

@@ -81,6 +81,7 @@ struct TcPlan {
   int ndt = 0, nch = 0, nsplit = 0;
   int Hs = 0;  // row stride (elements) of the h buffer
   size_t gate_smem_budget = 0, down_smem_budget = 0;  // pipeline-stage bytes per block
+  int gate_chunks = 0;                                // 64-wide K chunks per gate-up stage (0: 4)
 };
 struct TcMaps {
   CUtensorMap w1, w3;  // W1, W3 [H, D]: boxes of 64 columns x NU rows
