@@ -304,7 +304,12 @@ def batched_extras(ffns, layers, x, stream, args, peak):
                 sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
         tt = time_graph(g, stream, args.steps, args.warmup)
         us = 1e6 * tt / (args.steps * calls)
-        bytes_call = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
+        # The tensor-core path (bf16, standard gate, B >= 2) streams every unit slice of W1, W3
+        # and W2 (the union covers most units at these batch sizes) plus x, y and h (bf16 pair,
+        # written once, read once); union_gather_bytes is what a row-gathering design would read.
+        tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2"))
+        union_bytes = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
+        bytes_call = (3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H) if tc_path else union_bytes
         yd = torch.empty_like(x)
 
         def body():
@@ -320,11 +325,13 @@ def batched_extras(ffns, layers, x, stream, args, peak):
             body()
         td = time_graph(gd, stream, args.steps, args.warmup)
         usd = 1e6 * td / (args.steps * calls)
-        out[f"B{B}"] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,
-                        "union_fraction": mean_union / H, "gbs": bytes_call / (us * 1e3),
+        out[f"B{B}"] = {"path": "tensor cores: gate-up + down kernels" if tc_path else "CUDA cores, union gathers",
+                        "us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,
+                        "union_fraction": mean_union / H, "bytes_per_call": bytes_call,
+                        "union_gather_bytes": union_bytes, "gbs": bytes_call / (us * 1e3),
                         "frac_of_measured": bytes_call / (us * 1e3) / peak,
                         "dense_bf16_us_per_call": usd, "speedup_vs_dense_bf16": usd / us,
-                        "gpu_launches_per_call": 2 * ((B + 7) // 8)}
+                        "gpu_launches_per_call": 2 if tc_path else 2 * ((B + 7) // 8)}
         del g, gd
     return out
 
