@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 #pragma unroll
     for (int v = 0; v < VPC; ++v) yr[v] = fmaf(h, wf[v], yr[v]);
   };
+  uint4 r8[8];  // W2^T slices in flight
   for (int b0 = 0; b0 < n_live; b0 += RB) {
     const int nb = min(RB, n_live - b0);
     for (int i = tid; i < nb * nch; i += ST) {
@@ -324,7 +325,6 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       cp_async16(srows + i, W3 + (size_t)l_unit[b0 + u] * nch + c);
     }
     cp_async_commit();
-    uint4 r8[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m)
       r8[m] = (owns && m < nb) ? ld_stream(col + (size_t)l_unit[b0 + m] * nch) : make_uint4(0, 0, 0, 0);
@@ -351,15 +351,16 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 #pragma unroll
       for (int m = 0; m < 8; ++m)
         if (m < nb) fma_slice(r8[m], l_h[b0 + m]);
-      int j = 8;
-      for (; j + 4 <= nb; j += 4) {
-        uint4 r[4];
+      // the rest of the batch in predicated rounds of four loads in flight (a
+      // block with many live units sets the pace of the whole call)
+      for (int j = 8; j < nb; j += 4) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) r[m] = ld_stream(col + (size_t)l_unit[b0 + j + m] * nch);
+        for (int m = 0; m < 4; ++m)
+          r8[m] = j + m < nb ? ld_stream(col + (size_t)l_unit[b0 + j + m] * nch) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) fma_slice(r[m], l_h[b0 + j + m]);
+        for (int m = 0; m < 4; ++m)
+          if (j + m < nb) fma_slice(r8[m], l_h[b0 + j + m]);
       }
-      for (; j < nb; ++j) fma_slice(ld_stream(col + (size_t)l_unit[b0 + j] * nch), l_h[b0 + j]);
     }
     __syncthreads();  // the shared area is reused by the next batch
   }
@@ -376,15 +377,14 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 #pragma unroll
     for (int v = 0; v < VPC; ++v) yr[v] = 0.f;
     const uint4* col2 = col + 32;
-    int j = 0;
-    for (; j + 4 <= n_live; j += 4) {
-      uint4 r[4];
+    for (int j = 0; j < n_live; j += 8) {
 #pragma unroll
-      for (int m = 0; m < 4; ++m) r[m] = ld_stream(col2 + (size_t)l_unit[j + m] * nch);
+      for (int m = 0; m < 8; ++m)
+        r8[m] = j + m < n_live ? ld_stream(col2 + (size_t)l_unit[j + m] * nch) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) fma_slice(r[m], l_h[j + m]);
+      for (int m = 0; m < 8; ++m)
+        if (j + m < n_live) fma_slice(r8[m], l_h[j + m]);
     }
-    for (; j < n_live; ++j) fma_slice(ld_stream(col2 + (size_t)l_unit[j] * nch), l_h[j]);
 #pragma unroll
     for (int v = 0; v < VPC; v += 4)
       atomicAdd(reinterpret_cast<float4*>(yc + (size_t)(cs0 + 32 + lane) * VPC + v),
