@@ -49,6 +49,10 @@ def _bind(path):
         f = getattr(lib, name)
         f.restype = ip
         f.argtypes = [ip] * 6 + [vp] * 9
+    for name in ("oracle_ffn_dense_ex", "oracle_ffn_gate_first_ex"):
+        f = getattr(lib, name)
+        f.restype = ip
+        f.argtypes = [ip] * 7 + [ctypes.c_double] + [vp] * 9
     lib.oracle_num_threads.restype = ip
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -80,6 +84,10 @@ class Variant:
         return _call("oracle_ffn_gate_first", *a[:5], *a[5:11],
                      lambda B: np.full((B, a[1]), -1, dtype=np.int32), lib=self._lib)
 
+    def ffn_dense_ex(self, D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=1e-6):
+        return _call("oracle_ffn_dense_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
+                     lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps)
+
 
 def num_threads() -> int:
     """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
@@ -101,7 +109,7 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None):
+def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None, flags=None, eps=0.0):
     x = _as_input(x, dtype)
     B = x.size // D
     if x.size != B * D:
@@ -116,8 +124,9 @@ def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None):
     y = np.zeros((B, D), dtype=np.float64)
     n_live = np.zeros(B, dtype=np.int32)
     out = extra(B)
-    rc = getattr(lib or _load(), name)(D, H, r, act, dtype, B, _ptr(W1), _ptr(U), _ptr(V),
-                                _ptr(W3), _ptr(W2), _ptr(x), _ptr(y), _ptr(out), _ptr(n_live))
+    head = (D, H, r, act, dtype, B) if flags is None else (D, H, r, act, dtype, B, flags, float(eps))
+    rc = getattr(lib or _load(), name)(*head, _ptr(W1), _ptr(U), _ptr(V),
+                                       _ptr(W3), _ptr(W2), _ptr(x), _ptr(y), _ptr(out), _ptr(n_live))
     if rc != 0:
         raise RuntimeError(f"{name} failed with code {rc}")
     return y, out, n_live
@@ -133,3 +142,23 @@ def ffn_gate_first(D, H, r, act, dtype, W1, U, V, W3, W2, x):
     """Gate-first evaluation.  Returns (y[B,D] f64, idx[B,H] live set padded with -1, n_live[B])."""
     return _call("oracle_ffn_gate_first", D, H, r, act, dtype, W1, U, V, W3, W2, x,
                  lambda B: np.full((B, H), -1, dtype=np.int32))
+
+
+# Full low-rank gate of the pages ("LoPA Gating: moving the ceiling"): flags of the "_ex" forms.
+FLAG_TILED_G = 1      # z_i += x_{i mod D}  (G = tiled identity)
+FLAG_RMSNORM = 2      # t = RMSNorm(V x) = V x / sqrt(mean((V x)^2) + eps), no gain
+FLAG_DOUBLE_ACT = 4   # u = A(W3 x) instead of W3 x (either gate)
+RMSNORM_EPS = 1e-6
+
+
+def ffn_dense_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS):
+    """Dense definition with the full low-rank gate options.  Returns (y, z, n_live)."""
+    return _call("oracle_ffn_dense_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
+                 lambda B: np.zeros((B, H), dtype=np.float64), flags=flags, eps=eps)
+
+
+def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS):
+    """Gate-first evaluation with the full low-rank gate options.  Returns (y, idx, n_live)."""
+    return _call("oracle_ffn_gate_first_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
+                 lambda B: np.full((B, H), -1, dtype=np.int32), flags=flags, eps=eps)
+

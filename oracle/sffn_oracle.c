@@ -12,9 +12,16 @@
  * Definitions followed (one token x in R^D, hidden width H):
  *   z = W1 x                     standard gate,  W1 in R^{H x D}
  *   z = U (V x)                  low-rank gate,  U in R^{H x r}, V in R^{r x D}
- *                                (the UV part of W1 = G + UV; G, the RMSNorm
- *                                 between V and U and the double activation
- *                                 are not part of this path)
+ *                                (the UV part of W1 = G + UV)
+ *
+ * and, by flag (the "_ex" entry points), the pages' full low-rank form:
+ *   OR_FLAG_TILED_G    z_i += x_{i mod D}          G = the tiled identity T,
+ *                                                  (Tx)_i = x_{i mod D} (appendix,
+ *                                                  Figure 6 (c))
+ *   OR_FLAG_RMSNORM    V x -> RMSNorm(V x) = t / sqrt(mean_k t_k^2 + eps), no
+ *                      gain ("W1(x) = Gx + U RMSNorm(Vx)")
+ *   OR_FLAG_DOUBLE_ACT u = A(W3 x) instead of W3 x ("they apply the activation
+ *                      to the outputs of both W1 and W3"); either gate
  *   a = A(z)                     A = ReLU, or R-S+ (x*sigmoid(x) for x >= 0,
  *                                0 for x < 0)
  *   u = W3 x                     W3 in R^{H x D}
@@ -47,6 +54,9 @@
 #define OR_BF16 1
 #define OR_RELU 0
 #define OR_RSP 1
+#define OR_FLAG_TILED_G 1
+#define OR_FLAG_RMSNORM 2
+#define OR_FLAG_DOUBLE_ACT 4
 
 /* exact widening of one stored element to double */
 static double elem(const void* p, int dtype, size_t i) {
@@ -83,16 +93,24 @@ int oracle_num_threads(void) {
 #endif
 }
 
-static int check_args(int D, int H, int r, int act, int dtype, int B) {
+static int check_args(int D, int H, int r, int act, int dtype, int B, int flags, double eps) {
   if (D <= 0 || H <= 0 || r < 0 || B < 0) return -1;
   if (act != OR_RELU && act != OR_RSP) return -1;
   if (dtype != OR_F32 && dtype != OR_BF16) return -1;
+  if (flags & ~(OR_FLAG_TILED_G | OR_FLAG_RMSNORM | OR_FLAG_DOUBLE_ACT)) return -1;
+  if ((flags & (OR_FLAG_TILED_G | OR_FLAG_RMSNORM)) && r == 0) return -1; /* low-rank gate only */
+  if (!(eps >= 0.0)) return -1;
   return 0;
 }
 
+/* the up value of one unit: W3 x, or A(W3 x) with the double activation */
+static double up_value(int act, int flags, double u) {
+  return (flags & OR_FLAG_DOUBLE_ACT) ? activation(act, u) : u;
+}
+
 /* Gate pre-activations z[H] for one token xd[D] (already widened). */
-static int gate(int D, int H, int r, int dtype, const void* W1, const void* U,
-                const void* V, const double* xd, double* z) {
+static int gate(int D, int H, int r, int dtype, int flags, double eps, const void* W1,
+                const void* U, const void* V, const double* xd, double* z) {
   if (r == 0) {
     int bad = 0;
 #pragma omp parallel
@@ -112,7 +130,8 @@ static int gate(int D, int H, int r, int dtype, const void* W1, const void* U,
     }
     return bad ? -2 : 0;
   }
-  /* low-rank gate: t = V x (kept in double, not rounded), z = U t */
+  /* low-rank gate: t = V x (kept in double, not rounded), optionally
+     t <- t / sqrt(mean(t^2) + eps); z = U t, optionally + x_{i mod D} */
   double* t = (double*)malloc(sizeof(double) * (size_t)r);
   if (!t) return -2;
   int bad = 0;
@@ -129,11 +148,21 @@ static int gate(int D, int H, int r, int dtype, const void* W1, const void* U,
       widen_row(V, dtype, (size_t)k * D, D, row);
       t[k] = dot(row, xd, D);
     }
+#pragma omp single
+    {
+      if (flags & OR_FLAG_RMSNORM) {
+        double ss = 0.0;
+        for (int k = 0; k < r; ++k) ss += t[k] * t[k];
+        const double scale = 1.0 / sqrt(ss / (double)r + eps);
+        for (int k = 0; k < r; ++k) t[k] *= scale;
+      }
+    }
 #pragma omp for schedule(static)
     for (int i = 0; i < H; ++i) {
       if (!row) continue;
       widen_row(U, dtype, (size_t)i * r, r, row);
       z[i] = dot(row, t, r);
+      if (flags & OR_FLAG_TILED_G) z[i] += xd[i % D];
     }
     free(row);
   }
@@ -148,11 +177,11 @@ static int gate(int D, int H, int r, int dtype, const void* W1, const void* U,
  * n_live[B] (= |{i : z_i > 0}|, may be NULL).  Returns 0, or <0 on bad
  * arguments / allocation failure.
  */
-int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
-                     const void* W1, const void* U, const void* V,
-                     const void* W3, const void* W2, const void* x,
-                     double* y, double* z, int* n_live) {
-  if (check_args(D, H, r, act, dtype, B)) return -1;
+int oracle_ffn_dense_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps,
+                        const void* W1, const void* U, const void* V,
+                        const void* W3, const void* W2, const void* x,
+                        double* y, double* z, int* n_live) {
+  if (check_args(D, H, r, act, dtype, B, flags, eps)) return -1;
   double* xd = (double*)malloc(sizeof(double) * (size_t)D);
   double* zb = (double*)malloc(sizeof(double) * (size_t)H);
   double* g = (double*)malloc(sizeof(double) * (size_t)H);
@@ -163,7 +192,7 @@ int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
   int rc = 0;
   for (int b = 0; b < B && rc == 0; ++b) {
     widen_row(x, dtype, (size_t)b * D, D, xd);
-    rc = gate(D, H, r, dtype, W1, U, V, xd, zb);
+    rc = gate(D, H, r, dtype, flags, eps, W1, U, V, xd, zb);
     if (rc) break;
     int bad = 0;
 #pragma omp parallel
@@ -179,7 +208,7 @@ int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
         if (!row) continue;
         widen_row(W3, dtype, (size_t)i * D, D, row);
         double u = dot(row, xd, D);
-        g[i] = activation(act, zb[i]) * u;
+        g[i] = activation(act, zb[i]) * up_value(act, flags, u);
       }
       /* down projection: y_m = sum_i W2[m,i] g_i, i ascending */
 #pragma omp for schedule(static)
@@ -200,6 +229,13 @@ int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
   return rc;
 }
 
+int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
+                     const void* W1, const void* U, const void* V,
+                     const void* W3, const void* W2, const void* x,
+                     double* y, double* z, int* n_live) {
+  return oracle_ffn_dense_ex(D, H, r, act, dtype, B, 0, 0.0, W1, U, V, W3, W2, x, y, z, n_live);
+}
+
 /*
  * Gate-first evaluation: the gate over all units, then only the live set.
  *   S = {i : z_i > 0} in ascending order
@@ -208,11 +244,11 @@ int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
  * Same outputs and return codes as oracle_ffn_dense; idx[B*H] (may be NULL)
  * receives S for each token, padded with -1.
  */
-int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
-                          const void* W1, const void* U, const void* V,
-                          const void* W3, const void* W2, const void* x,
-                          double* y, int* idx, int* n_live) {
-  if (check_args(D, H, r, act, dtype, B)) return -1;
+int oracle_ffn_gate_first_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps,
+                             const void* W1, const void* U, const void* V,
+                             const void* W3, const void* W2, const void* x,
+                             double* y, int* idx, int* n_live) {
+  if (check_args(D, H, r, act, dtype, B, flags, eps)) return -1;
   double* xd = (double*)malloc(sizeof(double) * (size_t)D);
   double* zb = (double*)malloc(sizeof(double) * (size_t)H);
   double* h = (double*)malloc(sizeof(double) * (size_t)H);
@@ -224,7 +260,7 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
   int rc = 0;
   for (int b = 0; b < B && rc == 0; ++b) {
     widen_row(x, dtype, (size_t)b * D, D, xd);
-    rc = gate(D, H, r, dtype, W1, U, V, xd, zb);
+    rc = gate(D, H, r, dtype, flags, eps, W1, U, V, xd, zb);
     if (rc) break;
     int k = 0;
     for (int i = 0; i < H; ++i)
@@ -242,7 +278,7 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
         if (!row) continue;
         int i = S[q];
         widen_row(W3, dtype, (size_t)i * D, D, row);
-        h[q] = activation(act, zb[i]) * dot(row, xd, D);
+        h[q] = activation(act, zb[i]) * up_value(act, flags, dot(row, xd, D));
       }
 #pragma omp for schedule(static)
       for (int m = 0; m < D; ++m) {
@@ -261,4 +297,11 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
   }
   free(xd); free(zb); free(h); free(S);
   return rc;
+}
+
+int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
+                          const void* W1, const void* U, const void* V,
+                          const void* W3, const void* W2, const void* x,
+                          double* y, int* idx, int* n_live) {
+  return oracle_ffn_gate_first_ex(D, H, r, act, dtype, B, 0, 0.0, W1, U, V, W3, W2, x, y, idx, n_live);
 }

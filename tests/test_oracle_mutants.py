@@ -18,7 +18,7 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "sffn_oracle.c")
 MUTANTS = {
     "w2_transposed": ("widen_row(W2, dtype, (size_t)m * H, H, row);",
                       "for (int i2 = 0; i2 < H; ++i2) row[i2] = elem(W2, dtype, (size_t)i2 * D + m);"),
-    "w3_dropped": ("g[i] = activation(act, zb[i]) * u;", "g[i] = activation(act, zb[i]);"),
+    "w3_dropped": ("g[i] = activation(act, zb[i]) * up_value(act, flags, u);", "g[i] = activation(act, zb[i]);"),
     "gate_row_off_by_one": ("widen_row(W1, dtype, (size_t)i * D, D, row);",
                             "widen_row(W1, dtype, (size_t)((i + 1) % H) * D, D, row);"),
     "live_count_ge": ("cnt += (zb[i] > 0.0);", "cnt += (zb[i] >= 0.0);"),
@@ -32,6 +32,11 @@ MUTANTS = {
                      "for (int k2 = 0; k2 < r; ++k2) row[k2] = elem(U, dtype, (size_t)k2 * H + i);"),
     "gate_first_skips_first_live": ("for (int q = 0; q < k; ++q) {\n        if (!row) continue;",
                                     "for (int q = 1; q < k; ++q) {\n        if (!row) continue;"),
+    # the full low-rank gate
+    "tiled_g_index_shift": ("z[i] += xd[i % D];", "z[i] += xd[(i + 1) % D];"),
+    "rmsnorm_sum_not_mean": ("sqrt(ss / (double)r + eps)", "sqrt(ss + eps)"),
+    "rmsnorm_eps_outside_root": ("1.0 / sqrt(ss / (double)r + eps)", "1.0 / (sqrt(ss / (double)r) + eps)"),
+    "double_act_dropped": ("return (flags & OR_FLAG_DOUBLE_ACT) ? activation(act, u) : u;", "return u;"),
 }
 
 
@@ -101,6 +106,32 @@ def _pins(mod):
                             bits([0x3EAB, 0x3F80, 0x3F80]))
     h = 0.333984375 * (-2.0 * 0.333984375)
     check("bf16_bits", y[0].tolist() == [h, -2.0 * h, 0.333984375 * h])
+    # full low-rank gate (values derived in test_oracle_lopa_full)
+    f = lambda a: np.ascontiguousarray(a, dtype=np.float32)  # noqa: E731
+    rng = np.random.default_rng(21)
+    D, H, r, B = 8, 21, 4, 3
+    Ui = rng.integers(-2, 3, size=(H, r)).astype(np.float32)
+    Vi = rng.integers(-1, 2, size=(r, D)).astype(np.float32)
+    T = np.zeros((H, D), dtype=np.float32)
+    T[np.arange(H), np.arange(H) % D] = 1.0
+    G3 = f(rng.standard_normal((H, D)) / 3)
+    G2 = f(rng.standard_normal((D, H)) / 5)
+    xg = f(rng.standard_normal((B, D)))
+    yg, zg, _ = mod.ffn_dense_ex(D, H, r, oracle.RELU, oracle.F32, oracle.FLAG_TILED_G, None, f(Ui), f(Vi),
+                                 G3, G2, xg)
+    ys, zs, _ = mod.ffn_dense(D, H, 0, oracle.RELU, oracle.F32, f(T + Ui @ Vi), None, None, G3, G2, xg)
+    check("tiled_g_materialised", np.allclose(zg, zs, rtol=0, atol=1e-12) and np.allclose(yg, ys, rtol=1e-12))
+    Vh, Uh = f([[3.0, 0.0], [0.0, 4.0]]), f([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0], [-1.0, 0.0]])
+    _, zh, _ = mod.ffn_dense_ex(2, 4, 2, oracle.RELU, oracle.F32, oracle.FLAG_RMSNORM, None, Uh, Vh,
+                                f(np.ones((4, 2))), f(np.ones((2, 4))), f([[1.0, 1.0]]), 1e-6)
+    sh = math.sqrt(12.5 + 1e-6)
+    check("rmsnorm_hand", np.allclose(zh[0], [3 / sh, 4 / sh, 7 / sh, -3 / sh], rtol=1e-14, atol=0))
+    yp, _, _ = mod.ffn_dense_ex(D, H, 0, oracle.RELU, oracle.F32, oracle.FLAG_DOUBLE_ACT, f(T + Ui @ Vi), None,
+                                None, G3, G2, xg)
+    yn, _, _ = mod.ffn_dense_ex(D, H, 0, oracle.RELU, oracle.F32, oracle.FLAG_DOUBLE_ACT, f(T + Ui @ Vi), None,
+                                None, f(-G3), G2, xg)
+    check("double_act_relu_identity", np.allclose(yp - yn, ys, rtol=1e-12, atol=1e-13) and
+          not np.allclose(yp, ys))
     return failed
 
 
