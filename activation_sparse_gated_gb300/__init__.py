@@ -25,9 +25,10 @@ SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
 SFFN_ERR_TIMEOUT, SFFN_ERR_STATE, SFFN_ERR_NOMEM = -5, -6, -7
 SFFN_MAX_BATCH = 128
+SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT = 1, 2, 4
 
 #: every symbol include/sffn.h declares
-EXPORTS = ("sffn_create", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
+EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
            "sffn_active_mask", "sffn_synchronize", "sffn_destroy", "sffn_strerror",
            "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc")
 
@@ -52,6 +53,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, ip, cp = ctypes.c_void_p, ctypes.c_int, ctypes.c_char_p
     sig = {
         "sffn_create": (vp, [ip, ip, ip, ip, ip]),
+        "sffn_create_ex": (vp, [ip, ip, ip, ip, ip, ip]),
         "sffn_set_weights": (ip, [vp, vp, vp, vp, vp, vp]),
         "sffn_forward": (ip, [vp, vp, vp, ip, vp]),
         "sffn_active_counts": (ip, [vp, vp, ip]),
@@ -119,6 +121,13 @@ def sffn_create(D: int, H: int, r: int, act: int, dtype: int) -> int:
     return h
 
 
+def sffn_create_ex(D: int, H: int, r: int, act: int, dtype: int, flags: int) -> int:
+    h = load().sffn_create_ex(D, H, r, act, dtype, flags)
+    if not h:
+        raise SffnError(SFFN_ERR_ARG, sffn_last_error())
+    return h
+
+
 def sffn_set_weights(h, W1_or_U, V, W3, W2, stream=None):
     return _check(load().sffn_set_weights(h, _ptr(W1_or_U), _ptr(V), _ptr(W3), _ptr(W2), _stream(stream)))
 
@@ -163,17 +172,19 @@ def sffn_forward_noalloc(W1, W3, W2t, x, y, counts, D: int, H: int, B: int, act:
 class SparseFFN:
     """One FFN layer held by the library (a wrapper around one handle).
 
-    ``SparseFFN(D, H, r=0, act="relu", dtype="bf16")``; ``set_weights(W1_or_U, V,
+    ``SparseFFN(D, H, r=0, act="relu", dtype="bf16", flags=0)`` (flags: the
+    SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT options); ``set_weights(W1_or_U, V,
     W3, W2)`` with torch tensors in the layer's dtype (W2 as [D, H]);
     ``forward(x, y=None)`` with x [B, D] on the handle's device.
     """
 
-    def __init__(self, D: int, H: int, r: int = 0, act: str = "relu", dtype: str = "bf16"):
+    def __init__(self, D: int, H: int, r: int = 0, act: str = "relu", dtype: str = "bf16", flags: int = 0):
         self.D, self.H, self.r = D, H, r
         self.dtype = dtype
+        self.flags = flags
         self._act = {"relu": SFFN_ACT_RELU, "rsp": SFFN_ACT_RSP}[act]
         self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16}[dtype]
-        self.h = sffn_create(D, H, r, self._act, self._dt)
+        self.h = sffn_create_ex(D, H, r, self._act, self._dt, flags)
 
     def set_weights(self, W1_or_U, V, W3, W2, stream=None):
         for t in (W1_or_U, V, W3, W2):

@@ -41,6 +41,7 @@ void sffn::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s",
 
 struct sffn_s {
   int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
+  int flags = 0;  // SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT
   int device = 0, num_sms = 0;
   size_t max_smem = 0;
   void* gate_w = nullptr;  // W1[H, D] or U[H, r]
@@ -168,8 +169,21 @@ const char* sffn_strerror(int code) {
   }
 }
 
-sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
+sffn_t sffn_create(int D, int H, int r, int act, int dtype) { return sffn_create_ex(D, H, r, act, dtype, 0); }
+
+sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
   g_msg[0] = 0;
+  static_assert(SFFN_GATE_TILED_G == FLAG_TILED_G && SFFN_GATE_RMSNORM == FLAG_RMSNORM &&
+                    SFFN_DOUBLE_ACT == FLAG_DOUBLE_ACT,
+                "option bits of the ABI and of the kernels agree");
+  if (flags & ~(SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT)) {
+    fail(SFFN_ERR_ARG, "flags 0x%x has unknown bits", flags);
+    return nullptr;
+  }
+  if ((flags & (SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM)) && r == 0) {
+    fail(SFFN_ERR_ARG, "the tiled identity and RMSNorm options belong to the low-rank gate (r > 0)");
+    return nullptr;
+  }
   if (dtype != SFFN_F32 && dtype != SFFN_BF16) { fail(SFFN_ERR_ARG, "dtype %d unknown", dtype); return nullptr; }
   if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP) { fail(SFFN_ERR_ARG, "act %d unknown", act); return nullptr; }
   const int dmax = dtype == SFFN_BF16 ? SFFN_MAX_D_BF16 : SFFN_MAX_D_F32;
@@ -179,7 +193,7 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype) {
 
   sffn_s* h = new (std::nothrow) sffn_s;
   if (!h) { fail(SFFN_ERR_NOMEM, "host allocation failed"); return nullptr; }
-  h->D = D; h->H = H; h->r = r; h->act = act; h->dtype = dtype;
+  h->D = D; h->H = H; h->r = r; h->act = act; h->dtype = dtype; h->flags = flags;
   h->elt = dtype == SFFN_BF16 ? 2 : 4;
 
   auto bail = [&](int code, const char* what, cudaError_t e) -> sffn_t {
@@ -322,7 +336,8 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     // whole batch on the tensor cores: gate kernel, down kernel, finalize
     TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets};
     cudaError_t ce = cudaSuccess;
-    if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, kTimeoutNs, h->max_smem, s, &ce))
+    if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, kTimeoutNs, h->max_smem,
+                               s, &ce))
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
   }
@@ -350,6 +365,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.count_slot = b;
     p.rows_cap = h->stream_rows_cap;
     p.timeout_ns = kTimeoutNs;
+    p.flags = h->flags;
     if (nb == 1) {
       p.pref_rows = h->stream_plan.pref_rows;
       p.gather_rows = h->stream_plan.gather_rows;

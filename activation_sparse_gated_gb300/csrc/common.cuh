@@ -168,6 +168,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Options of the full low-rank gate ("LoPA Gating: moving the ceiling"),
+// the values of SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT:
+//   tiled identity G:  z_i += x_{i mod D}
+//   RMSNorm:           t = V x  ->  t / sqrt(mean(t^2) + eps), no gain
+//   double activation: the up value of a unit is A(W3 x) instead of W3 x
+constexpr int FLAG_TILED_G = 1;
+constexpr int FLAG_RMSNORM = 2;
+constexpr int FLAG_DOUBLE_ACT = 4;
+constexpr float RMSNORM_EPS = 1e-6f;
+
+// Element e of a vector staged as 16-byte chunks of its storage type.
+template <typename T>
+__device__ __forceinline__ float staged_elem(const uint4* v, int e);
+template <>
+__device__ __forceinline__ float staged_elem<float>(const uint4* v, int e) {
+  return reinterpret_cast<const float*>(v)[e];
+}
+template <>
+__device__ __forceinline__ float staged_elem<bf16_tag>(const uint4* v, int e) {
+  return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(v)[e] << 16);
+}
+
+// In place t_b <- t_b / sqrt(mean(t_b^2) + eps) for nb <= warps-per-block
+// vectors of k fp32 values in shared memory (warp b sums vector b).  Every
+// thread of the block calls it; scale[] holds nb floats of shared scratch.
+__device__ __forceinline__ void rmsnorm_shared(float* t, int nb, int k, float* scale, int nthreads) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < nb) {
+    float ss = 0.f;
+    for (int i = lane; i < k; i += 32) ss = fmaf(t[(size_t)warp * k + i], t[(size_t)warp * k + i], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) scale[warp] = 1.f / sqrtf(ss / (float)k + RMSNORM_EPS);
+  }
+  __syncthreads();
+  for (int i = tid; i < nb * k; i += nthreads) t[i] *= scale[i / k];
+  __syncthreads();
+}
+
 // The activation A on the gate.  Units with z <= 0 are dead for both.
 // R-S+ on the positive side is z * sigmoid(z) = z / (1 + e^-z).
 __device__ __forceinline__ float activation(int act, float z) {

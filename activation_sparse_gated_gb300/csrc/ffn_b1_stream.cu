@@ -216,8 +216,14 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   }
   cp_async_wait_all();
   __syncthreads();
+  if constexpr (LOPA) {
+    if (p.flags & FLAG_RMSNORM) rmsnorm_shared(ts, 1, p.gate_k, reinterpret_cast<float*>(misc + 2), ST);
+  }
 
   auto decide = [&](int q, float z) {  // z identical in every lane (butterfly sum)
+    if constexpr (LOPA) {
+      if (p.flags & FLAG_TILED_G) z += staged_elem<T>(xs, q % D);  // (G x)_q = x_{q mod D}
+    }
     const bool live = z > 0.f;
     if (lane == 0) {
       if (p.mask) p.mask[q] = live ? 1 : 0;
@@ -344,7 +350,7 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
         }
       }
       const float uval = warp_sum(a0 + a1);
-      if (lane == 0) l_h[b0 + u] = l_a[b0 + u] * uval;
+      if (lane == 0) l_h[b0 + u] = l_a[b0 + u] * ((p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, uval) : uval);
     }
     __syncthreads();
     if (owns) {

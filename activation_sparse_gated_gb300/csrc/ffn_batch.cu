@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   float* l_a = reinterpret_cast<float*>(l_unit + cap);  // [cap][NB]
   float* l_h = l_a + (size_t)cap * NB;                  // [cap][NB]
   int* misc = reinterpret_cast<int*>(l_h + (size_t)cap * NB);  // 0: list, 1: last, 2..: per-token counts
-  sp += al16((size_t)cap * (4 + 8 * NB) + 4 * (2 + NB));
+  float* rms_scale = reinterpret_cast<float*>(misc + 2 + NB);  // [NB] RMSNorm scratch
+  sp += al16((size_t)cap * (4 + 8 * NB) + 4 * (2 + 2 * NB));
   uint4* srows = reinterpret_cast<uint4*>(sp);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -149,9 +150,20 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   }
   cpa_wait();
   __syncthreads();
+  if constexpr (LOPA) {
+    if (p.flags & FLAG_RMSNORM) rmsnorm_shared(ts, nb, p.gate_k, rms_scale, BT);
+  }
 
   // a unit is kept if any token's gate is live; dead tokens get A(z) = 0
-  auto decide = [&](int q, const float (&z)[NB]) {
+  auto decide = [&](int q, const float (&z0)[NB]) {
+    float z[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      z[b] = z0[b];
+      if constexpr (LOPA) {
+        if ((p.flags & FLAG_TILED_G) && b < nb) z[b] += staged_elem<T>(xs + (size_t)b * nch, q % D);
+      }
+    }
     bool any = false;
 #pragma unroll
     for (int b = 0; b < NB; ++b) any |= (b < nb) && (z[b] > 0.f);
@@ -254,7 +266,9 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         const float uval = warp_sum(a2[b]);
-        if (lane == 0) l_h[(size_t)(b0 + u) * NB + b] = l_a[(size_t)(b0 + u) * NB + b] * uval;
+        if (lane == 0)
+          l_h[(size_t)(b0 + u) * NB + b] =
+              l_a[(size_t)(b0 + u) * NB + b] * ((p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, uval) : uval);
       }
     }
     __syncthreads();
@@ -327,7 +341,7 @@ BatchPlan plan_ffn_batch(int D, int gate_k, int elt_bytes, bool lopa, int rows_c
   const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 8) * row);
   pl.gather_rows = (int)std::max<size_t>(1, area / row);
   pl.smem = al16((size_t)nb_max * D * elt_bytes) + (lopa ? al16((size_t)nb_max * gate_k * 4) : 0) +
-            al16((size_t)rows_cap * (4 + 8 * nb_max) + 4 * (2 + nb_max)) + area;
+            al16((size_t)rows_cap * (4 + 8 * nb_max) + 4 * (2 + 2 * nb_max)) + area;
   return pl;
 }
 

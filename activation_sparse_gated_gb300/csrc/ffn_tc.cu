@@ -66,7 +66,7 @@ constexpr size_t TC_SMEM_BUDGET = 200 * 1024;
 constexpr int TC_NS_MAX = 8;
 
 struct TcGateArgs {
-  int D, H, B, NB, NU, KC, C, NCG, NS, act, Hs, nacc;
+  int D, H, B, NB, NU, KC, C, NCG, NS, act, Hs, nacc, flags;
   uint32_t tmem_cols;
   int* ctrl;
   uint8_t* mask;
@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
         if (lane == 0 && bal) atomicAdd(&s_cnt[b], __popc(bal));
         if (valid) {
           if (p.mask) p.mask[(size_t)b * p.H + u] = lv ? 1 : 0;
-          const float hv = lv ? activation(p.act, z) * pv : 0.f;
+          const float up = (p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, pv) : pv;
+          const float hv = lv ? activation(p.act, z) * up : 0.f;
           const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
           const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
           p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(hi);
@@ -537,7 +538,8 @@ cudaError_t ffn_tc_prepare(size_t max_smem) {
 }
 
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
-                  int B, int act, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err) {
+                  int B, int act, int flags, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
+                  cudaError_t* cuda_err) {
   *cuda_err = cudaSuccess;
   if (!plan.ok || B < 1 || B > 128) return -1;
   const int NB = (B + 15) / 16 * 16;
@@ -558,6 +560,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.gate_smem_budget / gate_stage_bytes(g.C, plan.NU, NB)));
   while (g.NS > 2 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS) > max_smem) --g.NS;
   g.act = act;
+  g.flags = flags;
   g.Hs = plan.Hs;
   {
     const int cols = 2 * plan.NU <= 128 ? NB : 2 * NB;  // one accumulator

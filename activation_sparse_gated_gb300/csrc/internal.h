@@ -29,6 +29,7 @@ struct B1Params {
   int pref_rows;          // streaming kernel: gate rows per block prefetched into shared memory
   int gather_rows;        // streaming kernel: W3 rows per gather batch (shared area / row)
   unsigned long long timeout_ns;
+  int flags = 0;          // FLAG_TILED_G | FLAG_RMSNORM (low-rank gate) | FLAG_DOUBLE_ACT
 };
 
 constexpr int B1_NWG = 8;                               // gate warps
@@ -106,7 +107,8 @@ cudaError_t ffn_tc_prepare(size_t max_smem);
 // Whole forward (y and counts written; no finalize kernel).  Returns 0 and sets
 // *cuda_err to the launch status, or a non-zero encode status.
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
-                  int B, int act, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
+                  int B, int act, int flags, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
+                  cudaError_t* cuda_err);
 
 // y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the
 // copies and publishes the nb live counts (chained behind a forward kernel).

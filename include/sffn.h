@@ -86,6 +86,28 @@ enum {
 sffn_t sffn_create(int D, int H, int r, int act, int dtype);
 
 /*
+ * Options of the pages' full low-rank gate ("LoPA Gating: moving the ceiling",
+ * W1(x) = Gx + U RMSNorm(Vx), with the activation applied to both W1 x and
+ * W3 x), combined with | in sffn_create_ex's flags:
+ *   SFFN_GATE_TILED_G  z_i += x_{i mod D}: G is the fixed tiled identity
+ *                      ("Model Casting and Low-Parameter Gating", appendix
+ *                      Figure 6 (c)); low-rank gate only
+ *   SFFN_GATE_RMSNORM  t = V x is replaced by t / sqrt(mean(t^2) + 1e-6), no
+ *                      gain (the pages give neither eps nor a gain); low-rank
+ *                      gate only
+ *   SFFN_DOUBLE_ACT    a unit's up value is A(W3 x) instead of W3 x; either gate
+ * The live test stays z_i > 0 on the (full) gate.
+ */
+enum { SFFN_GATE_TILED_G = 1, SFFN_GATE_RMSNORM = 2, SFFN_DOUBLE_ACT = 4 };
+
+/*
+ * sffn_create with options: flags is 0 or a combination of the values above.
+ * SFFN_ERR_ARG (NULL return) for unknown bits or a low-rank option with r == 0.
+ * sffn_create(D, H, r, act, dtype) is sffn_create_ex(D, H, r, act, dtype, 0).
+ */
+sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags);
+
+/*
  * Copy the layer's weights into the handle (host or device pointers, any
  * alignment, dtype of the handle):
  *   W1_or_U  W1[H, D] when r == 0, else U[H, r]

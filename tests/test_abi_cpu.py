@@ -41,7 +41,8 @@ def test_constants_match_header():
     text = open(HEADER).read()
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
-                 "SFFN_ERR_STATE", "SFFN_ERR_NOMEM"):
+                 "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
+                 "SFFN_DOUBLE_ACT"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
     assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
@@ -85,3 +86,11 @@ def test_noalloc_rejects_bad_sizes_on_host(lib):
         rc = lib.sffn_forward_noalloc(16, 16, 16, 16, 4096, None, D, H, B, 0, dt, None)
         assert rc == sffn.SFFN_ERR_ARG, (D, H, B, dt)
         assert "sffn_forward_noalloc" in sffn.sffn_last_error()
+
+
+@pytest.mark.parametrize("r,flags", [(64, 8), (64, -1), (0, sffn.SFFN_GATE_TILED_G), (0, sffn.SFFN_GATE_RMSNORM)])
+def test_create_ex_rejects_bad_options_before_touching_the_device(lib, r, flags):
+    """Unknown option bits, or a low-rank option without a low-rank gate."""
+    h = lib.sffn_create_ex(512, 1024, r, sffn.SFFN_ACT_RELU, sffn.SFFN_BF16, flags)
+    assert not h
+    assert "flags" in sffn.sffn_last_error() or "low-rank" in sffn.sffn_last_error()

@@ -378,3 +378,64 @@ def test_tc_matches_cuda_core_batched_kernel(monkeypatch):
     for b in range(12):
         den = np.linalg.norm(ref[0][b])
         assert np.linalg.norm(y_tc[b] - y_cc[b]) <= 2 * TOL["bf16"] * max(den, 1e-30)
+
+
+# --------------------------------------------------------------------------- the full low-rank gate
+# W1(x) = Gx + U RMSNorm(Vx) with the tiled identity G, and the double
+# activation ("LoPA Gating: moving the ceiling"): the same kernels with the
+# options of sffn_create_ex, against the oracle with the same options.
+TG, RN, DA = sffn.SFFN_GATE_TILED_G, sffn.SFFN_GATE_RMSNORM, sffn.SFFN_DOUBLE_ACT
+
+
+def make_ffn_ex(lw, flags, act="relu"):
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, act, lw.dtype, flags=flags)
+    w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
+    ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
+    return ffn
+
+
+def reference_ex(lw, x, flags, act="relu"):
+    v = {k: syn.oracle_view(t) for k, t in lw.tensors().items()}
+    a = oracle.RELU if act == "relu" else oracle.RSP
+    dt = oracle.F32 if lw.dtype == "f32" else oracle.BF16
+    return oracle.ffn_dense_ex(lw.D, lw.H, lw.r, a, dt, flags, v["W1"], v["U"], v["V"], v["W3"], v["W2"],
+                               syn.oracle_view(x))
+
+
+@pytest.mark.parametrize("flags", [TG, RN, DA, TG | RN, TG | RN | DA])
+@pytest.mark.parametrize("B", [1, 5])
+def test_full_lowrank_gate_options(flags, B):
+    lw = syn.lopa_layer(512, 2100, 64, dtype="bf16", seed=61)
+    x = syn.tokens(2 * B, 512, dtype="bf16", seed=62)
+    ffn = make_ffn_ex(lw, flags)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m, ref=reference_ex(lw, x, flags))
+
+
+@pytest.mark.parametrize("act", ["relu", "rsp"])
+def test_full_lowrank_gate_full_size_and_fp32(act):
+    """The pages' complete form at the low-rank workload's size (bf16), and in fp32."""
+    name = "lopa-bf16-D2560-H9787-r400-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, 6)
+    ffn = make_ffn_ex(lw, TG | RN | DA, act=act)
+    y, c, m = run_tokens(ffn, x)
+    check(lw, x, y, c, m, act=act, ref=reference_ex(lw, x, TG | RN | DA, act=act))
+    lw32 = syn.lopa_layer(384, 1200, 48, dtype="f32", seed=63)
+    x32 = syn.tokens(7, 384, dtype="f32", seed=64)
+    f32 = make_ffn_ex(lw32, TG | RN | DA, act=act)
+    for B in (1, 7):
+        y, c, m = run_tokens(f32, x32, B=B)
+        check(lw32, x32, y, c, m, act=act, ref=reference_ex(lw32, x32, TG | RN | DA, act=act))
+
+
+@pytest.mark.parametrize("B", [1, 6, 16])
+def test_double_activation_standard_gate(B):
+    """The double activation with the standard gate: streaming kernel (B = 1) and
+    the tensor-core path (B >= 2)."""
+    lw = syn.standard_layer(512, 2048, dtype="bf16", seed=65)
+    x = syn.tokens(B, 512, dtype="bf16", seed=66)
+    for act in ("relu", "rsp"):
+        ffn = make_ffn_ex(lw, DA, act=act)
+        y, c, m = run_tokens(ffn, x, B=B)
+        check(lw, x, y, c, m, act=act, ref=reference_ex(lw, x, DA, act=act))
