@@ -135,12 +135,19 @@ WORKLOADS = {
 
 
 def workload_layers(name: str, *, sets: int | None = None, gate: str | None = None,
-                    s: float | None = None):
-    """The weight sets of a named workload (CPU tensors)."""
+                    s: float | None = None, full_form: bool = False):
+    """The weight sets of a named workload (CPU tensors).
+
+    full_form: the low-rank layer is meant for the full gate Gx + U RMSNorm(Vx).
+    The tiled identity adds x_{i mod D} ~ N(0, 1) to every z_i, doubling the
+    variance of the unshifted gate, so the shift is scaled by sqrt(2) to keep
+    the same sparsity."""
     w = WORKLOADS[name]
     n = w["sets"] if sets is None else sets
     g = gate or (w["gate"] if isinstance(w["gate"], str) else "standard")
     shift = w.get("shift", SHIFT_90) if s is None else shift_for_sparsity(s)
+    if full_form:
+        shift *= math.sqrt(2.0)
     out = []
     for k in range(n):
         seed = 1000 * w["id"] + k

@@ -187,11 +187,11 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def build_ffns(layers, dev):
+def build_ffns(layers, dev, flags=0):
     import activation_sparse_gated_gb300 as sffn
     ffns = []
     for lw in layers:
-        f = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", lw.dtype)
+        f = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", lw.dtype, flags=flags)
         w = {k: (None if t is None else t.to(dev)) for k, t in lw.tensors().items()}
         f.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
         del w
@@ -452,6 +452,24 @@ def run_gpu(args):
                           "flop_ratio_eq4": flops.dense_macs(D, H) /
                           flops.lopa_macs(D, Hp, r, sum(lcounts) / len(lcounts))}
         del lffns, lg
+        # the pages' complete low-rank form: W1(x) = Gx + U RMSNorm(Vx), double activation
+        import activation_sparse_gated_gb300 as sffn_mod
+        full = sffn_mod.SFFN_GATE_TILED_G | sffn_mod.SFFN_GATE_RMSNORM | sffn_mod.SFFN_DOUBLE_ACT
+        del llayers
+        flayers = syn.workload_layers(LOPA_WORKLOAD, sets=lsets, full_form=True)
+        fffns = build_ffns(flayers, dev, flags=full)
+        fcounts = live_counts(fffns, lx, stream)
+        fbytes = sum(elt * r * (D + Hp) + 2 * elt * k * D + 2 * elt * D for k in fcounts)
+        fg = capture_step(fffns, lx, ly, stream)
+        ft = time_graph(fg, stream, args.steps, args.warmup)
+        fus = 1e6 * ft / (args.steps * li["tokens"])
+        extras["lopa_full_form"] = {"workload": LOPA_WORKLOAD + " + tiled G, RMSNorm(Vx), double activation",
+                                    "weight_sets": lsets, "us_per_call": fus, "tokens_per_s": 1e6 / fus,
+                                    "mean_live": sum(fcounts) / len(fcounts),
+                                    "gbs": fbytes * args.steps / (ft * 1e9),
+                                    "frac_of_measured": fbytes * args.steps / (ft * 1e9) / peak,
+                                    "speedup_vs_dense_bf16": us_dense / fus, "gpu_launches_per_call": 3}
+        del fffns, fg, flayers
         extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
 
     cpu = None
