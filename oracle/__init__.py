@@ -26,7 +26,7 @@ _SRC = os.path.join(_HERE, "sffn_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 F32, BF16 = 0, 1
-RELU, RSP = 0, 1
+RELU, RSP, SILU = 0, 1, 2
 
 _lib = None
 
@@ -52,7 +52,7 @@ def _bind(path):
     for name in ("oracle_ffn_dense_ex", "oracle_ffn_gate_first_ex"):
         f = getattr(lib, name)
         f.restype = ip
-        f.argtypes = [ip] * 7 + [ctypes.c_double] + [vp] * 9
+        f.argtypes = [ip] * 7 + [ctypes.c_double] * 2 + [vp] * 9
     lib.oracle_num_threads.restype = ip
     lib.oracle_num_threads.argtypes = []
     return lib
@@ -84,9 +84,10 @@ class Variant:
         return _call("oracle_ffn_gate_first", *a[:5], *a[5:11],
                      lambda B: np.full((B, a[1]), -1, dtype=np.int32), lib=self._lib)
 
-    def ffn_dense_ex(self, D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=1e-6):
+    def ffn_dense_ex(self, D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=1e-6, thr=0.0):
         return _call("oracle_ffn_dense_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
-                     lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps)
+                     lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps,
+                     thr=thr)
 
 
 def num_threads() -> int:
@@ -109,7 +110,7 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None, flags=None, eps=0.0):
+def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None, flags=None, eps=0.0, thr=0.0):
     x = _as_input(x, dtype)
     B = x.size // D
     if x.size != B * D:
@@ -124,7 +125,7 @@ def _call(name, D, H, r, act, dtype, W1, U, V, W3, W2, x, extra, lib=None, flags
     y = np.zeros((B, D), dtype=np.float64)
     n_live = np.zeros(B, dtype=np.int32)
     out = extra(B)
-    head = (D, H, r, act, dtype, B) if flags is None else (D, H, r, act, dtype, B, flags, float(eps))
+    head = (D, H, r, act, dtype, B) if flags is None else (D, H, r, act, dtype, B, flags, float(eps), float(thr))
     rc = getattr(lib or _load(), name)(*head, _ptr(W1), _ptr(U), _ptr(V),
                                        _ptr(W3), _ptr(W2), _ptr(x), _ptr(y), _ptr(out), _ptr(n_live))
     if rc != 0:
@@ -151,14 +152,15 @@ FLAG_DOUBLE_ACT = 4   # u = A(W3 x) instead of W3 x (either gate)
 RMSNORM_EPS = 1e-6
 
 
-def ffn_dense_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS):
-    """Dense definition with the full low-rank gate options.  Returns (y, z, n_live)."""
+def ffn_dense_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS, thr=0.0):
+    """Dense definition with the full low-rank gate options and a live threshold
+    (unit i is live iff |A(z_i)| > thr).  Returns (y, z, n_live)."""
     return _call("oracle_ffn_dense_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
-                 lambda B: np.zeros((B, H), dtype=np.float64), flags=flags, eps=eps)
+                 lambda B: np.zeros((B, H), dtype=np.float64), flags=flags, eps=eps, thr=thr)
 
 
-def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS):
-    """Gate-first evaluation with the full low-rank gate options.  Returns (y, idx, n_live)."""
+def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNORM_EPS, thr=0.0):
+    """Gate-first evaluation with the same options.  Returns (y, idx, n_live)."""
     return _call("oracle_ffn_gate_first_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
-                 lambda B: np.full((B, H), -1, dtype=np.int32), flags=flags, eps=eps)
+                 lambda B: np.full((B, H), -1, dtype=np.int32), flags=flags, eps=eps, thr=thr)
 

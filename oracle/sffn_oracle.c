@@ -22,8 +22,15 @@
  *                      gain ("W1(x) = Gx + U RMSNorm(Vx)")
  *   OR_FLAG_DOUBLE_ACT u = A(W3 x) instead of W3 x ("they apply the activation
  *                      to the outputs of both W1 and W3"); either gate
+ * and a live threshold thr >= 0 (the "_ex" entry points): unit i is live iff
+ * |A(z_i)| > thr, and a dead unit contributes exactly nothing ("treating
+ * anything below epsilon as zero").  With thr = 0 the ReLU and R-S+ live sets
+ * are {i : z_i > 0} as before; SiLU keeps every unit with z_i != 0.
  *   a = A(z)                     A = ReLU, or R-S+ (x*sigmoid(x) for x >= 0,
- *                                0 for x < 0)
+ *                                0 for x < 0), or SiLU (x*sigmoid(x) for every
+ *                                x: the smooth gate, "Model casting: compute the
+ *                                gate, then skip most of the FFN", sections on
+ *                                SiLU and on thresholding small values)
  *   u = W3 x                     W3 in R^{H x D}
  *   y = W2 (a .* u)              W2 in R^{D x H}
  *
@@ -35,7 +42,8 @@
  * Two evaluations are provided:
  *   oracle_ffn_dense      -- the formula above over all H units (the definition)
  *   oracle_ffn_gate_first -- the gate-first order the pages describe: compute
- *                            the gate, keep the live set S = {i : z_i > 0},
+ *                            the gate, keep the live set S = {i : z_i > 0}
+ *                            (|A(z_i)| > thr in the "_ex" forms),
  *                            evaluate W3 rows and W2 columns only for i in S.
  * The pages' claim (skipping dead units leaves y unchanged) says the two agree
  * exactly; the tests check that.
@@ -54,6 +62,7 @@
 #define OR_BF16 1
 #define OR_RELU 0
 #define OR_RSP 1
+#define OR_SILU 2
 #define OR_FLAG_TILED_G 1
 #define OR_FLAG_RMSNORM 2
 #define OR_FLAG_DOUBLE_ACT 4
@@ -78,11 +87,19 @@ static double dot(const double* a, const double* b, int n) {
   return s;
 }
 
-/* The activation A.  Both vanish for z <= 0, so the live test is z > 0. */
+/* The activation A.  ReLU and R-S+ vanish for z <= 0; SiLU is z * sigmoid(z)
+   everywhere. */
 static double activation(int act, double z) {
+  if (act == OR_SILU) return z / (1.0 + exp(-z));
   if (!(z > 0.0)) return 0.0;
   if (act == OR_RELU) return z;
   return z / (1.0 + exp(-z)); /* R-S+ on the positive side: z * sigmoid(z) */
+}
+
+/* the thresholded gate: A(z) when |A(z)| > thr (the unit is live), else 0 */
+static double gate_value(int act, double thr, double z) {
+  const double a = activation(act, z);
+  return fabs(a) > thr ? a : 0.0;
 }
 
 int oracle_num_threads(void) {
@@ -93,9 +110,10 @@ int oracle_num_threads(void) {
 #endif
 }
 
-static int check_args(int D, int H, int r, int act, int dtype, int B, int flags, double eps) {
+static int check_args(int D, int H, int r, int act, int dtype, int B, int flags, double eps, double thr) {
   if (D <= 0 || H <= 0 || r < 0 || B < 0) return -1;
-  if (act != OR_RELU && act != OR_RSP) return -1;
+  if (act != OR_RELU && act != OR_RSP && act != OR_SILU) return -1;
+  if (!(thr >= 0.0) || thr > 1e300) return -1;
   if (dtype != OR_F32 && dtype != OR_BF16) return -1;
   if (flags & ~(OR_FLAG_TILED_G | OR_FLAG_RMSNORM | OR_FLAG_DOUBLE_ACT)) return -1;
   if ((flags & (OR_FLAG_TILED_G | OR_FLAG_RMSNORM)) && r == 0) return -1; /* low-rank gate only */
@@ -177,11 +195,11 @@ static int gate(int D, int H, int r, int dtype, int flags, double eps, const voi
  * n_live[B] (= |{i : z_i > 0}|, may be NULL).  Returns 0, or <0 on bad
  * arguments / allocation failure.
  */
-int oracle_ffn_dense_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps,
+int oracle_ffn_dense_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps, double thr,
                         const void* W1, const void* U, const void* V,
                         const void* W3, const void* W2, const void* x,
                         double* y, double* z, int* n_live) {
-  if (check_args(D, H, r, act, dtype, B, flags, eps)) return -1;
+  if (check_args(D, H, r, act, dtype, B, flags, eps, thr)) return -1;
   double* xd = (double*)malloc(sizeof(double) * (size_t)D);
   double* zb = (double*)malloc(sizeof(double) * (size_t)H);
   double* g = (double*)malloc(sizeof(double) * (size_t)H);
@@ -208,7 +226,7 @@ int oracle_ffn_dense_ex(int D, int H, int r, int act, int dtype, int B, int flag
         if (!row) continue;
         widen_row(W3, dtype, (size_t)i * D, D, row);
         double u = dot(row, xd, D);
-        g[i] = activation(act, zb[i]) * up_value(act, flags, u);
+        g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);
       }
       /* down projection: y_m = sum_i W2[m,i] g_i, i ascending */
 #pragma omp for schedule(static)
@@ -221,7 +239,7 @@ int oracle_ffn_dense_ex(int D, int H, int r, int act, int dtype, int B, int flag
     }
     if (bad) { rc = -2; break; }
     int cnt = 0;
-    for (int i = 0; i < H; ++i) cnt += (zb[i] > 0.0);
+    for (int i = 0; i < H; ++i) cnt += (fabs(activation(act, zb[i])) > thr);
     if (n_live) n_live[b] = cnt;
     if (z) memcpy(z + (size_t)b * H, zb, sizeof(double) * (size_t)H);
   }
@@ -233,22 +251,22 @@ int oracle_ffn_dense(int D, int H, int r, int act, int dtype, int B,
                      const void* W1, const void* U, const void* V,
                      const void* W3, const void* W2, const void* x,
                      double* y, double* z, int* n_live) {
-  return oracle_ffn_dense_ex(D, H, r, act, dtype, B, 0, 0.0, W1, U, V, W3, W2, x, y, z, n_live);
+  return oracle_ffn_dense_ex(D, H, r, act, dtype, B, 0, 0.0, 0.0, W1, U, V, W3, W2, x, y, z, n_live);
 }
 
 /*
  * Gate-first evaluation: the gate over all units, then only the live set.
- *   S = {i : z_i > 0} in ascending order
+ *   S = {i : z_i > 0} in ascending order ({i : |A(z_i)| > thr} in the _ex form)
  *   h_i = A(z_i) * (W3[i,:] . x)          for i in S
  *   y_m = sum_{i in S} W2[m,i] h_i       (i ascending)
  * Same outputs and return codes as oracle_ffn_dense; idx[B*H] (may be NULL)
  * receives S for each token, padded with -1.
  */
-int oracle_ffn_gate_first_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps,
+int oracle_ffn_gate_first_ex(int D, int H, int r, int act, int dtype, int B, int flags, double eps, double thr,
                              const void* W1, const void* U, const void* V,
                              const void* W3, const void* W2, const void* x,
                              double* y, int* idx, int* n_live) {
-  if (check_args(D, H, r, act, dtype, B, flags, eps)) return -1;
+  if (check_args(D, H, r, act, dtype, B, flags, eps, thr)) return -1;
   double* xd = (double*)malloc(sizeof(double) * (size_t)D);
   double* zb = (double*)malloc(sizeof(double) * (size_t)H);
   double* h = (double*)malloc(sizeof(double) * (size_t)H);
@@ -264,7 +282,7 @@ int oracle_ffn_gate_first_ex(int D, int H, int r, int act, int dtype, int B, int
     if (rc) break;
     int k = 0;
     for (int i = 0; i < H; ++i)
-      if (zb[i] > 0.0) S[k++] = i;
+      if (fabs(activation(act, zb[i])) > thr) S[k++] = i;
     int bad = 0;
 #pragma omp parallel
     {
@@ -303,5 +321,5 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
                           const void* W1, const void* U, const void* V,
                           const void* W3, const void* W2, const void* x,
                           double* y, int* idx, int* n_live) {
-  return oracle_ffn_gate_first_ex(D, H, r, act, dtype, B, 0, 0.0, W1, U, V, W3, W2, x, y, idx, n_live);
+  return oracle_ffn_gate_first_ex(D, H, r, act, dtype, B, 0, 0.0, 0.0, W1, U, V, W3, W2, x, y, idx, n_live);
 }

@@ -18,10 +18,11 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "sffn_oracle.c")
 MUTANTS = {
     "w2_transposed": ("widen_row(W2, dtype, (size_t)m * H, H, row);",
                       "for (int i2 = 0; i2 < H; ++i2) row[i2] = elem(W2, dtype, (size_t)i2 * D + m);"),
-    "w3_dropped": ("g[i] = activation(act, zb[i]) * up_value(act, flags, u);", "g[i] = activation(act, zb[i]);"),
+    "w3_dropped": ("g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);",
+                   "g[i] = gate_value(act, thr, zb[i]);"),
     "gate_row_off_by_one": ("widen_row(W1, dtype, (size_t)i * D, D, row);",
                             "widen_row(W1, dtype, (size_t)((i + 1) % H) * D, D, row);"),
-    "live_count_ge": ("cnt += (zb[i] > 0.0);", "cnt += (zb[i] >= 0.0);"),
+    "live_count_ge": ("cnt += (fabs(activation(act, zb[i])) > thr);", "cnt += (fabs(activation(act, zb[i])) >= thr);"),
     "activation_wrong_side": ("if (!(z > 0.0)) return 0.0;", "if (!(z < 0.0)) return 0.0;"),
     "rsp_sigmoid_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     "rsp_missing_z": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
@@ -37,6 +38,11 @@ MUTANTS = {
     "rmsnorm_sum_not_mean": ("sqrt(ss / (double)r + eps)", "sqrt(ss + eps)"),
     "rmsnorm_eps_outside_root": ("1.0 / sqrt(ss / (double)r + eps)", "1.0 / (sqrt(ss / (double)r) + eps)"),
     "double_act_dropped": ("return (flags & OR_FLAG_DOUBLE_ACT) ? activation(act, u) : u;", "return u;"),
+    # SiLU and the live threshold
+    "silu_negative_side_zeroed": ("if (act == OR_SILU) return z / (1.0 + exp(-z));", ""),
+    "threshold_not_absolute": ("return fabs(a) > thr ? a : 0.0;", "return a > thr ? a : 0.0;"),
+    "threshold_ignored_in_dense": ("g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);",
+                                   "g[i] = activation(act, zb[i]) * up_value(act, flags, u);"),
 }
 
 
@@ -132,6 +138,22 @@ def _pins(mod):
                                 None, f(-G3), G2, xg)
     check("double_act_relu_identity", np.allclose(yp - yn, ys, rtol=1e-12, atol=1e-13) and
           not np.allclose(yp, ys))
+    # SiLU at threshold 0 is the dense SwiGLU product (torch's silu in fp64)
+    D, H, B = 10, 26, 3
+    S1, S3 = f(rng.standard_normal((H, D))), f(rng.standard_normal((H, D)))
+    S2, xs = f(rng.standard_normal((D, H))), f(rng.standard_normal((B, D)))
+    y0, _, n0 = mod.ffn_dense_ex(D, H, 0, oracle.SILU, oracle.F32, 0, S1, None, None, S3, S2, xs, 1e-6, 0.0)
+    d = [torch.from_numpy(a.astype(np.float64)) for a in (S1, S3, S2, xs)]
+    want = (torch.nn.functional.silu(d[3] @ d[0].T) * (d[3] @ d[1].T)) @ d[2].T
+    check("silu_swiglu_library", np.allclose(y0, want.numpy(), rtol=1e-12, atol=1e-12) and (n0 == H).all())
+    # a threshold keeps |A(z)| > thr: the error is at most thr * sum_i |W2[m,i]| |u_i|
+    thr = 0.3
+    yt, zt, nt = mod.ffn_dense_ex(D, H, 0, oracle.SILU, oracle.F32, 0, S1, None, None, S3, S2, xs, 1e-6, thr)
+    u = (d[3] @ d[1].T).numpy()
+    bound = thr * (np.abs(u) @ np.abs(d[2].numpy()).T)
+    a = torch.nn.functional.silu(torch.from_numpy(zt)).numpy()
+    check("threshold_error_bound", (np.abs(yt - y0) <= bound + 1e-12).all() and
+          (nt == (np.abs(a) > thr).sum(axis=1)).all() and (nt < H).all() and not np.allclose(yt, y0))
     return failed
 
 
