@@ -20,7 +20,7 @@ import os
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsffn.so")
 
 SFFN_F32, SFFN_BF16 = 0, 1
-SFFN_ACT_RELU, SFFN_ACT_RSP = 0, 1
+SFFN_ACT_RELU, SFFN_ACT_RSP, SFFN_ACT_SILU = 0, 1, 2
 SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
 SFFN_ERR_TIMEOUT, SFFN_ERR_STATE, SFFN_ERR_NOMEM = -5, -6, -7
@@ -28,7 +28,7 @@ SFFN_MAX_BATCH = 128
 SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT = 1, 2, 4
 
 #: every symbol include/sffn.h declares
-EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
+EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_live_threshold", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
            "sffn_active_mask", "sffn_synchronize", "sffn_destroy", "sffn_strerror",
            "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc")
 
@@ -54,6 +54,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "sffn_create": (vp, [ip, ip, ip, ip, ip]),
         "sffn_create_ex": (vp, [ip, ip, ip, ip, ip, ip]),
+        "sffn_set_live_threshold": (ip, [vp, ctypes.c_float]),
         "sffn_set_weights": (ip, [vp, vp, vp, vp, vp, vp]),
         "sffn_forward": (ip, [vp, vp, vp, ip, vp]),
         "sffn_active_counts": (ip, [vp, vp, ip]),
@@ -128,6 +129,10 @@ def sffn_create_ex(D: int, H: int, r: int, act: int, dtype: int, flags: int) -> 
     return h
 
 
+def sffn_set_live_threshold(h, thr: float):
+    return _check(load().sffn_set_live_threshold(h, float(thr)))
+
+
 def sffn_set_weights(h, W1_or_U, V, W3, W2, stream=None):
     return _check(load().sffn_set_weights(h, _ptr(W1_or_U), _ptr(V), _ptr(W3), _ptr(W2), _stream(stream)))
 
@@ -182,7 +187,7 @@ class SparseFFN:
         self.D, self.H, self.r = D, H, r
         self.dtype = dtype
         self.flags = flags
-        self._act = {"relu": SFFN_ACT_RELU, "rsp": SFFN_ACT_RSP}[act]
+        self._act = {"relu": SFFN_ACT_RELU, "rsp": SFFN_ACT_RSP, "silu": SFFN_ACT_SILU}[act]
         self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16}[dtype]
         self.h = sffn_create_ex(D, H, r, self._act, self._dt, flags)
 
@@ -213,6 +218,10 @@ class SparseFFN:
 
     def synchronize(self):
         sffn_synchronize(self.h)
+
+    def set_live_threshold(self, thr: float):
+        """Units with |A(z)| <= thr are skipped (0: the exact skip of ReLU / R-S+)."""
+        sffn_set_live_threshold(self.h, thr)
 
     def close(self):
         if getattr(self, "h", None):

@@ -42,6 +42,7 @@ void sffn::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s",
 struct sffn_s {
   int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
   int flags = 0;  // SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT
+  float thr = 0.f;  // live iff |A(z)| > thr (sffn_set_live_threshold)
   int device = 0, num_sms = 0;
   size_t max_smem = 0;
   void* gate_w = nullptr;  // W1[H, D] or U[H, r]
@@ -185,7 +186,10 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     return nullptr;
   }
   if (dtype != SFFN_F32 && dtype != SFFN_BF16) { fail(SFFN_ERR_ARG, "dtype %d unknown", dtype); return nullptr; }
-  if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP) { fail(SFFN_ERR_ARG, "act %d unknown", act); return nullptr; }
+  if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP && act != SFFN_ACT_SILU) {
+    fail(SFFN_ERR_ARG, "act %d unknown", act);
+    return nullptr;
+  }
   const int dmax = dtype == SFFN_BF16 ? SFFN_MAX_D_BF16 : SFFN_MAX_D_F32;
   if (D < 8 || D % 8 != 0 || D > dmax) { fail(SFFN_ERR_ARG, "D=%d must be a multiple of 8 in [8, %d]", D, dmax); return nullptr; }
   if (H < 1) { fail(SFFN_ERR_ARG, "H=%d must be >= 1", H); return nullptr; }
@@ -336,8 +340,8 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     // whole batch on the tensor cores: gate kernel, down kernel, finalize
     TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets};
     cudaError_t ce = cudaSuccess;
-    if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, kTimeoutNs, h->max_smem,
-                               s, &ce))
+    if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, h->thr, kTimeoutNs,
+                               h->max_smem, s, &ce))
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
   }
@@ -366,6 +370,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.rows_cap = h->stream_rows_cap;
     p.timeout_ns = kTimeoutNs;
     p.flags = h->flags;
+    p.thr = h->thr;
     if (nb == 1) {
       p.pref_rows = h->stream_plan.pref_rows;
       p.gather_rows = h->stream_plan.gather_rows;
@@ -405,6 +410,13 @@ int sffn_active_mask(sffn_t h, uint8_t* mask_host, int B) {
   if (B != h->last_B) return fail(SFFN_ERR_ARG, "B=%d but the last forward had B=%d", B, h->last_B);
   if (int rc = sync_and_check(h)) return rc;
   SFFN_CUDA(cudaMemcpy(mask_host, h->mask, (size_t)B * h->H, cudaMemcpyDeviceToHost));
+  return SFFN_OK;
+}
+
+int sffn_set_live_threshold(sffn_t h, float thr) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (!(thr >= 0.f) || thr > 3.0e38f) return fail(SFFN_ERR_ARG, "threshold %g must be finite and >= 0", (double)thr);
+  h->thr = thr;
   return SFFN_OK;
 }
 

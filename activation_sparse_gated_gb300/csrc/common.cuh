@@ -207,12 +207,18 @@ __device__ __forceinline__ void rmsnorm_shared(float* t, int nb, int k, float* s
   __syncthreads();
 }
 
-// The activation A on the gate.  Units with z <= 0 are dead for both.
-// R-S+ on the positive side is z * sigmoid(z) = z / (1 + e^-z).
+// The activation A on the gate: ReLU (0), R-S+ (1: z * sigmoid(z) = z / (1 + e^-z)
+// for z > 0, else 0) and the smooth SiLU (2: z * sigmoid(z) everywhere).
+constexpr int ACT_SILU = 2;
 __device__ __forceinline__ float activation(int act, float z) {
+  if (act == ACT_SILU) return z / (1.f + expf(-z));
   if (!(z > 0.f)) return 0.f;
   if (act == 0) return z;
   return z / (1.f + expf(-z));
 }
+
+// A unit is live when |A(z)| exceeds the handle's threshold (0 by default,
+// which for ReLU and R-S+ is z > 0).
+__device__ __forceinline__ bool is_live(float a, float thr) { return fabsf(a) > thr; }
 
 }  // namespace sffn

@@ -148,7 +148,10 @@ __device__ __forceinline__ float row_dot(uint4 (&w)[PIECE], const uint4* row, co
   return warp_sum(acc);
 }
 
-template <typename T, bool LOPA>
+// EXT: the options of the full low-rank gate, the smooth gate or a live
+// threshold are in use.  The plain instantiation keeps the hot loops free of
+// their registers (the kernel runs at its register cap).
+template <typename T, bool LOPA, bool EXT>
 __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) {
   using E = Elt<T>;
   constexpr int VPC = E::VPC;
@@ -216,21 +219,29 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   }
   cp_async_wait_all();
   __syncthreads();
-  if constexpr (LOPA) {
+  if constexpr (LOPA && EXT) {
     if (p.flags & FLAG_RMSNORM) rmsnorm_shared(ts, 1, p.gate_k, reinterpret_cast<float*>(misc + 2), ST);
   }
 
   auto decide = [&](int q, float z) {  // z identical in every lane (butterfly sum)
-    if constexpr (LOPA) {
+    if constexpr (LOPA && EXT) {
       if (p.flags & FLAG_TILED_G) z += staged_elem<T>(xs, q % D);  // (G x)_q = x_{q mod D}
     }
-    const bool live = z > 0.f;
+    bool live;
+    float a;
+    if constexpr (EXT) {
+      a = activation(p.act, z);
+      live = is_live(a, p.thr);
+    } else {  // ReLU or R-S+, threshold 0: live iff z > 0
+      live = z > 0.f;
+      a = live ? activation(p.act, z) : 0.f;
+    }
     if (lane == 0) {
       if (p.mask) p.mask[q] = live ? 1 : 0;
       if (live) {  // compaction: append to the block's live list
         const int j = atomicAdd(misc, 1);
         l_unit[j] = q;
-        l_a[j] = activation(p.act, z);
+        l_a[j] = a;
       }
     }
     if (live) {  // both gathered rows of the unit start moving into L2 now
@@ -350,7 +361,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
         }
       }
       const float uval = warp_sum(a0 + a1);
-      if (lane == 0) l_h[b0 + u] = l_a[b0 + u] * ((p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, uval) : uval);
+      if (lane == 0)
+        l_h[b0 + u] = l_a[b0 + u] * ((EXT && (p.flags & FLAG_DOUBLE_ACT)) ? activation(p.act, uval) : uval);
     }
     __syncthreads();
     if (owns) {
@@ -417,8 +429,11 @@ StreamPlan plan_ffn_b1_stream(int D, int gate_k, int elt_bytes, bool lopa, int r
 }
 
 cudaError_t ffn_b1_stream_prepare(size_t max_smem) {
-  void (*ks[4])(const B1Params) = {ffn_b1_stream_kernel<float, false>, ffn_b1_stream_kernel<float, true>,
-                                   ffn_b1_stream_kernel<bf16_tag, false>, ffn_b1_stream_kernel<bf16_tag, true>};
+  void (*ks[8])(const B1Params) = {
+      ffn_b1_stream_kernel<float, false, false>,    ffn_b1_stream_kernel<float, true, false>,
+      ffn_b1_stream_kernel<bf16_tag, false, false>, ffn_b1_stream_kernel<bf16_tag, true, false>,
+      ffn_b1_stream_kernel<float, false, true>,     ffn_b1_stream_kernel<float, true, true>,
+      ffn_b1_stream_kernel<bf16_tag, false, true>,  ffn_b1_stream_kernel<bf16_tag, true, true>};
   for (auto k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -432,11 +447,19 @@ int ffn_b1_stream_threads() { return ST; }
 cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
                                  cudaStream_t s) {
   const dim3 g(grid), b(ST);
-  if (dtype == 0)
-    return lopa ? launch_pdl(ffn_b1_stream_kernel<float, true>, g, b, smem, s, p)
-                : launch_pdl(ffn_b1_stream_kernel<float, false>, g, b, smem, s, p);
-  return lopa ? launch_pdl(ffn_b1_stream_kernel<bf16_tag, true>, g, b, smem, s, p)
-              : launch_pdl(ffn_b1_stream_kernel<bf16_tag, false>, g, b, smem, s, p);
+  const bool ext = p.flags != 0 || p.act == ACT_SILU || p.thr != 0.f;
+  if (dtype == 0) {
+    if (ext)
+      return lopa ? launch_pdl(ffn_b1_stream_kernel<float, true, true>, g, b, smem, s, p)
+                  : launch_pdl(ffn_b1_stream_kernel<float, false, true>, g, b, smem, s, p);
+    return lopa ? launch_pdl(ffn_b1_stream_kernel<float, true, false>, g, b, smem, s, p)
+                : launch_pdl(ffn_b1_stream_kernel<float, false, false>, g, b, smem, s, p);
+  }
+  if (ext)
+    return lopa ? launch_pdl(ffn_b1_stream_kernel<bf16_tag, true, true>, g, b, smem, s, p)
+                : launch_pdl(ffn_b1_stream_kernel<bf16_tag, false, true>, g, b, smem, s, p);
+  return lopa ? launch_pdl(ffn_b1_stream_kernel<bf16_tag, true, false>, g, b, smem, s, p)
+              : launch_pdl(ffn_b1_stream_kernel<bf16_tag, false, false>, g, b, smem, s, p);
 }
 
 }  // namespace sffn

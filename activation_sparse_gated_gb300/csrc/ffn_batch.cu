@@ -164,22 +164,29 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
         if ((p.flags & FLAG_TILED_G) && b < nb) z[b] += staged_elem<T>(xs + (size_t)b * nch, q % D);
       }
     }
+    float av[NB];  // A(z), zero where the token's unit is dead
+    bool lv[NB];
     bool any = false;
 #pragma unroll
-    for (int b = 0; b < NB; ++b) any |= (b < nb) && (z[b] > 0.f);
+    for (int b = 0; b < NB; ++b) {
+      av[b] = b < nb ? activation(p.act, z[b]) : 0.f;
+      lv[b] = b < nb && is_live(av[b], p.thr);
+      if (!lv[b]) av[b] = 0.f;
+      any |= lv[b];
+    }
     if (lane == 0) {
       if (p.mask) {
 #pragma unroll
         for (int b = 0; b < NB; ++b)
-          if (b < nb) p.mask[(size_t)b * p.H + q] = z[b] > 0.f ? 1 : 0;
+          if (b < nb) p.mask[(size_t)b * p.H + q] = lv[b] ? 1 : 0;
       }
       if (any) {
         const int j = atomicAdd(misc, 1);
         l_unit[j] = q;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          l_a[(size_t)j * NB + b] = (b < nb) ? activation(p.act, z[b]) : 0.f;
-          if (b < nb && z[b] > 0.f) atomicAdd(misc + 2 + b, 1);
+          l_a[(size_t)j * NB + b] = av[b];
+          if (lv[b]) atomicAdd(misc + 2 + b, 1);
         }
       }
     }

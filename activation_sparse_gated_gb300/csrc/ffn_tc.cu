@@ -67,6 +67,7 @@ constexpr int TC_NS_MAX = 8;
 
 struct TcGateArgs {
   int D, H, B, NB, NU, KC, C, NCG, NS, act, Hs, nacc, flags;
+  float thr;  // live iff |A(z)| > thr
   uint32_t tmem_cols;
   int* ctrl;
   uint8_t* mask;
@@ -268,13 +269,14 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       for (int b = g; b < p.B; b += 4) {
         const float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
         const float pv = !valid ? 0.f : fused ? s_acc[(size_t)(p.NU + r) * ldc + b] : s_acc[(size_t)r * ldc + NB + b];
-        const bool lv = valid && z > 0.f;
+        const float az = activation(p.act, z);
+        const bool lv = valid && is_live(az, p.thr);
         const unsigned bal = __ballot_sync(0xffffffffu, lv);
         if (lane == 0 && bal) atomicAdd(&s_cnt[b], __popc(bal));
         if (valid) {
           if (p.mask) p.mask[(size_t)b * p.H + u] = lv ? 1 : 0;
           const float up = (p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, pv) : pv;
-          const float hv = lv ? activation(p.act, z) * up : 0.f;
+          const float hv = lv ? az * up : 0.f;
           const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
           const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
           p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(hi);
@@ -538,7 +540,7 @@ cudaError_t ffn_tc_prepare(size_t max_smem) {
 }
 
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
-                  int B, int act, int flags, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
+                  int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
                   cudaError_t* cuda_err) {
   *cuda_err = cudaSuccess;
   if (!plan.ok || B < 1 || B > 128) return -1;
@@ -561,6 +563,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   while (g.NS > 2 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS) > max_smem) --g.NS;
   g.act = act;
   g.flags = flags;
+  g.thr = thr;
   g.Hs = plan.Hs;
   {
     const int cols = 2 * plan.NU <= 128 ? NB : 2 * NB;  // one accumulator

@@ -30,6 +30,7 @@ struct B1Params {
   int gather_rows;        // streaming kernel: W3 rows per gather batch (shared area / row)
   unsigned long long timeout_ns;
   int flags = 0;          // FLAG_TILED_G | FLAG_RMSNORM (low-rank gate) | FLAG_DOUBLE_ACT
+  float thr = 0.f;        // live iff |A(z)| > thr
 };
 
 constexpr int B1_NWG = 8;                               // gate warps
@@ -107,7 +108,7 @@ cudaError_t ffn_tc_prepare(size_t max_smem);
 // Whole forward (y and counts written; no finalize kernel).  Returns 0 and sets
 // *cuda_err to the launch status, or a non-zero encode status.
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
-                  int B, int act, int flags, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
+                  int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
                   cudaError_t* cuda_err);
 
 // y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the

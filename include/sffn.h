@@ -51,7 +51,7 @@ enum { SFFN_F32 = 0, SFFN_BF16 = 1 };
 
 /* activation A: ReLU, or R-S+ (z * sigmoid(z) for z >= 0, 0 for z < 0;
    "Model casting: make sparsity a target") */
-enum { SFFN_ACT_RELU = 0, SFFN_ACT_RSP = 1 };
+enum { SFFN_ACT_RELU = 0, SFFN_ACT_RSP = 1, SFFN_ACT_SILU = 2 };
 
 enum {
   SFFN_OK = 0,
@@ -77,7 +77,8 @@ enum {
  *   H      hidden width (H' for the low-rank gate), any H >= 1
  *   r      0 for the standard gate W1; r > 0 selects the low-rank gate U(Vx)
  *          with rank r, r % 8 == 0, r <= D
- *   act    SFFN_ACT_RELU or SFFN_ACT_RSP
+ *   act    SFFN_ACT_RELU, SFFN_ACT_RSP, or SFFN_ACT_SILU (z sigmoid(z) for every
+ *          z: the smooth gate, never exactly zero; see sffn_set_live_threshold)
  *   dtype  SFFN_F32 or SFFN_BF16
  * Returns NULL on error (see sffn_last_error()).  Allocates device memory:
  * 3*H*D (+ r*D + H*r) elements of weights plus O(B_max * (D + r + H)) bytes of
@@ -106,6 +107,18 @@ enum { SFFN_GATE_TILED_G = 1, SFFN_GATE_RMSNORM = 2, SFFN_DOUBLE_ACT = 4 };
  * sffn_create(D, H, r, act, dtype) is sffn_create_ex(D, H, r, act, dtype, 0).
  */
 sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags);
+
+/*
+ * Live threshold (default 0): unit i is live -- its W3 row and W2 column are
+ * read -- iff |A(z_i)| > thr; a dead unit contributes exactly nothing.  With
+ * thr = 0, ReLU and R-S+ keep {i : z_i > 0} (the exact skip); SiLU needs a
+ * thr > 0 to skip anything, which makes the result an approximation whose
+ * error per output is at most thr * sum_i |W2[m, i]| |(W3 x)_i| ("Model
+ * casting: compute the gate, then skip most of the FFN": thresholding the
+ * small values of a smooth gate).  thr must be finite and >= 0 (SFFN_ERR_ARG);
+ * it applies to the forwards issued after the call.
+ */
+int sffn_set_live_threshold(sffn_t h, float thr);
 
 /*
  * Copy the layer's weights into the handle (host or device pointers, any

@@ -42,7 +42,7 @@ def test_constants_match_header():
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
                  "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
-                 "SFFN_DOUBLE_ACT"):
+                 "SFFN_DOUBLE_ACT", "SFFN_ACT_SILU"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
     assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
@@ -94,3 +94,8 @@ def test_create_ex_rejects_bad_options_before_touching_the_device(lib, r, flags)
     h = lib.sffn_create_ex(512, 1024, r, sffn.SFFN_ACT_RELU, sffn.SFFN_BF16, flags)
     assert not h
     assert "flags" in sffn.sffn_last_error() or "low-rank" in sffn.sffn_last_error()
+
+
+def test_live_threshold_rejects_bad_values_on_host(lib):
+    import ctypes
+    assert lib.sffn_set_live_threshold(None, ctypes.c_float(0.1)) == sffn.SFFN_ERR_ARG

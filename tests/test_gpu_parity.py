@@ -439,3 +439,92 @@ def test_double_activation_standard_gate(B):
         ffn = make_ffn_ex(lw, DA, act=act)
         y, c, m = run_tokens(ffn, x, B=B)
         check(lw, x, y, c, m, act=act, ref=reference_ex(lw, x, DA, act=act))
+
+
+# --------------------------------------------------------------------------- smooth gate + live threshold
+# SiLU never returns an exact zero; a unit is skipped when |A(z)| <= thr
+# (sffn_set_live_threshold).  Live sets are compared outside a 1e-3 band
+# around the threshold (the GPU's z differs from the oracle's by fp32 rounding).
+def silu_np(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def act_np(act, z):
+    if act == "silu":
+        return silu_np(z)
+    zp = np.maximum(z, 0.0)
+    return zp if act == "relu" else np.where(z > 0, silu_np(z), 0.0)
+
+
+def check_thr(lw, x, y, counts, masks, act, thr, flags=0):
+    a = {"relu": oracle.RELU, "rsp": oracle.RSP, "silu": oracle.SILU}[act]
+    v = {k: syn.oracle_view(t) for k, t in lw.tensors().items()}
+    dt = oracle.F32 if lw.dtype == "f32" else oracle.BF16
+    yref, z, n = oracle.ffn_dense_ex(lw.D, lw.H, lw.r, a, dt, flags, v["W1"], v["U"], v["V"], v["W3"], v["W2"],
+                                     syn.oracle_view(x), thr=thr)
+    tol = TOL[lw.dtype]
+    A = np.abs(act_np(act, z))
+    for b in range(x.shape[0]):
+        den = np.linalg.norm(yref[b])
+        err = np.linalg.norm(y[b] - yref[b]) / den if den > 0 else np.abs(y[b]).max()
+        assert err <= tol, f"token {b}: relative L2 {err:.3e} > {tol}"
+        sure = np.abs(A[b] - thr) > 1e-3
+        bad = np.nonzero(sure & (masks[b].astype(bool) != (A[b] > thr)))[0]
+        assert bad.size == 0, f"token {b}: live set differs at units {bad[:10]}"
+        assert counts[b] == masks[b].sum()
+    return A
+
+
+def thr_for_live_fraction(lw, x, act, frac, flags=0):
+    a = {"relu": oracle.RELU, "rsp": oracle.RSP, "silu": oracle.SILU}[act]
+    v = {k: syn.oracle_view(t) for k, t in lw.tensors().items()}
+    dt = oracle.F32 if lw.dtype == "f32" else oracle.BF16
+    _, z, _ = oracle.ffn_dense_ex(lw.D, lw.H, lw.r, a, dt, flags, v["W1"], v["U"], v["V"], v["W3"], v["W2"],
+                                  syn.oracle_view(x))
+    return float(np.quantile(np.abs(act_np(act, z)), 1.0 - frac))
+
+
+@pytest.mark.parametrize("B", [1, 2, 16])
+def test_silu_zero_threshold_is_dense_swiglu(B):
+    """SiLU with thr = 0 keeps every unit: the dense SwiGLU FFN (streaming and tensor-core paths)."""
+    lw = syn.standard_layer(512, 1536, dtype="bf16", seed=71)
+    x = syn.tokens(B, 512, dtype="bf16", seed=72)
+    ffn = make_ffn_ex(lw, 0, act="silu")
+    y, c, m = run_tokens(ffn, x, B=B)
+    check_thr(lw, x, y, c, m, "silu", 0.0)
+    assert (c == lw.H).all()
+
+
+@pytest.mark.parametrize("B", [1, 3, 16])
+@pytest.mark.parametrize("gate", ["standard", "lopa"])
+def test_silu_threshold_ten_percent_live(B, gate):
+    lw = (syn.standard_layer(768, 2400, dtype="bf16", seed=73) if gate == "standard" else
+          syn.lopa_layer(768, 2600, 96, dtype="bf16", seed=73))
+    x = syn.tokens(B, 768, dtype="bf16", seed=74)
+    thr = thr_for_live_fraction(lw, x, "silu", 0.10)
+    ffn = make_ffn_ex(lw, 0, act="silu")
+    ffn.set_live_threshold(thr)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check_thr(lw, x, y, c, m, "silu", thr)
+    assert 0.05 < c.mean() / lw.H < 0.15
+
+
+def test_threshold_with_relu_fp32_and_full_lowrank_form():
+    """A positive threshold on ReLU (fp32, streaming + CUDA-core batches), and on
+    SiLU with the complete low-rank form."""
+    lw = syn.standard_layer(384, 1024, dtype="f32", seed=75)
+    x = syn.tokens(6, 384, dtype="f32", seed=76)
+    ffn = make_ffn_ex(lw, 0, act="relu")
+    ffn.set_live_threshold(0.3)
+    for B in (1, 6):
+        y, c, m = run_tokens(ffn, x, B=B)
+        check_thr(lw, x, y, c, m, "relu", 0.3)
+    full = TG | RN | DA
+    lw2 = syn.lopa_layer(512, 2100, 64, dtype="bf16", seed=77)
+    x2 = syn.tokens(4, 512, dtype="bf16", seed=78)
+    thr = thr_for_live_fraction(lw2, x2, "silu", 0.2, flags=full)
+    f2 = make_ffn_ex(lw2, full, act="silu")
+    f2.set_live_threshold(thr)
+    for B in (1, 4):
+        y, c, m = run_tokens(f2, x2, B=B)
+        check_thr(lw2, x2, y, c, m, "silu", thr, flags=full)
