@@ -187,11 +187,13 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def build_ffns(layers, dev, flags=0):
+def build_ffns(layers, dev, flags=0, act="relu", thr=0.0):
     import activation_sparse_gated_gb300 as sffn
     ffns = []
     for lw in layers:
-        f = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", lw.dtype, flags=flags)
+        f = sffn.SparseFFN(lw.D, lw.H, lw.r, act, lw.dtype, flags=flags)
+        if thr:
+            f.set_live_threshold(thr)
         w = {k: (None if t is None else t.to(dev)) for k, t in lw.tensors().items()}
         f.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
         del w
@@ -470,6 +472,22 @@ def run_gpu(args):
                                     "frac_of_measured": fbytes * args.steps / (ft * 1e9) / peak,
                                     "speedup_vs_dense_bf16": us_dense / fus, "gpu_launches_per_call": 3}
         del fffns, fg, flayers
+        # the smooth SiLU gate with a live threshold: an unshifted gate (z ~ N(0, 1)),
+        # |SiLU(z)| > 1.0 keeps ~10 % of the units; the skip is then an approximation
+        slayers = syn.workload_layers(WORKLOAD, sets=n_sets, s=0.5)
+        sffns = build_ffns(slayers, dev, act="silu", thr=1.0)
+        scounts = live_counts(sffns, x, stream)
+        sbytes = sum(elt * H * D + 2 * elt * k * D + 2 * elt * D for k in scounts)
+        sg = capture_step(sffns, x, y, stream)
+        st = time_graph(sg, stream, args.steps, args.warmup)
+        sus = 1e6 * st / (args.steps * n_tok)
+        extras["silu_threshold"] = {"workload": WORKLOAD + " with an unshifted gate, SiLU, live iff |A(z)| > 1.0",
+                                    "weight_sets": n_sets, "us_per_call": sus, "tokens_per_s": 1e6 / sus,
+                                    "mean_live": sum(scounts) / len(scounts),
+                                    "gbs": sbytes * args.steps / (st * 1e9),
+                                    "frac_of_measured": sbytes * args.steps / (st * 1e9) / peak,
+                                    "speedup_vs_dense_bf16": us_dense / sus, "gpu_launches_per_call": 2}
+        del sffns, sg, slayers
         extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
 
     cpu = None
