@@ -64,11 +64,11 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// L2 prefetch of a row by a whole warp, one 128-byte line per lane per step
-// (plain prefetch instructions, no copy-engine operation per row).
-__device__ __forceinline__ void prefetch_row_l2(const void* row, uint32_t bytes, int lane) {
+// L2 prefetch of a row by nl lanes (lane j of them), one 128-byte line per
+// lane per step (plain prefetch instructions, no copy-engine operation per row).
+__device__ __forceinline__ void prefetch_row_l2(const void* row, uint32_t bytes, int j, int nl) {
   const char* b = static_cast<const char*>(row);
-  for (uint32_t off = (uint32_t)lane * 128u; off < bytes; off += 32u * 128u)
+  for (uint32_t off = (uint32_t)j * 128u; off < bytes; off += (uint32_t)nl * 128u)
     asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(b + off));
 }
 
@@ -172,8 +172,9 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   int* l_unit = reinterpret_cast<int*>(sp);
   float* l_a = reinterpret_cast<float*>(l_unit + cap);
   float* l_h = l_a + cap;
-  int* misc = reinterpret_cast<int*>(l_h + cap);  // 0: live count
-  sp += align16((size_t)cap * 12 + 16);
+  int* misc = reinterpret_cast<int*>(l_h + cap);  // 0: live count, 2..3: RMSNorm scratch
+  uint8_t* l_mask = reinterpret_cast<uint8_t*>(misc + 4);  // live flag of every unit of the block
+  sp += align16((size_t)cap * 13 + 16);
   uint4* srows = reinterpret_cast<uint4*>(sp);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -223,7 +224,9 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     if (p.flags & FLAG_RMSNORM) rmsnorm_shared(ts, 1, p.gate_k, reinterpret_cast<float*>(misc + 2), ST);
   }
 
-  auto decide = [&](int q, float z) {  // z identical in every lane (butterfly sum)
+  // z of unit q is known to lanes [j0, j0 + nl) of the warp (identical in each);
+  // this lane is lane j of them
+  auto decide = [&](int q, float z, int j, int nl) {
     if constexpr (LOPA && EXT) {
       if (p.flags & FLAG_TILED_G) z += staged_elem<T>(xs, q % D);  // (G x)_q = x_{q mod D}
     }
@@ -236,8 +239,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       live = z > 0.f;
       a = live ? activation(p.act, z) : 0.f;
     }
-    if (lane == 0) {
-      if (p.mask) p.mask[q] = live ? 1 : 0;
+    if (j == 0) {
+      l_mask[q - row0] = live ? 1 : 0;  // written out once at the end
       if (live) {  // compaction: append to the block's live list
         const int j = atomicAdd(misc, 1);
         l_unit[j] = q;
@@ -245,19 +248,37 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       }
     }
     if (live) {  // both gathered rows of the unit start moving into L2 now
-      prefetch_row_l2(W3 + (size_t)q * nch, (uint32_t)nch * 16u, lane);
-      prefetch_row_l2(W2t + (size_t)q * nch, (uint32_t)nch * 16u, lane);
+      prefetch_row_l2(W3 + (size_t)q * nch, (uint32_t)nch * 16u, j, nl);
+      prefetch_row_l2(W2t + (size_t)q * nch, (uint32_t)nch * 16u, j, nl);
     }
   };
   // z for n rows of the shared area, the first being slice row `first`
   auto shared_rows = [&](int first, int n) {
-    for (int i = warp; i < n; i += SW) {
-      const uint4* r = srows + (size_t)i * nchg;
-      float a0 = 0.f, a1 = 0.f;
-      for (int c = lane; c < nchg; c += 32) {
-        if constexpr (LOPA) {
-          dot_chunk_t<E>(r[c], ts, c, a0, a1);
-        } else {
+    if constexpr (LOPA) {
+      // Low-rank gate rows are short (r values): a warp per row would spend
+      // most of its time in the five-step sum and the per-row decision.  Here
+      // 8 lanes share a row and a warp takes four rows at a time: the groups
+      // read the same chunks of t (one broadcast), the sum takes three steps
+      // and the four decisions run side by side.
+      const int g = lane >> 3, j = lane & 7;
+      for (int i0 = warp * 4; i0 < n; i0 += SW * 4) {
+        const int i = i0 + g;
+        float a0 = 0.f, a1 = 0.f;
+        if (i < n) {
+          const uint4* r = srows + (size_t)i * nchg;
+          for (int c = j; c < nchg; c += 8) dot_chunk_t<E>(r[c], ts, c, a0, a1);
+        }
+        float z = a0 + a1;
+        z += __shfl_xor_sync(0xffffffffu, z, 4);
+        z += __shfl_xor_sync(0xffffffffu, z, 2);
+        z += __shfl_xor_sync(0xffffffffu, z, 1);
+        if (i < n) decide(row0 + first + i, z, j, 8);
+      }
+    } else {
+      for (int i = warp; i < n; i += SW) {
+        const uint4* r = srows + (size_t)i * nchg;
+        float a0 = 0.f, a1 = 0.f;
+        for (int c = lane; c < nchg; c += 32) {
           float wf[VPC], xf[VPC];
           E::unpack(r[c], wf);
           E::unpack(xs[c], xf);
@@ -267,8 +288,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
             a1 = fmaf(wf[v + 1], xf[v + 1], a1);
           }
         }
+        decide(row0 + first + i, warp_sum(a0 + a1), lane, 32);
       }
-      decide(row0 + first + i, warp_sum(a0 + a1));
     }
   };
   shared_rows(0, R);
@@ -287,7 +308,7 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     if (pc == npg - 1) {
       const float z = warp_sum(acc);
       acc = 0.f;
-      decide(row0 + R + warp, z);
+      decide(row0 + R + warp, z, lane, 32);
     }
   };
   for (int pc = 0; pc < n_seq; pc += 2) {
@@ -412,6 +433,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
   // sums the accumulator copies once every block has finished (kernel
   // completion orders all of these atomics before it)
   if (tid == 0 && n_live > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot, n_live);
+  if (p.mask)  // the block's live flags, one coalesced store (a byte store per gate row stalls the gate)
+    for (int i = tid; i < nrows; i += ST) p.mask[row0 + i] = l_mask[i];
 }
 
 }  // namespace
@@ -421,10 +444,12 @@ StreamPlan plan_ffn_b1_stream(int D, int gate_k, int elt_bytes, bool lopa, int r
   const size_t grow = (size_t)gate_k * elt_bytes, row = (size_t)D * elt_bytes;
   // ~96 KB of gate rows per block keeps two blocks resident on an SM
   pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, (96u * 1024u) / grow);
-  const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 8) * row);
+  // the gather batch holds up to 16 W3 rows: a block with more live units than
+  // fit pays another round trip for each further batch
+  const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 16) * row);
   pl.gather_rows = (int)std::max<size_t>(1, area / row);
   pl.smem = align16((size_t)D * elt_bytes) + (lopa ? align16((size_t)gate_k * 4) : 0) +
-            align16((size_t)rows_cap * 12 + 16) + area;
+            align16((size_t)rows_cap * 13 + 16) + area;
   return pl;
 }
 

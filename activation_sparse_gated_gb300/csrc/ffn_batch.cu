@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   float* l_h = l_a + (size_t)cap * NB;                  // [cap][NB]
   int* misc = reinterpret_cast<int*>(l_h + (size_t)cap * NB);  // 0: list, 1: last, 2..: per-token counts
   float* rms_scale = reinterpret_cast<float*>(misc + 2 + NB);  // [NB] RMSNorm scratch
-  sp += al16((size_t)cap * (4 + 8 * NB) + 4 * (2 + 2 * NB));
+  uint8_t* l_mask = reinterpret_cast<uint8_t*>(rms_scale + NB);  // [rows][NB] live flags
+  sp += al16((size_t)cap * (4 + 8 * NB) + 4 * (2 + 2 * NB) + (size_t)cap * NB);
   uint4* srows = reinterpret_cast<uint4*>(sp);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -175,11 +176,8 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
       any |= lv[b];
     }
     if (lane == 0) {
-      if (p.mask) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b)
-          if (b < nb) p.mask[(size_t)b * p.H + q] = lv[b] ? 1 : 0;
-      }
+      for (int b = 0; b < NB; ++b) l_mask[(size_t)(q - row0) * NB + b] = lv[b] ? 1 : 0;  // written out at the end
       if (any) {
         const int j = atomicAdd(misc, 1);
         l_unit[j] = q;
@@ -320,6 +318,11 @@ __global__ void __launch_bounds__(BT, 1) ffn_batch_kernel(const B1Params p, int 
   }
   // per-token live counts; the finalize kernel chained behind sums the copies
   if (tid < nb && misc[2 + tid] > 0) atomicAdd(p.ctrl + CTRL_COUNT + p.count_slot + tid, misc[2 + tid]);
+  if (p.mask)  // the block's live flags, coalesced per token
+    for (int i = tid; i < nb * (row1 - row0); i += BT) {
+      const int b = i / (row1 - row0), u = i - b * (row1 - row0);
+      p.mask[(size_t)b * p.H + row0 + u] = l_mask[(size_t)u * NB + b];
+    }
 }
 
 template <typename T, bool LOPA, int NB>
@@ -348,7 +351,7 @@ BatchPlan plan_ffn_batch(int D, int gate_k, int elt_bytes, bool lopa, int rows_c
   const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 8) * row);
   pl.gather_rows = (int)std::max<size_t>(1, area / row);
   pl.smem = al16((size_t)nb_max * D * elt_bytes) + (lopa ? al16((size_t)nb_max * gate_k * 4) : 0) +
-            al16((size_t)rows_cap * (4 + 8 * nb_max) + 4 * (2 + 2 * nb_max)) + area;
+            al16((size_t)rows_cap * (4 + 8 * nb_max) + 4 * (2 + 2 * nb_max) + (size_t)rows_cap * nb_max) + area;
   return pl;
 }
 
