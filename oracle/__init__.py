@@ -55,6 +55,10 @@ def _bind(path):
         f.argtypes = [ip] * 7 + [ctypes.c_double] * 2 + [vp] * 9
     lib.oracle_num_threads.restype = ip
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_quantize_rows.restype = ip
+    lib.oracle_quantize_rows.argtypes = [ip, ip, vp, vp, vp]
+    lib.oracle_ffn_dense_q8.restype = ip
+    lib.oracle_ffn_dense_q8.argtypes = [ip] * 5 + [ctypes.c_double] + [vp] * 10
     return lib
 
 
@@ -88,6 +92,12 @@ class Variant:
         return _call("oracle_ffn_dense_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
                      lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps,
                      thr=thr)
+
+    def quantize_rows(self, W):
+        return _quantize_rows(W, self._lib)
+
+    def ffn_dense_q8(self, D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0):
+        return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, self._lib)
 
 
 def num_threads() -> int:
@@ -164,3 +174,45 @@ def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNO
     return _call("oracle_ffn_gate_first_ex", D, H, r, act, dtype, W1, U, V, W3, W2, x,
                  lambda B: np.full((B, H), -1, dtype=np.int32), flags=flags, eps=eps, thr=thr)
 
+
+
+# Weight-only int8 ("Model Casting and Low-Parameter Gating", appendix Table 17):
+# symmetric per-output-channel scales, codes decided in binary32 (see the C file).
+def _quantize_rows(W, lib=None):
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    rows, cols = W.shape
+    q = np.zeros((rows, cols), dtype=np.int8)
+    s = np.zeros(rows, dtype=np.float32)
+    rc = (lib or _load()).oracle_quantize_rows(rows, cols, _ptr(W), _ptr(q), _ptr(s))
+    if rc != 0:
+        raise RuntimeError(f"oracle_quantize_rows failed with code {rc}")
+    return q, s
+
+
+def quantize_rows(W):
+    """Per-row int8 codes and fp32 scales of a float32 matrix: (q[rows, cols] int8, s[rows] f32)."""
+    return _quantize_rows(W)
+
+
+def _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, lib=None):
+    i8 = lambda a, n: np.ascontiguousarray(a, dtype=np.int8).reshape(n)  # noqa: E731
+    f32 = lambda a, n: np.ascontiguousarray(a, dtype=np.float32).reshape(n)  # noqa: E731
+    q1, q3, q2 = i8(q1, H * D), i8(q3, H * D), i8(q2, D * H)
+    s1, s3, s2 = f32(s1, H), f32(s3, H), f32(s2, D)
+    x = _as_input(x, BF16)
+    B = x.size // D
+    y = np.zeros((B, D), dtype=np.float64)
+    z = np.zeros((B, H), dtype=np.float64)
+    n_live = np.zeros(B, dtype=np.int32)
+    rc = (lib or _load()).oracle_ffn_dense_q8(D, H, act, B, flags, float(thr), _ptr(q1), _ptr(s1), _ptr(q3),
+                                              _ptr(s3), _ptr(q2), _ptr(s2), _ptr(x), _ptr(y), _ptr(z),
+                                              _ptr(n_live))
+    if rc != 0:
+        raise RuntimeError(f"oracle_ffn_dense_q8 failed with code {rc}")
+    return y, z, n_live
+
+
+def ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0):
+    """Dense definition with int8 weights (q1, q3 [H, D], scales [H]; q2 [D, H], scales [D]) and
+    bf16 x (uint16 bits).  flags: 0 or FLAG_DOUBLE_ACT.  Returns (y, z, n_live)."""
+    return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr)

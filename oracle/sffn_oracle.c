@@ -48,6 +48,16 @@
  * The pages' claim (skipping dead units leaves y unchanged) says the two agree
  * exactly; the tests check that.
  *
+ * Weight-only int8 (the "_q8" entry points): "Model Casting and Low-Parameter
+ * Gating", appendix Table 17, quantises the cast models weight-only to int8 and
+ * int4 and gives no scale convention.  Reading taken: symmetric, one fp32
+ * scale per output channel -- per row of W1 and of W3 (per unit i), per row of
+ * W2 (per output element y_m) -- s = max_j |w_j| / 127, code =
+ * round-half-to-even(w / s) clamped to [-127, 127], both decided in binary32
+ * (the precision of the weights being quantised); an all-zero row has s = 0
+ * and codes 0.  The forward is the definition above with every weight replaced
+ * by its dequantised value q * s (exact in double); x is bf16.
+ *
  * Portable C99 + OpenMP; no SIMD intrinsics, no -ffast-math.
  */
 #include <math.h>
@@ -322,4 +332,94 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
                           const void* W3, const void* W2, const void* x,
                           double* y, int* idx, int* n_live) {
   return oracle_ffn_gate_first_ex(D, H, r, act, dtype, B, 0, 0.0, 0.0, W1, U, V, W3, W2, x, y, idx, n_live);
+}
+
+/* ------------------------------------------------------------------------ int8 */
+
+/* Per-row symmetric int8 quantisation of W[rows, cols] (binary32 decisions). */
+int oracle_quantize_rows(int rows, int cols, const float* W, int8_t* q, float* s) {
+  if (rows < 0 || cols <= 0) return -1;
+  for (int i = 0; i < rows; ++i) {
+    const float* w = W + (size_t)i * cols;
+    float amax = 0.0f;
+    for (int j = 0; j < cols; ++j) {
+      const float a = fabsf(w[j]);
+      if (a > amax) amax = a;
+    }
+    const float sc = amax / 127.0f;
+    s[i] = sc;
+    for (int j = 0; j < cols; ++j) {
+      float v = 0.0f;
+      if (sc > 0.0f) {
+        v = rintf(w[j] / sc); /* default rounding mode: to nearest, ties to even */
+        if (v > 127.0f) v = 127.0f;
+        if (v < -127.0f) v = -127.0f;
+      }
+      q[(size_t)i * cols + j] = (int8_t)v;
+    }
+  }
+  return 0;
+}
+
+/* row i of a quantised matrix, dequantised: q[i, j] * s[i] (exact in double) */
+static void dequant_row(const int8_t* q, const float* s, size_t i, int n, double* out) {
+  for (int j = 0; j < n; ++j) out[j] = (double)q[i * (size_t)n + j] * (double)s[i];
+}
+
+/*
+ * Dense definition with weight-only int8 weights: q1, q3 [H, D] with scales
+ * s1, s3 [H]; q2 [D, H] with scales s2 [D]; x [B, D] bf16 bits.  flags may only
+ * hold OR_FLAG_DOUBLE_ACT (the standard gate).  Outputs as oracle_ffn_dense_ex.
+ */
+int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
+                        const int8_t* q1, const float* s1, const int8_t* q3, const float* s3,
+                        const int8_t* q2, const float* s2, const void* x,
+                        double* y, double* z, int* n_live) {
+  if (check_args(D, H, 0, act, OR_BF16, B, flags, 0.0, thr)) return -1;
+  if (flags & ~OR_FLAG_DOUBLE_ACT) return -1;
+  double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* zb = (double*)malloc(sizeof(double) * (size_t)H);
+  double* g = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!xd || !zb || !g) {
+    free(xd); free(zb); free(g);
+    return -2;
+  }
+  int rc = 0;
+  for (int b = 0; b < B && rc == 0; ++b) {
+    widen_row(x, OR_BF16, (size_t)b * D, D, xd);
+    int bad = 0;
+#pragma omp parallel
+    {
+      double* row = (double*)malloc(sizeof(double) * (size_t)(D > H ? D : H));
+      if (!row) {
+#pragma omp atomic write
+        bad = 1;
+      }
+      /* gate and up projection of every unit */
+#pragma omp for schedule(static)
+      for (int i = 0; i < H; ++i) {
+        if (!row) continue;
+        dequant_row(q1, s1, (size_t)i, D, row);
+        zb[i] = dot(row, xd, D);
+        dequant_row(q3, s3, (size_t)i, D, row);
+        const double u = dot(row, xd, D);
+        g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);
+      }
+      /* down projection: y_m = sum_i (q2[m, i] s2[m]) g_i, i ascending */
+#pragma omp for schedule(static)
+      for (int m = 0; m < D; ++m) {
+        if (!row) continue;
+        dequant_row(q2, s2, (size_t)m, H, row);
+        y[(size_t)b * D + m] = dot(row, g, H);
+      }
+      free(row);
+    }
+    if (bad) { rc = -2; break; }
+    int cnt = 0;
+    for (int i = 0; i < H; ++i) cnt += (fabs(activation(act, zb[i])) > thr);
+    if (n_live) n_live[b] = cnt;
+    if (z) memcpy(z + (size_t)b * H, zb, sizeof(double) * (size_t)H);
+  }
+  free(xd); free(zb); free(g);
+  return rc;
 }

@@ -1,0 +1,101 @@
+"""Pins of the oracle's weight-only int8 path.
+
+"Model Casting and Low-Parameter Gating", appendix Table 17: the cast models
+are quantised weight-only to int8.  The oracle reads this as symmetric
+per-output-channel quantisation (s = max|w| / 127, codes rounded half to even
+in binary32, clamped to [-127, 127]) and evaluates the FFN definition on the
+dequantised weights q * s.  Pins: hand-worked codes (the rounding rule and the
+scale), invariants that hold for any matrix, weights whose dequantised value
+is exactly representable (then the int8 oracle must equal the already-pinned
+float32 oracle), and a hand-worked forward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+F32, RELU, RSP, SILU = oracle.F32, oracle.RELU, oracle.RSP, oracle.SILU
+
+
+def bf16_bits(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).bfloat16().view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def test_quantize_hand_worked():
+    W = np.array([[127.0, -63.5, 2.5, -3.5, 0.4, 0.0],      # s = 1: ties go to the even code
+                  [0.0, 0.0, 0.0, 0.0, 0.0, 0.0],            # an all-zero row: s = 0, codes 0
+                  [254.0, 1.0, 3.0, -5.0, 127.0, -128.0]],   # s = 2: 0.5 -> 0, 1.5 -> 2, -2.5 -> -2
+                 dtype=np.float32)
+    q, s = oracle.quantize_rows(W)
+    assert s.tolist() == [1.0, 0.0, 2.0]
+    assert q.tolist() == [[127, -64, 2, -4, 0, 0], [0] * 6, [127, 0, 2, -2, 64, -64]]
+
+
+def test_quantize_invariants():
+    rng = np.random.default_rng(1)
+    W = (rng.standard_normal((64, 300)) * rng.uniform(0.01, 10.0, size=(64, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows(W)
+    assert q.dtype == np.int8 and (np.abs(q.astype(np.int32)) <= 127).all()
+    # the largest magnitude of every row maps to +-127 and keeps its sign
+    j = np.abs(W).argmax(axis=1)
+    assert (np.abs(q[np.arange(64), j].astype(np.int32)) == 127).all()
+    assert (np.sign(q[np.arange(64), j]) == np.sign(W[np.arange(64), j])).all()
+    # round to nearest: at most half a step away (plus binary32 rounding of w / s)
+    err = np.abs(W.astype(np.float64) - q.astype(np.float64) * s[:, None].astype(np.float64))
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-5)).all()
+    # no sign flips
+    assert (q.astype(np.int32) * np.sign(W) >= 0).all()
+
+
+def exact_layer(D, H, seed):
+    """Codes with a +-127 in every row and power-of-two scales: q * s is exact in binary32."""
+    rng = np.random.default_rng(seed)
+
+    def mat(rows, cols):
+        q = rng.integers(-127, 128, size=(rows, cols)).astype(np.int8)
+        q[np.arange(rows), rng.integers(0, cols, size=rows)] = rng.choice([-127, 127], size=rows)
+        s = np.ldexp(1.0, -rng.integers(3, 9, size=rows)).astype(np.float32)
+        return q, s, (q.astype(np.float32) * s[:, None]).astype(np.float32)
+
+    return mat(H, D), mat(H, D), mat(D, H)
+
+
+@pytest.mark.parametrize("act", [RELU, RSP, SILU])
+@pytest.mark.parametrize("flags", [0, oracle.FLAG_DOUBLE_ACT])
+def test_q8_equals_float_oracle_on_exact_weights(act, flags):
+    D, H, B = 48, 130, 4
+    (q1, s1, W1), (q3, s3, W3), (q2, s2, W2) = exact_layer(D, H, 2)
+    # quantising the exact weights gives back the same codes and scales
+    for q, s, W in ((q1, s1, W1), (q3, s3, W3), (q2, s2, W2)):
+        qq, ss = oracle.quantize_rows(W)
+        assert np.array_equal(qq, q) and np.array_equal(ss, s)
+    x = torch.from_numpy(np.random.default_rng(3).standard_normal((B, D)).astype(np.float32)).bfloat16()
+    xf = x.float().numpy()
+    thr = 0.05 if act == SILU else 0.0
+    y8, z8, n8 = oracle.ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, bf16_bits(xf), thr=thr)
+    yf, zf, nf = oracle.ffn_dense_ex(D, H, 0, act, F32, flags, W1, None, None, W3, W2, xf, thr=thr)
+    np.testing.assert_allclose(z8, zf, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(y8, yf, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(n8, nf)
+
+
+def test_q8_hand_worked():
+    """D = 2, H = 2: z = (s1 q1) x, u = (s3 q3) x, y = (s2 q2) (relu(z) u) by hand."""
+    q1 = np.array([[2, -1], [-3, 1]], dtype=np.int8); s1 = np.array([0.5, 0.25], dtype=np.float32)
+    q3 = np.array([[1, 1], [4, 0]], dtype=np.int8); s3 = np.array([2.0, 1.0], dtype=np.float32)
+    q2 = np.array([[1, 5], [-2, 7]], dtype=np.int8); s2 = np.array([0.125, 4.0], dtype=np.float32)
+    x = np.array([[3.0, 1.0]], dtype=np.float32)
+    # z = (0.5 * (6 - 1), 0.25 * (-9 + 1)) = (2.5, -2); u = (2 * 4, 12); h = (20, 0)
+    y, z, n = oracle.ffn_dense_q8(2, 2, RELU, 0, q1, s1, q3, s3, q2, s2, bf16_bits(x))
+    assert z.tolist() == [[2.5, -2.0]] and n.tolist() == [1]
+    assert y.tolist() == [[0.125 * 20.0, 4.0 * -2.0 * 20.0]]
+
+
+def test_q8_rejects_low_rank_flags():
+    q = np.zeros((4, 8), dtype=np.int8)
+    s = np.ones(4, dtype=np.float32)
+    x = bf16_bits(np.ones((1, 8), dtype=np.float32))
+    with pytest.raises(RuntimeError):
+        oracle.ffn_dense_q8(8, 4, RELU, oracle.FLAG_TILED_G, q, s, q, s, q.T.copy(), np.ones(8, np.float32), x)

@@ -43,6 +43,14 @@ MUTANTS = {
     "threshold_not_absolute": ("return fabs(a) > thr ? a : 0.0;", "return a > thr ? a : 0.0;"),
     "threshold_ignored_in_dense": ("g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);",
                                    "g[i] = activation(act, zb[i]) * up_value(act, flags, u);"),
+    # weight-only int8
+    "q8_truncate": ("v = rintf(w[j] / sc);", "v = truncf(w[j] / sc);"),
+    "q8_round_half_away": ("v = rintf(w[j] / sc);", "v = roundf(w[j] / sc);"),
+    "q8_amax_signed": ("const float a = fabsf(w[j]);", "const float a = w[j];"),
+    "q8_one_scale": ("out[j] = (double)q[i * (size_t)n + j] * (double)s[i];",
+                     "out[j] = (double)q[i * (size_t)n + j] * (double)s[0];"),
+    "q8_down_uses_gate_scales": ("dequant_row(q2, s2, (size_t)m, H, row);", "dequant_row(q2, s1, (size_t)m, H, row);"),
+    "q8_up_uses_gate_codes": ("dequant_row(q3, s3, (size_t)i, D, row);", "dequant_row(q1, s3, (size_t)i, D, row);"),
 }
 
 
@@ -154,6 +162,26 @@ def _pins(mod):
     a = torch.nn.functional.silu(torch.from_numpy(zt)).numpy()
     check("threshold_error_bound", (np.abs(yt - y0) <= bound + 1e-12).all() and
           (nt == (np.abs(a) > thr).sum(axis=1)).all() and (nt < H).all() and not np.allclose(yt, y0))
+    # weight-only int8 (values derived in test_oracle_int8)
+    q, sc = mod.quantize_rows(f([[127.0, -63.5, 2.5, -3.5, 0.4, 0.0], [254.0, 1.0, 3.0, -5.0, 127.0, -128.0]]))
+    check("q8_hand_codes", q.tolist() == [[127, -64, 2, -4, 0, 0], [127, 0, 2, -2, 64, -64]] and
+          sc.tolist() == [1.0, 2.0])
+    Wr = f(rng.standard_normal((16, 40)) * 3)
+    q, sc = mod.quantize_rows(Wr)
+    err = np.abs(Wr.astype(np.float64) - q.astype(np.float64) * sc[:, None])
+    check("q8_round_trip", (err <= sc[:, None].astype(np.float64) * (0.5 + 1e-5)).all())
+    D, H, B = 12, 30, 3
+    mats = []
+    for rows, cols in ((H, D), (H, D), (D, H)):
+        qq = rng.integers(-127, 128, size=(rows, cols)).astype(np.int8)
+        qq[:, 0] = 127
+        ss = np.ldexp(1.0, -rng.integers(3, 9, size=rows)).astype(np.float32)
+        mats.append((qq, ss, f(qq.astype(np.float32) * ss[:, None])))
+    (q1, s1, E1), (q3, s3, E3), (q2, s2, E2) = mats
+    xq = f(torch.from_numpy(f(rng.standard_normal((B, D)))).bfloat16().float().numpy())
+    y8, _, n8 = mod.ffn_dense_q8(D, H, oracle.RELU, 0, q1, s1, q3, s3, q2, s2, _bf16_bits(xq))
+    yf, _, nf = mod.ffn_dense(D, H, 0, oracle.RELU, oracle.F32, E1, None, None, E3, E2, xq)
+    check("q8_exact_weights", np.allclose(y8, yf, rtol=1e-12, atol=1e-12) and np.array_equal(n8, nf))
     return failed
 
 
