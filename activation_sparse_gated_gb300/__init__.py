@@ -8,7 +8,8 @@ or fails to load, every entry point raises.
 The functions mirror the C ABI one to one (``sffn_create``, ``sffn_set_weights``,
 ``sffn_forward``, ``sffn_active_counts``, ``sffn_active_mask``,
 ``sffn_synchronize``, ``sffn_destroy``, ``sffn_strerror``, ``sffn_last_error``,
-``sffn_version``, ``sffn_debug_timeout_probe``, ``sffn_forward_noalloc``).  Tensor arguments are passed by
+``sffn_version``, ``sffn_debug_timeout_probe``, ``sffn_forward_noalloc``,
+``sffn_set_weights_int8``, ``sffn_get_weights_int8``).  Tensor arguments are passed by
 their data pointer; ``stream`` defaults to the current torch stream.
 ``SparseFFN`` wraps one handle.
 """
@@ -19,7 +20,7 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsffn.so")
 
-SFFN_F32, SFFN_BF16 = 0, 1
+SFFN_F32, SFFN_BF16, SFFN_I8W = 0, 1, 2
 SFFN_ACT_RELU, SFFN_ACT_RSP, SFFN_ACT_SILU = 0, 1, 2
 SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
@@ -30,7 +31,8 @@ SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT = 1, 2, 4
 #: every symbol include/sffn.h declares
 EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_live_threshold", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
            "sffn_active_mask", "sffn_synchronize", "sffn_destroy", "sffn_strerror",
-           "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc")
+           "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc",
+           "sffn_set_weights_int8", "sffn_get_weights_int8")
 
 _lib = None
 
@@ -66,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sffn_version": (ip, []),
         "sffn_debug_timeout_probe": (ip, [vp, ip, vp]),
         "sffn_forward_noalloc": (ip, [vp, vp, vp, vp, vp, vp, ip, ip, ip, ip, ip, vp]),
+        "sffn_set_weights_int8": (ip, [vp] * 8),
+        "sffn_get_weights_int8": (ip, [vp] * 8),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -174,13 +178,26 @@ def sffn_forward_noalloc(W1, W3, W2t, x, y, counts, D: int, H: int, B: int, act:
                                                _ptr(counts), D, H, B, act, dtype, _stream(stream)))
 
 
+def sffn_set_weights_int8(h, W1q, s1, W3q, s3, W2q, s2, stream=None):
+    """Load int8 codes and fp32 scales (W1q, W3q [H, D] with s1, s3 [H]; W2q [D, H] with s2 [D])."""
+    return _check(load().sffn_set_weights_int8(h, _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3), _ptr(W2q),
+                                                _ptr(s2), _stream(stream)))
+
+
+def sffn_get_weights_int8(h, W1q, s1, W3q, s3, W2q, s2, stream=None):
+    """Copy the handle's int8 codes and scales out (same layout as sffn_set_weights_int8; None skips)."""
+    return _check(load().sffn_get_weights_int8(h, _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3), _ptr(W2q),
+                                                _ptr(s2), _stream(stream)))
+
+
 class SparseFFN:
     """One FFN layer held by the library (a wrapper around one handle).
 
     ``SparseFFN(D, H, r=0, act="relu", dtype="bf16", flags=0)`` (flags: the
     SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT options); ``set_weights(W1_or_U, V,
     W3, W2)`` with torch tensors in the layer's dtype (W2 as [D, H]);
-    ``forward(x, y=None)`` with x [B, D] on the handle's device.
+    ``forward(x, y=None)`` with x [B, D] on the handle's device.  dtype "int8": weight-only
+    int8 (bf16 weights given to ``set_weights`` are quantised on the device; x and y bf16).
     """
 
     def __init__(self, D: int, H: int, r: int = 0, act: str = "relu", dtype: str = "bf16", flags: int = 0):
@@ -188,7 +205,7 @@ class SparseFFN:
         self.dtype = dtype
         self.flags = flags
         self._act = {"relu": SFFN_ACT_RELU, "rsp": SFFN_ACT_RSP, "silu": SFFN_ACT_SILU}[act]
-        self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16}[dtype]
+        self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16, "int8": SFFN_I8W}[dtype]
         self.h = sffn_create_ex(D, H, r, self._act, self._dt, flags)
 
     def set_weights(self, W1_or_U, V, W3, W2, stream=None):
@@ -218,6 +235,20 @@ class SparseFFN:
 
     def synchronize(self):
         sffn_synchronize(self.h)
+
+    def set_weights_int8(self, W1q, s1, W3q, s3, W2q, s2, stream=None):
+        """Codes and scales quantised elsewhere (int8 [H, D], [H, D], [D, H]; fp32 [H], [H], [D])."""
+        sffn_set_weights_int8(self.h, W1q, s1, W3q, s3, W2q, s2, stream)
+
+    def int8_weights(self, device="cuda"):
+        """The handle's codes and scales as tensors: (W1q, s1, W3q, s3, W2q, s2), W2q as [D, H]."""
+        import torch
+        D, H = self.D, self.H
+        out = (torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(H, device=device),
+               torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(H, device=device),
+               torch.empty(D, H, dtype=torch.int8, device=device), torch.empty(D, device=device))
+        sffn_get_weights_int8(self.h, *out)
+        return out
 
     def set_live_threshold(self, thr: float):
         """Units with |A(z)| <= thr are skipped (0: the exact skip of ReLU / R-S+)."""

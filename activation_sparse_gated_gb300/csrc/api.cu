@@ -41,6 +41,7 @@ void sffn::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s",
 
 struct sffn_s {
   int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
+  int welt = 0;  // bytes of a stored weight element (1: int8 codes of SFFN_I8W)
   int flags = 0;  // SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT
   float thr = 0.f;  // live iff |A(z)| > thr (sffn_set_live_threshold)
   int device = 0, num_sms = 0;
@@ -71,6 +72,11 @@ struct sffn_s {
   int tc_min_batch = 2;    // batches of at least this many tokens take the tensor-core path
   uint16_t* hbuf = nullptr;
   int* tickets = nullptr;
+  // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
+  float* qs1 = nullptr;
+  float* qs3 = nullptr;
+  float* qs2 = nullptr;
+  StreamPlan i8_plan;
 };
 
 namespace {
@@ -89,6 +95,9 @@ void release(sffn_s* h) {
   cudaFree(h->mask);
   cudaFree(h->hbuf);
   cudaFree(h->tickets);
+  cudaFree(h->qs1);
+  cudaFree(h->qs3);
+  cudaFree(h->qs2);
   if (h->ev) cudaEventDestroy(h->ev);
 }
 
@@ -185,12 +194,19 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     fail(SFFN_ERR_ARG, "the tiled identity and RMSNorm options belong to the low-rank gate (r > 0)");
     return nullptr;
   }
-  if (dtype != SFFN_F32 && dtype != SFFN_BF16) { fail(SFFN_ERR_ARG, "dtype %d unknown", dtype); return nullptr; }
+  if (dtype != SFFN_F32 && dtype != SFFN_BF16 && dtype != SFFN_I8W) {
+    fail(SFFN_ERR_ARG, "dtype %d unknown", dtype);
+    return nullptr;
+  }
+  if (dtype == SFFN_I8W && (r != 0 || D % 16 != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
+    fail(SFFN_ERR_DTYPE, "int8 weights need the standard gate (r = 0), D %% 16 == 0 and no low-rank option");
+    return nullptr;
+  }
   if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP && act != SFFN_ACT_SILU) {
     fail(SFFN_ERR_ARG, "act %d unknown", act);
     return nullptr;
   }
-  const int dmax = dtype == SFFN_BF16 ? SFFN_MAX_D_BF16 : SFFN_MAX_D_F32;
+  const int dmax = dtype == SFFN_F32 ? SFFN_MAX_D_F32 : SFFN_MAX_D_BF16;
   if (D < 8 || D % 8 != 0 || D > dmax) { fail(SFFN_ERR_ARG, "D=%d must be a multiple of 8 in [8, %d]", D, dmax); return nullptr; }
   if (H < 1) { fail(SFFN_ERR_ARG, "H=%d must be >= 1", H); return nullptr; }
   if (r < 0 || r % 8 != 0 || r > D) { fail(SFFN_ERR_ARG, "r=%d must be 0 or a multiple of 8 <= D", r); return nullptr; }
@@ -198,7 +214,8 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
   sffn_s* h = new (std::nothrow) sffn_s;
   if (!h) { fail(SFFN_ERR_NOMEM, "host allocation failed"); return nullptr; }
   h->D = D; h->H = H; h->r = r; h->act = act; h->dtype = dtype; h->flags = flags;
-  h->elt = dtype == SFFN_BF16 ? 2 : 4;
+  h->elt = dtype == SFFN_F32 ? 4 : 2;
+  h->welt = dtype == SFFN_I8W ? 1 : h->elt;
 
   auto bail = [&](int code, const char* what, cudaError_t e) -> sffn_t {
     fail(code, "%s: %s", what, cudaGetErrorString(e));
@@ -215,13 +232,17 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     return bail(SFFN_ERR_CUDA, "cudaDeviceGetAttribute", e);
   h->max_smem = (size_t)optin;
 
-  const size_t elt = h->elt;
+  const size_t welt = h->welt;
   const size_t gk = (size_t)gate_k(h);
+  const bool i8 = dtype == SFFN_I8W;
   struct { void** p; size_t bytes; } allocs[] = {
-      {&h->gate_w, (size_t)H * gk * elt},
-      {&h->V, (size_t)std::max(r, 1) * D * elt},
-      {&h->W3, (size_t)H * D * elt},
-      {&h->W2t, (size_t)H * D * elt},
+      {&h->gate_w, (size_t)H * gk * welt},
+      {&h->V, (size_t)std::max(r, 1) * D * welt},
+      {&h->W3, (size_t)H * D * welt},
+      {&h->W2t, (size_t)H * D * welt},
+      {(void**)&h->qs1, i8 ? sizeof(float) * H : 16},
+      {(void**)&h->qs3, i8 ? sizeof(float) * H : 16},
+      {(void**)&h->qs2, i8 ? sizeof(float) * D : 16},
       {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * D},
       {(void**)&h->tbuf, sizeof(float) * SFFN_MAX_BATCH * std::max(r, 8)},
       {(void**)&h->ctrl, sizeof(int) * CTRL_INTS},
@@ -274,6 +295,19 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
       return nullptr;
     }
     if ((e = ffn_batch_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+    if (i8) {
+      h->i8_plan = plan_ffn_b1_i8(D, h->stream_rows_cap);
+      if (h->i8_plan.smem > h->max_smem) {
+        fail(SFFN_ERR_DTYPE, "shared-memory plan of the int8 kernel exceeds the device limit");
+        char keep[sizeof g_msg];
+        std::memcpy(keep, g_msg, sizeof keep);
+        release(h);
+        delete h;
+        std::memcpy(g_msg, keep, sizeof keep);
+        return nullptr;
+      }
+      if ((e = ffn_b1_i8_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+    }
     if ((e = ffn_b1_stream_prepare(h->max_smem)))
       return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   }
@@ -303,6 +337,27 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
   if (!W1_or_U || !W3 || !W2 || (h->r > 0 && !V)) return fail(SFFN_ERR_ARG, "null weight pointer");
   if (int rc = check_device(h)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->dtype == SFFN_I8W) {
+    // bf16 weights in, per-output-channel int8 codes and scales out (W2's codes transposed)
+    const size_t D = h->D, H = h->H;
+    void* stage = nullptr;
+    int8_t* q2 = nullptr;
+    SFFN_CUDA(cudaMalloc(&stage, D * H * 2));
+    cudaError_t e = cudaMalloc(&q2, D * H);
+    if (!e) e = cudaMemcpyAsync(stage, W1_or_U, H * D * 2, cudaMemcpyDefault, s);
+    if (!e) e = launch_quantize_rows(stage, static_cast<int8_t*>(h->gate_w), h->qs1, (int)H, (int)D, s);
+    if (!e) e = cudaMemcpyAsync(stage, W3, H * D * 2, cudaMemcpyDefault, s);
+    if (!e) e = launch_quantize_rows(stage, static_cast<int8_t*>(h->W3), h->qs3, (int)H, (int)D, s);
+    if (!e) e = cudaMemcpyAsync(stage, W2, D * H * 2, cudaMemcpyDefault, s);
+    if (!e) e = launch_quantize_rows(stage, q2, h->qs2, (int)D, (int)H, s);
+    if (!e) e = launch_transpose(q2, h->W2t, (int)D, (int)H, 1, s);
+    if (!e) e = cudaStreamSynchronize(s);
+    cudaFree(stage);
+    cudaFree(q2);
+    if (e) return fail(SFFN_ERR_CUDA, "weight quantisation failed: %s", cudaGetErrorString(e));
+    h->weights_set = true;
+    return SFFN_OK;
+  }
   const size_t elt = h->elt, D = h->D, H = h->H, gk = gate_k(h);
   SFFN_CUDA(cudaMemcpyAsync(h->gate_w, W1_or_U, H * gk * elt, cudaMemcpyDefault, s));
   if (h->r > 0) SFFN_CUDA(cudaMemcpyAsync(h->V, V, (size_t)h->r * D * elt, cudaMemcpyDefault, s));
@@ -320,6 +375,56 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
     h->tc_ready = true;
   }
   h->weights_set = true;
+  return SFFN_OK;
+}
+
+int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const int8_t* W3q, const float* s3,
+                          const int8_t* W2q, const float* s2, void* stream) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (h->dtype != SFFN_I8W) return fail(SFFN_ERR_STATE, "the handle does not hold int8 weights");
+  if (!W1q || !s1 || !W3q || !s3 || !W2q || !s2) return fail(SFFN_ERR_ARG, "null weight pointer");
+  if (int rc = check_device(h)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t D = h->D, H = h->H;
+  int8_t* q2 = nullptr;
+  SFFN_CUDA(cudaMalloc(&q2, D * H));
+  cudaError_t e = cudaMemcpyAsync(h->gate_w, W1q, H * D, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(h->W3, W3q, H * D, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(h->qs1, s1, sizeof(float) * H, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(h->qs3, s3, sizeof(float) * H, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(h->qs2, s2, sizeof(float) * D, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(q2, W2q, D * H, cudaMemcpyDefault, s);
+  if (!e) e = launch_transpose(q2, h->W2t, (int)D, (int)H, 1, s);
+  if (!e) e = cudaStreamSynchronize(s);
+  cudaFree(q2);
+  if (e) return fail(SFFN_ERR_CUDA, "int8 weight upload failed: %s", cudaGetErrorString(e));
+  h->weights_set = true;
+  return SFFN_OK;
+}
+
+int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* s3, int8_t* W2q, float* s2,
+                          void* stream) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (h->dtype != SFFN_I8W) return fail(SFFN_ERR_STATE, "the handle does not hold int8 weights");
+  if (!h->weights_set) return fail(SFFN_ERR_STATE, "no weights have been set");
+  if (int rc = check_device(h)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t D = h->D, H = h->H;
+  cudaError_t e = cudaSuccess;
+  if (W1q) e = cudaMemcpyAsync(W1q, h->gate_w, H * D, cudaMemcpyDefault, s);
+  if (!e && W3q) e = cudaMemcpyAsync(W3q, h->W3, H * D, cudaMemcpyDefault, s);
+  if (!e && s1) e = cudaMemcpyAsync(s1, h->qs1, sizeof(float) * H, cudaMemcpyDefault, s);
+  if (!e && s3) e = cudaMemcpyAsync(s3, h->qs3, sizeof(float) * H, cudaMemcpyDefault, s);
+  if (!e && s2) e = cudaMemcpyAsync(s2, h->qs2, sizeof(float) * D, cudaMemcpyDefault, s);
+  int8_t* q2 = nullptr;
+  if (!e && W2q) {
+    e = cudaMalloc(&q2, D * H);
+    if (!e) e = launch_transpose(h->W2t, q2, (int)H, (int)D, 1, s);
+    if (!e) e = cudaMemcpyAsync(W2q, q2, D * H, cudaMemcpyDefault, s);
+  }
+  if (!e) e = cudaStreamSynchronize(s);
+  cudaFree(q2);
+  if (e) return fail(SFFN_ERR_CUDA, "int8 weight download failed: %s", cudaGetErrorString(e));
   return SFFN_OK;
 }
 
@@ -345,9 +450,40 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
   }
+  if (h->dtype == SFFN_I8W) {
+    // weight-only int8: one streaming pass per token
+    for (int b = 0; b < B; ++b) {
+      B1Params p;
+      p.gate_w = h->gate_w;
+      p.W3 = h->W3;
+      p.W2t = h->W2t;
+      p.x = static_cast<const uint8_t*>(x) + b * row;
+      p.y = static_cast<uint8_t*>(y) + b * row;
+      p.yacc = h->yacc;
+      p.ctrl = h->ctrl;
+      p.counts = h->counts + b;
+      p.mask = h->mask + (size_t)b * h->H;
+      p.D = h->D;
+      p.H = h->H;
+      p.gate_k = h->D;
+      p.act = h->act;
+      p.count_slot = b;
+      p.rows_cap = h->stream_rows_cap;
+      p.pref_rows = h->i8_plan.pref_rows;
+      p.gather_rows = h->i8_plan.gather_rows;
+      p.timeout_ns = kTimeoutNs;
+      p.flags = h->flags;
+      p.thr = h->thr;
+      p.s1 = h->qs1;
+      p.s3 = h->qs3;
+      p.s2 = h->qs2;
+      SFFN_CUDA(launch_ffn_b1_i8(p, h->stream_grid, h->i8_plan.smem, s));
+      SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, 1, SFFN_BF16, s));
+    }
+  }
   if (lopa) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
-  for (int b = 0; b < B && !(h->tc_ready && B >= h->tc_min_batch);) {
+  for (int b = 0; b < B && h->dtype != SFFN_I8W && !(h->tc_ready && B >= h->tc_min_batch);) {
     const int nb = std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;

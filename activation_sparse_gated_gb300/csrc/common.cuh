@@ -162,6 +162,25 @@ struct Elt<bf16_tag> {
   }
 };
 
+// Packed fp32x2 arithmetic (sm_100 and later): two lanes of fp32 per
+// instruction, each lane rounded exactly as the scalar operation.
+__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
+  asm("{\n\t.reg .b64 A, B, C;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%0, %1};\n\t"
+      "fma.rn.f32x2 C, A, B, C;\n\tmov.b64 {%0, %1}, C;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 A, B, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t"
+      "add.rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // fp32 -> storage type, round to nearest even (bf16 via the CUDA intrinsic)
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -31,6 +31,9 @@ struct B1Params {
   unsigned long long timeout_ns;
   int flags = 0;          // FLAG_TILED_G | FLAG_RMSNORM (low-rank gate) | FLAG_DOUBLE_ACT
   float thr = 0.f;        // live iff |A(z)| > thr
+  const float* s1 = nullptr;  // int8 weights: per-unit scales of the W1 and W3 codes,
+  const float* s3 = nullptr;  // per-output scales of the W2 codes
+  const float* s2 = nullptr;
 };
 
 constexpr int B1_NWG = 8;                               // gate warps
@@ -116,11 +119,21 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
 cudaError_t launch_finalize(float* yacc, void* y, int* ctrl, int* counts, int count_slot, int D, int nb,
                             int dtype, cudaStream_t s);
 
+// Weight-only int8, standard gate, one token per launch (ffn_b1_i8.cu): codes
+// W1q, W3q, W2tq [H, D] in gate_w, W3, W2t; scales s1, s3 [H], s2 [D] in the
+// params (each block scales its partial y by s2 before adding it up).
+StreamPlan plan_ffn_b1_i8(int D, int rows_cap);
+cudaError_t ffn_b1_i8_prepare(size_t max_smem);
+cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s);
+// Per-row symmetric int8 quantisation of a bf16 matrix [rows, cols].
+cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols,
+                                 cudaStream_t s);
+
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,
                           cudaStream_t s);
 
-// W2[D, H] -> W2t[H, D] (element size 2 or 4 bytes).
+// W2[D, H] -> W2t[H, D] (element size 1, 2 or 4 bytes).
 cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int elt_bytes,
                              cudaStream_t s);
 

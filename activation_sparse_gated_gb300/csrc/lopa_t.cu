@@ -116,6 +116,9 @@ cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int
   if (elt_bytes == 4)
     transpose_kernel<uint32_t><<<g, b, 0, s>>>(static_cast<const uint32_t*>(src),
                                                static_cast<uint32_t*>(dst), rows, cols);
+  else if (elt_bytes == 1)
+    transpose_kernel<uint8_t><<<g, b, 0, s>>>(static_cast<const uint8_t*>(src),
+                                              static_cast<uint8_t*>(dst), rows, cols);
   else
     transpose_kernel<uint16_t><<<g, b, 0, s>>>(static_cast<const uint16_t*>(src),
                                                static_cast<uint16_t*>(dst), rows, cols);

@@ -187,11 +187,11 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def build_ffns(layers, dev, flags=0, act="relu", thr=0.0):
+def build_ffns(layers, dev, flags=0, act="relu", thr=0.0, dtype=None):
     import activation_sparse_gated_gb300 as sffn
     ffns = []
     for lw in layers:
-        f = sffn.SparseFFN(lw.D, lw.H, lw.r, act, lw.dtype, flags=flags)
+        f = sffn.SparseFFN(lw.D, lw.H, lw.r, act, dtype or lw.dtype, flags=flags)
         if thr:
             f.set_live_threshold(thr)
         w = {k: (None if t is None else t.to(dev)) for k, t in lw.tensors().items()}
@@ -488,6 +488,20 @@ def run_gpu(args):
                                     "frac_of_measured": sbytes * args.steps / (st * 1e9) / peak,
                                     "speedup_vs_dense_bf16": us_dense / sus, "gpu_launches_per_call": 2}
         del sffns, sg, slayers
+        # weight-only int8 (per-output-channel scales, quantised on the device), same layers
+        qffns = build_ffns(layers, dev, dtype="int8")
+        qcounts = live_counts(qffns, x, stream)
+        qbytes = sum(H * D + 4 * H + 2 * k * D + 4 * k + 2 * elt * D + 4 * D for k in qcounts)
+        qg = capture_step(qffns, x, y, stream)
+        qt = time_graph(qg, stream, args.steps, args.warmup)
+        qus = 1e6 * qt / (args.steps * n_tok)
+        extras["int8_weights"] = {"workload": WORKLOAD + ", weight-only int8 (per-output-channel fp32 scales), "
+                                  "bf16 x and y", "weight_sets": n_sets, "us_per_call": qus,
+                                  "tokens_per_s": 1e6 / qus, "mean_live": sum(qcounts) / len(qcounts),
+                                  "gbs": qbytes * args.steps / (qt * 1e9),
+                                  "frac_of_measured": qbytes * args.steps / (qt * 1e9) / peak,
+                                  "speedup_vs_dense_bf16": us_dense / qus, "gpu_launches_per_call": 2}
+        del qffns, qg
         extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
 
     cpu = None

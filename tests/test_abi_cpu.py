@@ -15,7 +15,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(sffn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(sffn_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -42,7 +42,7 @@ def test_constants_match_header():
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
                  "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
-                 "SFFN_DOUBLE_ACT", "SFFN_ACT_SILU"):
+                 "SFFN_DOUBLE_ACT", "SFFN_ACT_SILU", "SFFN_I8W"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
     assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
@@ -61,12 +61,15 @@ def test_null_handle_is_rejected_on_host(lib):
     assert lib.sffn_set_weights(None, None, None, None, None, None) == sffn.SFFN_ERR_ARG
     assert lib.sffn_active_counts(None, None, 1) == sffn.SFFN_ERR_ARG
     assert lib.sffn_synchronize(None) == sffn.SFFN_ERR_ARG
+    assert lib.sffn_set_weights_int8(None, None, None, None, None, None, None, None) == sffn.SFFN_ERR_ARG
+    assert lib.sffn_get_weights_int8(None, None, None, None, None, None, None, None) == sffn.SFFN_ERR_ARG
     lib.sffn_destroy(None)
 
 
 @pytest.mark.parametrize("args", [(0, 64, 0, 0, 1), (12, 64, 0, 0, 1), (8192, 64, 0, 0, 1),
                                   (4096, 64, 0, 0, 0), (64, 0, 0, 0, 1), (64, 64, 12, 0, 1),
-                                  (64, 64, 128, 0, 1), (64, 64, 0, 2, 1), (64, 64, 0, 0, 7)])
+                                  (64, 64, 128, 0, 1), (64, 64, 0, 3, 1), (64, 64, 0, 0, 7),
+                                  (64, 64, 8, 0, 2), (24, 64, 0, 0, 2), (8192, 64, 0, 0, 2)])
 def test_create_rejects_bad_shapes_before_touching_the_device(lib, args):
     h = lib.sffn_create(*args)
     assert not h

@@ -1,0 +1,206 @@
+"""GPU parity of the weight-only int8 path (dtype SFFN_I8W) against the oracle.
+
+* The device quantiser must give the oracle's codes and scales bit for bit
+  (an integer result decided in binary32 on both sides).
+* The forward must match the oracle's int8 definition (dequantised weights
+  q * s, fp64) within the bf16 output bar, with the live set identical outside
+  the 1e-2 band, for every activation, the live threshold, the double
+  activation and batches (one streaming pass per token).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import activation_sparse_gated_gb300 as sffn
+from activation_sparse_gated_gb300 import synthetic as syn
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+BAND = 1e-2
+ACTS = {"relu": oracle.RELU, "rsp": oracle.RSP, "silu": oracle.SILU}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from activation_sparse_gated_gb300 import build
+    build.build()
+    sffn.load()
+    torch.cuda.set_device(0)
+
+
+def floats(lw):
+    t = lw.tensors()
+    return [t[k].float().numpy() for k in ("W1", "W3", "W2")]
+
+
+def oracle_codes(lw):
+    W1, W3, W2 = floats(lw)
+    return oracle.quantize_rows(W1) + oracle.quantize_rows(W3) + oracle.quantize_rows(W2)
+
+
+def make_int8(lw, act="relu", flags=0, thr=0.0):
+    ffn = sffn.SparseFFN(lw.D, lw.H, 0, act, "int8", flags=flags)
+    t = lw.tensors()
+    ffn.set_weights(t["W1"].cuda(), None, t["W3"].cuda(), t["W2"].cuda())
+    if thr:
+        ffn.set_live_threshold(thr)
+    return ffn
+
+
+def run(ffn, x, B=1):
+    xd = x.cuda()
+    ys, counts, masks = [], [], []
+    for s in range(0, x.shape[0], B):
+        xb = xd[s:s + B].contiguous()
+        y = ffn(xb)
+        counts += ffn.active_counts(xb.shape[0])
+        masks.append(ffn.active_mask(xb.shape[0]))
+        ys.append(y.float().cpu().numpy().astype(np.float64))
+    return np.concatenate(ys), np.array(counts), np.concatenate(masks)
+
+
+def act_abs(act, z):
+    if act == "silu":
+        return np.abs(z / (1.0 + np.exp(-z)))
+    zp = np.maximum(z, 0.0)
+    return zp if act == "relu" else np.where(z > 0, z / (1.0 + np.exp(-z)), 0.0)
+
+
+def check(lw, x, y, counts, masks, act="relu", flags=0, thr=0.0, codes=None):
+    q1, s1, q3, s3, q2, s2 = codes if codes is not None else oracle_codes(lw)
+    yref, z, n = oracle.ffn_dense_q8(lw.D, lw.H, ACTS[act], flags, q1, s1, q3, s3, q2, s2,
+                                     syn.oracle_view(x), thr=thr)
+    A = act_abs(act, z)
+    for b in range(x.shape[0]):
+        den = np.linalg.norm(yref[b])
+        if den == 0:
+            assert (y[b] == 0).all(), f"token {b}: no live unit but y != 0"
+        else:
+            err = np.linalg.norm(y[b] - yref[b]) / den
+            assert err <= TOL, f"token {b}: relative L2 {err:.3e} > {TOL}"
+        live = A[b] > thr
+        sure = (np.abs(z[b]) > BAND) if thr == 0 else (np.abs(A[b] - thr) > 1e-3)
+        bad = np.nonzero(sure & (masks[b].astype(bool) != live))[0]
+        assert bad.size == 0, f"token {b}: live set differs at units {bad[:10]}"
+        assert counts[b] == masks[b].sum()
+    return yref, z, n
+
+
+def crafted_rows(W):
+    """Put the hand-worked quantisation rows (ties, an all-zero row) into W."""
+    W = W.copy()
+    W[0, :6] = [127.0, -63.5, 2.5, -3.5, 0.5, 0.0]
+    W[0, 6:] = 0.0
+    W[1, :] = 0.0
+    W[2, :6] = [254.0, 1.0, 3.0, -5.0, 127.0, -128.0]
+    W[2, 6:] = 0.0
+    return W
+
+
+@pytest.mark.parametrize("D,H", [(512, 1500), (2560, 7168)])
+def test_device_quantiser_is_bitexact(D, H):
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=81)
+    t = lw.tensors()
+    W1 = crafted_rows(t["W1"].float().numpy())
+    W1b = torch.from_numpy(W1).bfloat16()
+    assert np.array_equal(W1b.float().numpy(), W1)  # the crafted values are bf16 numbers
+    ffn = sffn.SparseFFN(D, H, 0, "relu", "int8")
+    ffn.set_weights(W1b.cuda(), None, t["W3"].cuda(), t["W2"].cuda())
+    got = [a.cpu().numpy() for a in ffn.int8_weights()]
+    want = oracle.quantize_rows(W1) + oracle.quantize_rows(t["W3"].float().numpy()) + \
+        oracle.quantize_rows(t["W2"].float().numpy())
+    for g, w, name in zip(got, want, ("W1q", "s1", "W3q", "s3", "W2q", "s2")):
+        assert g.shape == w.shape, name
+        assert np.array_equal(g.view(np.uint8) if g.dtype == np.int8 else g.view(np.uint32),
+                              w.view(np.uint8) if w.dtype == np.int8 else w.view(np.uint32)), name
+    assert got[0][0, :6].tolist() == [127, -64, 2, -4, 0, 0] and got[1][0] == 1.0
+    assert (got[0][1] == 0).all() and got[1][1] == 0.0
+    assert got[0][2, :6].tolist() == [127, 0, 2, -2, 64, -64] and got[1][2] == 2.0
+
+
+@pytest.mark.parametrize("act,flags,thr", [("relu", 0, 0.0), ("rsp", 0, 0.0), ("relu", sffn.SFFN_DOUBLE_ACT, 0.0),
+                                           ("silu", 0, 0.3), ("relu", 0, 0.05)])
+@pytest.mark.parametrize("B", [1, 3])
+def test_forward_matches_oracle(act, flags, thr, B):
+    kw = {"shift": 0.0} if act == "silu" else {}
+    lw = syn.standard_layer(512, 1500, dtype="bf16", seed=82, **kw)
+    x = syn.tokens(2 * B, 512, dtype="bf16", seed=83)
+    ffn = make_int8(lw, act, flags, thr)
+    y, c, m = run(ffn, x, B=B)
+    check(lw, x, y, c, m, act, flags, thr)
+
+
+def test_full_size_workload():
+    name = "std-bf16-D2560-H7168-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, 6)
+    ffn = make_int8(lw)
+    y, c, m = run(ffn, x)
+    _, _, n = check(lw, x, y, c, m)
+    assert 0.02 < n.mean() / lw.H < 0.3
+
+
+def test_d4096_shape():
+    lw = syn.workload_layers("sweep-bf16-D4096-H14336", sets=1, s=0.75)[0]
+    x = syn.workload_tokens("sweep-bf16-D4096-H14336", 2)
+    ffn = make_int8(lw)
+    y, c, m = run(ffn, x)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("D,H", [(16, 1), (16, 37), (64, 151), (64, 153), (48, 300)])
+def test_ragged_shapes(D, H):
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=84)
+    x = syn.tokens(3, D, dtype="bf16", seed=85)
+    ffn = make_int8(lw)
+    y, c, m = run(ffn, x)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("shift", [+20.0, -20.0])
+def test_all_live_and_none_live(shift):
+    lw = syn.standard_layer(256, 700, dtype="bf16", seed=86, shift=shift)
+    x = syn.tokens(2, 256, dtype="bf16", seed=87)
+    ffn = make_int8(lw)
+    y, c, m = run(ffn, x)
+    check(lw, x, y, c, m)
+    if shift < 0:
+        assert (c == 0).all() and (y == 0).all()
+    else:
+        assert (c == lw.H).all()
+
+
+def test_external_codes_and_round_trip():
+    """Codes and scales quantised by the oracle, loaded with sffn_set_weights_int8, give the
+    same layer as the device quantiser, and read back unchanged."""
+    lw = syn.standard_layer(384, 1200, dtype="bf16", seed=88)
+    x = syn.tokens(4, 384, dtype="bf16", seed=89)
+    codes = oracle_codes(lw)
+    ext = sffn.SparseFFN(384, 1200, 0, "relu", "int8")
+    ext.set_weights_int8(*[torch.from_numpy(a).cuda() for a in codes])
+    back = [a.cpu().numpy() for a in ext.int8_weights()]
+    for g, w in zip(back, codes):
+        assert np.array_equal(g, w)
+    y1, c1, m1 = run(ext, x)
+    y2, c2, m2 = run(make_int8(lw), x)
+    check(lw, x, y1, c1, m1, codes=codes)
+    assert np.array_equal(m1, m2) and np.array_equal(c1, c2)
+    np.testing.assert_allclose(y1, y2, rtol=1e-2, atol=1e-6)
+
+
+def test_int8_argument_errors():
+    with pytest.raises(sffn.SffnError):
+        sffn.SparseFFN(256, 512, 32, "relu", "int8")          # low-rank gate
+    with pytest.raises(sffn.SffnError):
+        sffn.SparseFFN(40, 512, 0, "relu", "int8")            # D % 16 != 0
+    bf = sffn.SparseFFN(256, 512, 0, "relu", "bf16")
+    q = torch.zeros(512, 256, dtype=torch.int8, device="cuda")
+    s = torch.ones(512, device="cuda")
+    with pytest.raises(sffn.SffnError) as e:
+        bf.set_weights_int8(q, s, q, s, torch.zeros(256, 512, dtype=torch.int8, device="cuda"),
+                            torch.ones(256, device="cuda"))
+    assert e.value.code == sffn.SFFN_ERR_STATE
