@@ -442,14 +442,20 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
 StreamPlan plan_ffn_b1_stream(int D, int gate_k, int elt_bytes, bool lopa, int rows_cap) {
   StreamPlan pl;
   const size_t grow = (size_t)gate_k * elt_bytes, row = (size_t)D * elt_bytes;
-  // ~96 KB of gate rows per block keeps two blocks resident on an SM
-  pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, (96u * 1024u) / grow);
-  // the gather batch holds up to 16 W3 rows: a block with more live units than
-  // fit pays another round trip for each further batch
-  const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 16) * row);
+  // Two blocks per SM (the next call's blocks prefetch while this call runs):
+  // at most 110 KB per block.  The shared area holds up to 96 KB of gate rows
+  // before the wait and then a gather batch of up to 16 W3 rows (a block with
+  // more live units than fit pays another round trip per further batch).
+  const size_t fixed = align16((size_t)D * elt_bytes) + (lopa ? align16((size_t)gate_k * 4) : 0) +
+                       align16((size_t)rows_cap * 13 + 16);
+  const size_t budget = 110u * 1024u;
+  const size_t free_area = budget > fixed ? budget - fixed : 0;
+  pl.pref_rows = (int)std::max<size_t>(1, std::min<size_t>((size_t)rows_cap,
+                                                           std::min<size_t>(96u * 1024u, free_area) / grow));
+  const size_t g = std::max<size_t>(1, std::min<size_t>(std::min(rows_cap, 16), free_area / row));
+  const size_t area = std::max((size_t)pl.pref_rows * grow, g * row);
   pl.gather_rows = (int)std::max<size_t>(1, area / row);
-  pl.smem = align16((size_t)D * elt_bytes) + (lopa ? align16((size_t)gate_k * 4) : 0) +
-            align16((size_t)rows_cap * 13 + 16) + area;
+  pl.smem = fixed + area;
   return pl;
 }
 
