@@ -1,6 +1,6 @@
 """A small, self-contained forward loop for profiler captures.
 
-    python -m activation_sparse_gated_gb300.profile_case --workload std --calls 8
+    python -m activation_sparse_gated_gb300.profile_case --workload std --calls 8 [--dtype int8]
 
 builds ONE full-size layer of the named workload, runs `--calls` forwards of
 `--batch` tokens through the C ABI with a synchronisation after each, and exits
@@ -32,6 +32,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(CASES), default="std")
     ap.add_argument("--calls", type=int, default=8)
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--dtype", choices=["bf16", "f32", "int8"], default=None,
+                    help="handle dtype (default: the workload's); int8 quantises the layer on the device")
     args = ap.parse_args()
 
     import torch
@@ -42,7 +44,7 @@ def main():
     build.build()
     name, gate = CASES[args.workload]
     lw = syn.workload_layers(name, sets=1, gate=gate)[0]
-    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", lw.dtype)
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", args.dtype or lw.dtype)
     w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
     ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
     x = syn.workload_tokens(name, args.calls * args.batch).cuda()
