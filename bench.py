@@ -12,10 +12,13 @@ Printed (rank 0, one JSON line): tokens/s of the whole job (value), us per
 call, achieved HBM GB/s on the bytes the method touches (the gate matrix plus
 the live rows of W3 and W2^T, plus x and y) as a fraction of the measured copy
 peak and of the nominal 8 TB/s, the same figures for the dense bf16 FFN
-(cuBLAS through torch) and for the low-rank gate layer (D=2560, H'=9787,
-r=400, 16 rotated sets), an end-to-end figure with host buffers, SM clocks
-sampled during the timed region, and the fp64 CPU oracle timed on a bounded
-sample of the same workload.
+(cuBLAS through torch), and for the variants: the low-rank gate layer
+(D=2560, H'=9787, r=400, 32 rotated sets) alone and in the full form (tiled
+identity G, RMSNorm, double activation), the smooth SiLU gate with a live
+threshold, weight-only int8 weights, and batches of 4 / 16 / 64 tokens on the
+tensor cores; an end-to-end figure with host buffers, SM clocks sampled during
+the timed region, and the fp64 CPU oracle timed on a bounded sample of the
+same workload.
 
 --impl reference times the reference arm: the fp64 CPU oracle, as it stands,
 on the host cores (rank 0 only), on a bounded sample of the same workload.
@@ -433,9 +436,10 @@ def run_gpu(args):
                                 "gbs": dense_bytes / (us_dense * 1e3), "speedup_sparse": us_dense / us_call,
                                 "forms_us": {k: 1e6 * v / (args.steps * n_tok) for k, v in dense_t.items()}}
         del ld, dg
-        # low-rank gate layer, 16 rotated sets (its gate weights exceed L2 above ~13 sets)
+        # low-rank gate layer, 32 rotated sets: the gate weights (U, V) of all sets are 316 MB,
+        # 2.5x the 129 MB L2, so the gate is read from HBM as in a real model's stack of layers
         li = syn.WORKLOADS[LOPA_WORKLOAD]
-        lsets = 16
+        lsets = 32
         llayers = syn.workload_layers(LOPA_WORKLOAD, sets=lsets)
         lffns = build_ffns(llayers, dev)
         lx = syn.workload_tokens(LOPA_WORKLOAD).to(dev)
