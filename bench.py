@@ -233,6 +233,20 @@ def capture_step(ffns, x, y, stream):
     return g
 
 
+def replica_totals(t_local, units_per_rank, world, dist=None, device=None):
+    """Whole-job figures of N weakly scaled replicas (one rank per GPU, no data
+    exchange): the timed region ends when the slowest rank ends, so the job's
+    time is the maximum over ranks, and its throughput is the units all ranks
+    processed divided by that time.  Returns (seconds, units per second)."""
+    t = float(t_local)
+    if dist is not None and world > 1:
+        import torch
+        tt = torch.tensor([t], device=device, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return t, world * units_per_rank / t
+
+
 def time_graph(g, stream, steps, warmup, dist=None):
     import torch
     for _ in range(warmup):
@@ -380,11 +394,7 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         t = time_graph(g, stream, args.steps, args.warmup, dist)
     clocks = clk.summary()
-    if dist is not None:
-        tt = torch.tensor([t], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    value = world * args.steps * n_tok / t
+    t, value = replica_totals(t, args.steps * n_tok, world, dist, dev)
     us_call = 1e6 * t / (args.steps * n_tok)
     achieved = bytes_step * args.steps / (t * 1e9)   # per GPU
 
@@ -411,12 +421,8 @@ def run_gpu(args):
             yh.copy_(y, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": world * args.steps * n_tok / t_e2e, "unit": "tokens/s",
+    t_e2e, v_e2e = replica_totals(e0.elapsed_time(e1) / 1e3, args.steps * n_tok, world, dist, dev)
+    e2e = {"value": v_e2e, "unit": "tokens/s",
            "h2d_bytes_per_step": xh.numel() * xh.element_size(),
            "d2h_bytes_per_step": yh.numel() * yh.element_size()}
 
