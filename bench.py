@@ -155,6 +155,19 @@ def time_oracle(layers, x, budget_s: float, max_tokens: int):
     return n, time.perf_counter() - t0, oracle.num_threads()
 
 
+def oracle_one_thread(budget_s: float):
+    """The same oracle sample on one OpenMP thread (a child process with OMP_NUM_THREADS=1)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", RANK="0", WORLD_SIZE="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread", str(budget_s)],
+                           env=env, capture_output=True, text=True, timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
+        return None
+    return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": d["cores"],
+            "sample": f"first {d['tokens']} tokens, {d['seconds']:.1f} s"}
+
+
 def run_reference(args):
     """The reference arm: the fp64 oracle on the host cores, rank 0 only."""
     if int(os.environ.get("RANK", "0")) != 0:
@@ -520,6 +533,9 @@ def run_gpu(args):
         cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"first {n} tokens of the {WORKLOAD} decode stream (token t through weight set "
                          f"t mod 2), fp64 dense oracle, {dt:.1f} s"}
+        one = oracle_one_thread(3.0)
+        if one:
+            cpu["one_thread"] = one
 
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -562,8 +578,16 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the dense and low-rank comparisons")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
+                    help="(internal) time the oracle on this process's OpenMP threads for SECONDS, print JSON")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
+    if args.oracle_one_thread > 0:
+        from activation_sparse_gated_gb300 import synthetic as syn
+        n, dt, cores = time_oracle(syn.workload_layers(WORKLOAD, sets=2), syn.workload_tokens(WORKLOAD, 64),
+                                   args.oracle_one_thread, 64)
+        print(json.dumps({"tokens": n, "seconds": dt, "cores": cores}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
