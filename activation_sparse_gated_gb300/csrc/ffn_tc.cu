@@ -113,8 +113,11 @@ uint32_t tmem_cols_for(int n) {
   return c;
 }
 
+// Round a dynamic shared-memory pointer up to 1024 bytes by pointer arithmetic
+// (an integer round trip would hide the shared address space from the
+// compiler and turn every access through the result into a generic one).
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // --------------------------------------------------------------------------- gate-up kernel
