@@ -96,7 +96,7 @@ __device__ __forceinline__ float dot_piece(const uint4 (&w)[PIECE], const uint4*
     if (c < nch) {
       float wf[VPC], xf[VPC];
       E::unpack(w[k], wf);
-      E::unpack(xs[c], xf);
+      E::unpack(lds16(xs + c), xf);
 #pragma unroll
       for (int v = 0; v < VPC; v += 2) {
         a0 = fmaf(wf[v], xf[v], a0);
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
         float a0 = 0.f, a1 = 0.f;
         if (i < n) {
           const uint4* r = srows + (size_t)i * nchg;
-          for (int c = j; c < nchg; c += 8) dot_chunk_t<E>(r[c], ts, c, a0, a1);
+          for (int c = j; c < nchg; c += 8) dot_chunk_t<E>(lds16(r + c), ts, c, a0, a1);
         }
         float z = a0 + a1;
         z += __shfl_xor_sync(0xffffffffu, z, 4);
@@ -280,8 +280,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
         float a0 = 0.f, a1 = 0.f;
         for (int c = lane; c < nchg; c += 32) {
           float wf[VPC], xf[VPC];
-          E::unpack(r[c], wf);
-          E::unpack(xs[c], xf);
+          E::unpack(lds16(r + c), wf);
+          E::unpack(lds16(xs + c), xf);
 #pragma unroll
           for (int v = 0; v < VPC; v += 2) {
             a0 = fmaf(wf[v], xf[v], a0);
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       float a0 = 0.f, a1 = 0.f;
       for (int c = lane; c < nch; c += 32) {
         float wf[VPC], xf[VPC];
-        E::unpack(r[c], wf);
-        E::unpack(xs[c], xf);
+        E::unpack(lds16(r + c), wf);
+        E::unpack(lds16(xs + c), xf);
 #pragma unroll
         for (int v = 0; v < VPC; v += 2) {
           a0 = fmaf(wf[v], xf[v], a0);
