@@ -75,7 +75,7 @@ __device__ __forceinline__ void dot_chunk(const uint4& w, const float4* xq, int 
   for (int k = 0; k < 4; ++k) {
     float2 v01, v23;
     widen_i8x4(words[k], v01, v23);
-    const float4 xv = xq[k * ncw + c];
+    const float4 xv = lds_f4(xq + k * ncw + c);
     ffma2(acc, v01, make_float2(xv.x, xv.y));
     ffma2(acc, v23, make_float2(xv.z, xv.w));
   }
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
     for (int i = warp; i < n; i += QW) {
       const uint4* r = srows + (size_t)i * ncw;
       float2 acc = make_float2(0.f, 0.f);
-      for (int c = lane; c < ncw; c += 32) dot_chunk(r[c], xq, ncw, c, acc);
+      for (int c = lane; c < ncw; c += 32) dot_chunk(lds16(r + c), xq, ncw, c, acc);
       decide(row0 + first + i, warp_sum(acc.x + acc.y));
     }
   };
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
     for (int u = warp; u < nb; u += QW) {
       const uint4* r = srows + (size_t)u * ncw;
       float2 acc2 = make_float2(0.f, 0.f);
-      for (int c = lane; c < ncw; c += 32) dot_chunk(r[c], xq, ncw, c, acc2);
+      for (int c = lane; c < ncw; c += 32) dot_chunk(lds16(r + c), xq, ncw, c, acc2);
       const float uval = s3s[l_unit[b0 + u] - row0] * warp_sum(acc2.x + acc2.y);
       if (lane == 0) l_h[b0 + u] = l_a[b0 + u] * (dbl ? activation(p.act, uval) : uval);
     }
