@@ -70,6 +70,8 @@ struct sffn_s {
   TcMaps tcm;
   bool tc_ready = false;
   int tc_min_batch = 2;    // batches of at least this many tokens take the tensor-core path
+  int tcu_max_batch = 2;   // ... and up to this many gather the union of their live sets (ffn_tcu.cu;
+                           // from B = 3 its per-block partial sums of all B x D outputs cost more)
   uint16_t* hbuf = nullptr;
   int* tickets = nullptr;
   // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
@@ -324,6 +326,8 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
       if ((e = cudaMemset(h->hbuf, 0, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))))
         return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if ((e = ffn_tcu_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if (const char* env = std::getenv("SFFN_TCU_MAX_BATCH")) h->tcu_max_batch = std::max(0, std::min(8, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TC_MIN_BATCH")) h->tc_min_batch = std::max(1, std::atoi(env));
     }
   }
@@ -441,7 +445,16 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   const bool lopa = h->r > 0;
   const size_t row = (size_t)h->D * h->elt;
 
-  if (h->tc_ready && B >= h->tc_min_batch) {
+  const bool tcu = h->tc_ready && B >= h->tc_min_batch && B <= h->tcu_max_batch;
+  if (tcu) {
+    // small batch: the gate on the tensor cores, the union of the live sets gathered, then finalize
+    cudaError_t ce = cudaSuccess;
+    if (int rc = launch_ffn_tcu(h->tc, h->tcm, h->W3, h->W2t, h->yacc, h->ctrl, h->mask, x, h->D, h->H, B, h->act,
+                                h->flags, h->thr, kTimeoutNs, h->max_smem, s, &ce))
+      return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
+    SFFN_CUDA(ce);
+    SFFN_CUDA(launch_finalize(h->yacc, y, h->ctrl, h->counts, 0, h->D, B, h->dtype, s));
+  } else if (h->tc_ready && B >= h->tc_min_batch) {
     // whole batch on the tensor cores: gate kernel, down kernel, finalize
     TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets};
     cudaError_t ce = cudaSuccess;

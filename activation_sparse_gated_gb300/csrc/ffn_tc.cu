@@ -472,6 +472,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // --------------------------------------------------------------------------- host side
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
@@ -498,8 +500,6 @@ int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)r;
 }
-
-}  // namespace
 
 TcPlan plan_ffn_tc(int D, int H, int num_sms) {
   TcPlan p;

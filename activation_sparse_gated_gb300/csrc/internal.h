@@ -103,6 +103,11 @@ struct TcBuffers {
 };
 constexpr int TC_TICKETS = 64;  // >= slices of 128 y values (D <= 8192)
 TcPlan plan_ffn_tc(int D, int H, int num_sms);
+// Tensor map of a bf16 matrix [rows, cols] (row stride in bytes): boxes of 64
+// columns x box_rows rows, 128-byte swizzle.  0 on success, else a driver
+// status (-1: the encoder entry point is unavailable).
+int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride_bytes,
+              uint32_t box_rows);
 size_t ffn_tc_hbuf_elems(const TcPlan& p);
 // 0 on success, else a driver status (or -1: tensor-map encoder unavailable)
 int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, const void* W2t, uint16_t* hbuf,
@@ -113,6 +118,15 @@ cudaError_t ffn_tc_prepare(size_t max_smem);
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
                   cudaError_t* cuda_err);
+
+// Small batches (2..8 tokens, bf16, standard gate; ffn_tcu.cu): the gate on the
+// tensor cores, the union of the live sets gathered on the CUDA cores, fp32
+// atomics into the accumulator copies (the finalize kernel follows).  Returns 0
+// and sets *cuda_err to the launch status, or a non-zero encode status.
+cudaError_t ffn_tcu_prepare(size_t max_smem);
+int launch_ffn_tcu(const TcPlan& plan, const TcMaps& maps, const void* W3, const void* W2t, float* yacc, int* ctrl,
+                   uint8_t* mask, const void* x, int D, int H, int B, int act, int flags, float thr,
+                   unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
 
 // y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the
 // copies and publishes the nb live counts (chained behind a forward kernel).

@@ -380,6 +380,31 @@ def test_tc_matches_cuda_core_batched_kernel(monkeypatch):
         assert np.linalg.norm(y_tc[b] - y_cc[b]) <= 2 * TOL["bf16"] * max(den, 1e-30)
 
 
+@pytest.mark.parametrize("B", [2, 3, 5, 8])
+@pytest.mark.parametrize("act,thr,flags", [("relu", 0.0, 0), ("silu", 0.3, 0), ("relu", 0.0, sffn.SFFN_DOUBLE_ACT)])
+def test_union_gather_kernel(monkeypatch, B, act, thr, flags):
+    """Small batches through the union-gather kernel (gate on the tensor cores, the union of the live
+    sets gathered on the CUDA cores) for every batch size it takes, against the oracle and against the
+    streaming tensor-core path."""
+    kw = {"shift": 0.0} if act == "silu" else {}
+    lw = syn.standard_layer(640, 2300, dtype="bf16", seed=57, **kw)
+    x = syn.tokens(2 * B, 640, dtype="bf16", seed=58)
+    monkeypatch.setenv("SFFN_TCU_MAX_BATCH", "8")  # read when a handle is created
+    un = make_ffn_ex(lw, flags, act)
+    if thr:
+        un.set_live_threshold(thr)
+    y_u, c_u, m_u = run_tokens(un, x, B=B)
+    monkeypatch.setenv("SFFN_TCU_MAX_BATCH", "0")
+    st = make_ffn_ex(lw, flags, act)
+    if thr:
+        st.set_live_threshold(thr)
+    y_s, c_s, m_s = run_tokens(st, x, B=B)
+    check_thr(lw, x, y_u, c_u, m_u, act, thr, flags)
+    A = check_thr(lw, x, y_s, c_s, m_s, act, thr, flags)
+    sure = np.abs(A - thr) > 1e-3
+    assert np.array_equal(m_u[sure], m_s[sure])
+
+
 # --------------------------------------------------------------------------- the full low-rank gate
 # W1(x) = Gx + U RMSNorm(Vx) with the tiled identity G, and the double
 # activation ("LoPA Gating: moving the ceiling"): the same kernels with the
