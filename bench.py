@@ -318,7 +318,7 @@ def batched_extras(ffns, layers, x, stream, args, peak):
     n_sets = len(ffns)
     ld = [{"W1": lw.W1.to(dev), "W3": lw.W3.to(dev), "W2": lw.W2.to(dev)} for lw in layers]
     out = {}
-    for B in (4, 16, 64):
+    for B in (2, 4, 16, 64):
         calls = x.shape[0] // B
         y = torch.empty_like(x)
         # union of the tokens' live sets per call (untimed)
@@ -336,10 +336,13 @@ def batched_extras(ffns, layers, x, stream, args, peak):
                 sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
         tt = time_graph(g, stream, args.steps, args.warmup)
         us = 1e6 * tt / (args.steps * calls)
-        # The tensor-core path (bf16, standard gate, B >= 2) streams every unit slice of W1, W3
-        # and W2 (the union covers most units at these batch sizes) plus x, y and h (bf16 pair,
-        # written once, read once); union_gather_bytes is what a row-gathering design would read.
-        tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2"))
+        # B = 2 gathers the union of the live sets (gate on the tensor cores, union rows of W3 and
+        # W2^T on the CUDA cores): W1 + the union rows + x, y.  From B = 3 the tensor-core path
+        # streams every unit slice of W1, W3 and W2 (the union covers most units) plus x, y and h
+        # (bf16 pair, written once, read once); union_gather_bytes is what a row-gathering design
+        # would read.
+        union_path = 2 <= B <= int(os.environ.get("SFFN_TCU_MAX_BATCH", "2"))
+        tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2")) and not union_path
         union_bytes = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
         bytes_call = (3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H) if tc_path else union_bytes
         yd = torch.empty_like(x)
@@ -357,7 +360,10 @@ def batched_extras(ffns, layers, x, stream, args, peak):
             body()
         td = time_graph(gd, stream, args.steps, args.warmup)
         usd = 1e6 * td / (args.steps * calls)
-        out[f"B{B}"] = {"path": "tensor cores: gate-up + down kernels" if tc_path else "CUDA cores, union gathers",
+        path = ("tensor cores: gate-up + down kernels" if tc_path else
+                "union gathers: gate on the tensor cores, union rows on the CUDA cores" if union_path else
+                "CUDA cores, union gathers")
+        out[f"B{B}"] = {"path": path,
                         "us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,
                         "union_fraction": mean_union / H, "bytes_per_call": bytes_call,
                         "union_gather_bytes": union_bytes, "gbs": bytes_call / (us * 1e3),
