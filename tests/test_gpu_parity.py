@@ -349,6 +349,30 @@ def test_tc_batched_shapes(D, H, B):
     check(lw, x, y, c, m)
 
 
+@pytest.mark.parametrize("D,H", [(512, 2048), (384, 1000), (520, 1500), (256, 10000), (64, 151), (16, 40)])
+def test_union_gather_shapes(D, H):
+    """B = 2 takes the union-gather kernel: slices of 16 and 72 units, ragged H, D off a multiple of 64
+    (zero-filled K tail), and a single tiny slice."""
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=53)
+    x = syn.tokens(6, D, dtype="bf16", seed=54)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=2)
+    check(lw, x, y, c, m)
+
+
+def test_union_gather_full_size_and_d4096():
+    """B = 2 at the standard workload's size and at the D = 4096 sweep shape (75 % sparsity)."""
+    name = "std-bf16-D2560-H7168-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, 4)
+    y, c, m = run_tokens(make_ffn(lw), x, B=2)
+    check(lw, x, y, c, m)
+    lw = syn.workload_layers("sweep-bf16-D4096-H14336", sets=1, s=0.75)[0]
+    x = syn.workload_tokens("sweep-bf16-D4096-H14336", 2)
+    y, c, m = run_tokens(make_ffn(lw), x, B=2)
+    check(lw, x, y, c, m)
+
+
 def test_tc_batched_rsp_and_changing_batch():
     """R-S+ activation, and consecutive calls whose token count changes the padded width."""
     lw = syn.standard_layer(512, 3000, dtype="bf16", seed=53)
