@@ -65,15 +65,17 @@ struct sffn_s {
   int stream_rows_cap = 0;
   StreamPlan stream_plan;
   BatchPlan batch_plan;  // groups of up to 8 tokens
-  // tensor-core batched path (bf16, standard gate)
+  // tensor-core batched path (bf16; standard gate, or the low-rank gate without RMSNorm)
   TcPlan tc;
   TcMaps tcm;
   bool tc_ready = false;
   int tc_min_batch = 2;    // batches of at least this many tokens take the tensor-core path
+  int tc_t_cuda_max = TC_T_CUDA_CORE_MAX_B;  // low-rank batches up to this many tokens: t on the CUDA cores
   int tcu_max_batch = 2;   // ... and up to this many gather the union of their live sets (ffn_tcu.cu;
                            // from B = 3 its per-block partial sums of all B x D outputs cost more)
   uint16_t* hbuf = nullptr;
   int* tickets = nullptr;
+  uint16_t* tpair = nullptr;  // low-rank gate: [256, r] bf16 t pairs of a tensor-core batch
   // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
   float* qs1 = nullptr;
   float* qs3 = nullptr;
@@ -97,6 +99,7 @@ void release(sffn_s* h) {
   cudaFree(h->mask);
   cudaFree(h->hbuf);
   cudaFree(h->tickets);
+  cudaFree(h->tpair);
   cudaFree(h->qs1);
   cudaFree(h->qs3);
   cudaFree(h->qs2);
@@ -310,11 +313,17 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
       }
       if ((e = ffn_b1_i8_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     }
+    if (r > 0 && (e = lopa_t_prepare())) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     if ((e = ffn_b1_stream_prepare(h->max_smem)))
       return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   }
-  if (dtype == SFFN_BF16 && r == 0) {
-    h->tc = plan_ffn_tc(D, H, h->num_sms);
+  if (dtype == SFFN_BF16) {
+    h->tc = plan_ffn_tc(D, H, r, h->num_sms);
+    if (h->tc.ok && r > 0) {
+      h->tcu_max_batch = 0;  // the union-gather kernel computes a standard gate only
+      if ((e = cudaMalloc(&h->tpair, sizeof(uint16_t) * 256 * r))) return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
+      if ((e = cudaMemset(h->tpair, 0, sizeof(uint16_t) * 256 * r))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+    }
     if (h->tc.ok) {
       if ((e = cudaMalloc(&h->hbuf, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))) ||
           (e = cudaMalloc(&h->tickets, sizeof(int) * TC_TICKETS)))
@@ -327,8 +336,10 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
         return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
       if ((e = ffn_tcu_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
-      if (const char* env = std::getenv("SFFN_TCU_MAX_BATCH")) h->tcu_max_batch = std::max(0, std::min(8, std::atoi(env)));
+      if (const char* env = std::getenv("SFFN_TCU_MAX_BATCH"))
+        if (r == 0) h->tcu_max_batch = std::max(0, std::min(8, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TC_MIN_BATCH")) h->tc_min_batch = std::max(1, std::atoi(env));
+      if (const char* env = std::getenv("SFFN_TC_T_CUDA_MAX_B")) h->tc_t_cuda_max = std::max(0, std::atoi(env));
     }
   }
   if ((e = cudaDeviceSynchronize())) return bail(SFFN_ERR_CUDA, "cudaDeviceSynchronize", e);
@@ -374,7 +385,7 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
   cudaFree(stage);
   if (e) return fail(SFFN_ERR_CUDA, "weight upload failed: %s", cudaGetErrorString(e));
   if (h->tc.ok) {
-    if (int rc = encode_tc_maps(&h->tcm, h->tc, h->gate_w, h->W3, h->W2t, h->hbuf, h->D, h->H))
+    if (int rc = encode_tc_maps(&h->tcm, h->tc, h->gate_w, h->V, h->W3, h->W2t, h->hbuf, h->D, h->H))
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of the weights failed (status %d)", rc);
     h->tc_ready = true;
   }
@@ -445,7 +456,9 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   const bool lopa = h->r > 0;
   const size_t row = (size_t)h->D * h->elt;
 
-  const bool tcu = h->tc_ready && B >= h->tc_min_batch && B <= h->tcu_max_batch;
+  // batches on the tensor cores (the low-rank gate's RMSNorm needs all of t first: CUDA-core path)
+  const bool tc_batch = h->tc_ready && B >= h->tc_min_batch && !(lopa && (h->flags & FLAG_RMSNORM));
+  const bool tcu = tc_batch && !lopa && B <= h->tcu_max_batch;
   if (tcu) {
     // small batch: the gate on the tensor cores, the union of the live sets gathered, then finalize
     cudaError_t ce = cudaSuccess;
@@ -454,12 +467,14 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
     SFFN_CUDA(launch_finalize(h->yacc, y, h->ctrl, h->counts, 0, h->D, B, h->dtype, s));
-  } else if (h->tc_ready && B >= h->tc_min_batch) {
-    // whole batch on the tensor cores: gate kernel, down kernel, finalize
-    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets};
+  } else if (tc_batch) {
+    // whole batch on the tensor cores: (t kernel,) gate-up kernel, down kernel
+    const bool t_cuda_cores = lopa && B <= h->tc_t_cuda_max;
+    if (t_cuda_cores) SFFN_CUDA(launch_lopa_t_pair(h->V, x, h->tpair, h->r, h->D, B, (B + 15) / 16 * 16, s));
+    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, h->tpair};
     cudaError_t ce = cudaSuccess;
     if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, h->thr, kTimeoutNs,
-                               h->max_smem, s, &ce))
+                               h->max_smem, s, &ce, t_cuda_cores))
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
   }
@@ -494,9 +509,9 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, 1, SFFN_BF16, s));
     }
   }
-  if (lopa) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
+  if (lopa && !tc_batch) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
-  for (int b = 0; b < B && h->dtype != SFFN_I8W && !(h->tc_ready && B >= h->tc_min_batch);) {
+  for (int b = 0; b < B && h->dtype != SFFN_I8W && !tc_batch;) {
     const int nb = std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;

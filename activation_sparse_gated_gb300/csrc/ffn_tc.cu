@@ -1,5 +1,5 @@
 // ffn_tc.cu -- gate-first FFN for a batch of tokens on the tensor cores (bf16
-// weights and tokens, fp32 accumulation, standard gate).
+// weights and tokens, fp32 accumulation, standard or low-rank gate).
 //
 // Per token b the method is unchanged ("Model casting: compute the gate, then
 // skip most of the FFN", section "What an FFN actually computes"):
@@ -27,6 +27,17 @@
 //               fp32 atomics into an accumulator; the last block of a y slice
 //               (a ticket per slice) rounds it into y and clears it, and block
 //               0 publishes the per-token live counts.
+//
+// Low-rank gate ("LoPA Gating: moving the ceiling", W1 = UV), three kernels:
+//   t kernel: the gate-up kernel's low-rank form with no U chunks and V in
+//             place of W3, so it computes T = V X^T (one block per slice of
+//             the r rows of V); its epilogue stores t_b as a bf16 pair, t_hi
+//             in rows [0, NB) and t_lo in rows [NB, 2 NB) of one buffer;
+//   gate-up:  the first K chunk groups run over the r columns of U, two MMAs
+//             per K step into the Z accumulator (U t_hi, then U t_lo), the
+//             remaining groups over the D columns of W3 into the P accumulator;
+//             the accumulator layout is the unfused one, so the epilogue and
+//   down:     the down kernel are the standard gate's.
 //
 // All operands move by 2D TMA tiles with 128-byte swizzle, several tiles per
 // pipeline stage (one lane of a producer warp issues them, one lane of an MMA
@@ -67,6 +78,9 @@ constexpr int TC_NS_MAX = 8;
 
 struct TcGateArgs {
   int D, H, B, NB, NU, KC, C, NCG, NS, act, Hs, nacc, flags;
+  int KCZ, NCZ;          // low-rank gate: K chunks of r and the chunk groups they fill (the first NCZ)
+  const uint16_t* x;     // [B, D] bf16 bits (the tiled identity G of the low-rank gate)
+  uint16_t* tout;        // t kernel: the t pair [2 NB, H] (H = r) instead of h, masks and counts
   float thr;  // live iff |A(z)| > thr
   uint32_t tmem_cols;
   int* ctrl;
@@ -103,6 +117,20 @@ size_t gate_smem_bytes(int C, int MT, int NU, int NB, int NS) {
   return 1024 + (size_t)NS * gate_stage_bytes(C, NU, NB) + gate_slack_bytes(C, MT, NU, NB) + 8 * (2 * NS + 2) + 8 +
          4 * NB + 64;
 }
+// Low-rank stages: A regions [C][NU x 128 B] (U or W3 rows), then B regions
+// [C][2 NB x 128 B] (t_hi and t_lo, or x in the first half).  An MMA reads MT
+// rows from an A region's start; past the last one lie the B regions.
+__host__ __device__ constexpr uint32_t lopa_stage_bytes(int C, int NU, int NB) {
+  return (uint32_t)C * 128u * (uint32_t)(NU + 2 * NB);
+}
+__host__ __device__ inline uint32_t lopa_slack_bytes(int C, int MT, int NU, int NB) {
+  const int over = (MT - NU) * 128 - C * 2 * NB * 128;
+  return over > 0 ? (uint32_t)(over + 1023) / 1024 * 1024 : 0u;
+}
+size_t lopa_smem_bytes(int C, int MT, int NU, int NB, int NS) {
+  return 1024 + (size_t)NS * lopa_stage_bytes(C, NU, NB) + lopa_slack_bytes(C, MT, NU, NB) + 8 * (2 * NS + 2) + 8 +
+         4 * NB + 64;
+}
 size_t down_smem_bytes(int NB, int NS) {
   return 1024 + (size_t)NS * TC_DC * down_chunk_bytes(NB) + 8 * (2 * NS + 2) + 8 + 64;
 }
@@ -125,17 +153,21 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // [NU x 128 B]; then X regions [C][NB x 128 B].  K chunk group q covers chunks
 // q*C .. q*C+C-1.  TMEM: fused (2 NU <= 128): lanes [0, NU) = Z, [NU, 2 NU) =
 // P, NB columns; otherwise lanes [0, NU), Z in columns [0, NB), P in [NB, 2 NB).
-template <int MT>
+// LOPA: mW1 maps U [H, r] and mT the t pair [2 NB, r]; the stages hold the
+// low-rank layout (lopa_stage_bytes) and TMEM the unfused one.
+template <int MT, bool LOPA>
 __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
     ffn_tc_gateup_kernel(const __grid_constant__ CUtensorMap mW1, const __grid_constant__ CUtensorMap mW3,
-                         const __grid_constant__ CUtensorMap mX, const TcGateArgs p) {
+                         const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mT,
+                         const TcGateArgs p) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int NS = p.NS, NB = p.NB, C = p.C;
   const uint32_t wreg = (uint32_t)p.NU * 128u, xreg = (uint32_t)NB * 128u;
-  const uint32_t st_bytes = gate_stage_bytes(C, p.NU, NB);
+  const uint32_t st_bytes = LOPA ? lopa_stage_bytes(C, p.NU, NB) : gate_stage_bytes(C, p.NU, NB);
+  const uint32_t slack = LOPA ? lopa_slack_bytes(C, MT, p.NU, NB) : gate_slack_bytes(C, MT, p.NU, NB);
   // stages, then slack for the rows an MMA reads past the last A region
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes + gate_slack_bytes(C, MT, p.NU, NB));
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)NS * st_bytes + slack);
   uint64_t* empty = full + NS;
   uint64_t* done = empty + NS;  // every MMA complete (one commit per MMA warp)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 2);
@@ -163,7 +195,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // Let the next kernel launch only once this block holds its TMEM: a later
   // kernel's blocks then never take the columns an earlier one still needs.
   if (tid == 0) pdl_launch_dependents();
-  const bool fused = 2 * p.NU <= 128;
+  const bool fused = !LOPA && 2 * p.NU <= 128;
   const int ncol = fused ? NB : 2 * NB, ldc = ncol + 1;  // epilogue copy of the accumulator
   float* s_acc = reinterpret_cast<float*>(sm);
   int stage_ok = 1;
@@ -175,7 +207,50 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       tma_prefetch_map(&mW1);
       tma_prefetch_map(&mW3);
       tma_prefetch_map(&mX);
+      if (LOPA) tma_prefetch_map(&mT);
     }
+    if constexpr (LOPA) {
+      // groups [0, NCZ): U and t chunks (K over r); then W3 and x chunks (K over D)
+      auto zgroup = [&](int q) { return q < p.NCZ; };
+      auto nchunks = [&](int q) { return zgroup(q) ? min(C, p.KCZ - q * C) : min(C, p.KC - (q - p.NCZ) * C); };
+      auto kbase = [&](int q) { return (zgroup(q) ? q : q - p.NCZ) * C; };
+      auto tx = [&](int q) { return (uint32_t)nchunks(q) * (wreg + (zgroup(q) ? 2u : 1u) * xreg); };
+      const int npre = min(NS, p.NCG);
+      for (int q = 0; q < npre; ++q) {  // weights first, before the dependency wait
+        uint8_t* st = sm + (size_t)q * st_bytes;
+        if (lane == 0) mbar_arrive_expect_tx(&full[q], tx(q));
+        __syncwarp();
+        if (lane < nchunks(q))
+          tma_tile_2d(st + lane * wreg, zgroup(q) ? &mW1 : &mW3, (kbase(q) + lane) * 64, u0, &full[q]);
+      }
+      pdl_wait();  // t and x come from earlier kernels
+      for (int q = 0; q < npre; ++q)
+        if (lane < nchunks(q))
+          tma_tile_2d(sm + (size_t)q * st_bytes + C * wreg + lane * 2 * xreg, zgroup(q) ? &mT : &mX,
+                      (kbase(q) + lane) * 64, 0, &full[q]);
+      int issued = npre;
+      for (int q = npre; q < p.NCG; ++q) {
+        const int s = q % NS;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&empty[s], ((q / NS) - 1) & 1, abort_flag, err, p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        uint8_t* st = sm + (size_t)s * st_bytes;
+        const int nc = nchunks(q);
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], tx(q));
+        __syncwarp();
+        if (lane < 2 * nc) {
+          const int c = lane >> 1, kb = (kbase(q) + c) * 64;
+          if ((lane & 1) == 0)
+            tma_tile_2d(st + c * wreg, zgroup(q) ? &mW1 : &mW3, kb, u0, &full[s]);
+          else
+            tma_tile_2d(st + C * wreg + c * 2 * xreg, zgroup(q) ? &mT : &mX, kb, 0, &full[s]);
+        }
+        issued = q + 1;
+      }
+      if (lane == 0)
+        for (int q = max(0, issued - NS); q < issued; ++q) mbar_wait_drain(&full[q % NS], (q / NS) & 1, p.timeout_ns);
+      __syncwarp();
+    } else {
     auto nchunks = [&](int q) { return min(C, p.KC - q * C); };
     const int npre = min(NS, p.NCG);
     // the weights do not depend on the previous kernel: request them first
@@ -213,6 +288,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
     if (lane == 0)
       for (int q = max(0, issued - NS); q < issued; ++q) mbar_wait_drain(&full[q % NS], (q / NS) & 1, p.timeout_ns);
     __syncwarp();
+    }
   } else if (warp >= TC_GATE_MMA_WARP0) {
     const int mw = warp - TC_GATE_MMA_WARP0;  // this warp issues K steps kk = mw (mod nacc) into accumulator mw
     if (mw < p.nacc && lane == 0) {
@@ -220,6 +296,33 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       const uint32_t acc_cols = fused ? (uint32_t)NB : 2u * NB;  // columns of one accumulator
       const uint32_t da = tmem + (uint32_t)mw * acc_cols;
       bool started = false;
+      if constexpr (LOPA) {
+        bool started_p = false;
+        for (int q = 0; q < p.NCG; ++q) {
+          const int s = q % NS;
+          if (!mbar_wait(&full[s], (q / NS) & 1, abort_flag, err, p.timeout_ns)) break;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(sm + (size_t)s * st_bytes);
+          const uint64_t a0 = smem_desc(sa, 16, 1024, SMEM_LAYOUT_SW128);
+          const uint64_t b0 = smem_desc(sa + C * wreg, 16, 1024, SMEM_LAYOUT_SW128);
+          const bool zq = q < p.NCZ;
+          const int nc = zq ? min(C, p.KCZ - q * C) : min(C, p.KC - (q - p.NCZ) * C);
+          for (int c = 0; c < nc; ++c) {
+            const uint64_t ac = a0 + ((c * wreg) >> 4), bc = b0 + ((c * 2 * xreg) >> 4);
+            for (int kk = mw; kk < 4; kk += p.nacc) {
+              if (zq) {  // z += U t_hi + U t_lo
+                tc_mma(da, ac + 2 * kk, bc + 2 * kk, idesc, started);
+                tc_mma(da, ac + 2 * kk, bc + (xreg >> 4) + 2 * kk, idesc, true);
+                started = true;
+              } else {   // p += W3 x
+                tc_mma(da + (uint32_t)NB, ac + 2 * kk, bc + 2 * kk, idesc, started_p);
+                started_p = true;
+              }
+            }
+          }
+          tc_commit(&empty[s]);
+        }
+      } else {
       for (int q = 0; q < p.NCG; ++q) {
         const int s = q % NS;
         if (!mbar_wait(&full[s], (q / NS) & 1, abort_flag, err, p.timeout_ns)) break;
@@ -238,6 +341,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           }
         }
         tc_commit(&empty[s]);
+      }
       }
       tc_commit(done);
       mbar_wait_drain(done, 0, p.timeout_ns);  // every MMA warp's work complete before TMEM is released
@@ -264,13 +368,32 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // ---- epilogue on warps 0..7: thread (unit r, token group g = tid / 64) takes
   // tokens g, g + 4, ... (units in rounds of 64); a warp shares each token, so
   // the counts are ballots
-  if (__syncthreads_and(stage_ok) && warp < 8) {
+  if (LOPA && p.tout) {
+    // t kernel: P = V X^T of this slice of V's rows, stored as a bf16 pair
+    // (zero rows for the padding tokens, so the gate's MMA columns stay finite)
+    if (__syncthreads_and(stage_ok) && warp < 8) {
+      for (int r0 = 0; r0 < p.NU; r0 += 64) {
+        const int r = r0 + (tid & 63), u = u0 + r;
+        if (r < p.NU && u < p.H) {
+          for (int b = tid >> 6; b < NB; b += 4) {
+            const float tv = b < p.B ? s_acc[(size_t)r * ldc + NB + b] : 0.f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
+            p.tout[(size_t)b * p.H + u] = __bfloat16_as_ushort(hi);
+            p.tout[(size_t)(NB + b) * p.H + u] = __bfloat16_as_ushort(lo);
+          }
+        }
+      }
+    }
+  } else if (__syncthreads_and(stage_ok) && warp < 8) {
     for (int r0 = 0; r0 < p.NU; r0 += 64) {
       const int r = r0 + (tid & 63), g = tid >> 6;
       const bool valid = r < p.NU && u0 + r < p.H;
       const int u = u0 + r;
       for (int b = g; b < p.B; b += 4) {
-        const float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
+        float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
+        if (LOPA && valid && (p.flags & FLAG_TILED_G))  // (G x)_u = x_{u mod D}
+          z += __bfloat162float(__ushort_as_bfloat16(p.x[(size_t)b * p.D + u % p.D]));
         const float pv = !valid ? 0.f : fused ? s_acc[(size_t)(p.NU + r) * ldc + b] : s_acc[(size_t)r * ldc + NB + b];
         const float az = activation(p.act, z);
         const bool lv = valid && is_live(az, p.thr);
@@ -501,15 +624,27 @@ int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
   return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-TcPlan plan_ffn_tc(int D, int H, int num_sms) {
+TcPlan plan_ffn_tc(int D, int H, int r, int num_sms) {
   TcPlan p;
-  if (D % 8 != 0 || num_sms < 1) return p;
+  if (D % 8 != 0 || r % 8 != 0 || num_sms < 1) return p;
   const int per = (H + num_sms - 1) / num_sms;
-  p.NU = std::max(8, (per + 7) / 8 * 8);
-  if (p.NU > 128) return p;  // more than 128 units per block: not planned
-  p.MT = p.NU <= 64 ? 64 : 128;
+  // one slice per SM; an MMA covers at most 128 units, so past 128 units per
+  // SM the slices fill more than one wave
+  p.NU = std::min(128, std::max(8, (per + 7) / 8 * 8));
+  // An M = 64 MMA does not map accumulator rows to TMEM lanes one to one (16
+  // rows per 32-lane quarter), so every product that the epilogue reads by
+  // lane runs with M = 128; the rows past NU are never read.  Only the
+  // standard gate's stacked form (2 NU <= 128) has NU <= 64, and it issues M = 128.
+  p.MT = 128;
   p.ntiles = (H + p.NU - 1) / p.NU;
   p.KC = (D + 63) / 64;
+  p.r = r;
+  p.KCZ = (r + 63) / 64;
+  p.num_sms = num_sms;
+  if (r > 0) {  // the t kernel: slices of V's rows
+    p.NUt = std::min(128, std::max(8, ((r + num_sms - 1) / num_sms + 7) / 8 * 8));
+    p.ntiles_t = (r + p.NUt - 1) / p.NUt;
+  }
   p.ndt = (D + TC_DTILE - 1) / TC_DTILE;
   p.nch = (H + TC_UCH - 1) / TC_UCH;
   p.nsplit = std::max(1, std::min(p.nch, num_sms / p.ndt));
@@ -523,9 +658,11 @@ TcPlan plan_ffn_tc(int D, int H, int num_sms) {
 
 size_t ffn_tc_hbuf_elems(const TcPlan& p) { return (size_t)2 * 128 * p.Hs; }
 
-int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, const void* W2t, uint16_t* hbuf,
-                   int D, int H) {
-  int rc = encode_2d(&m->w1, W1, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NU);
+int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, const void* W3, const void* W2t,
+                   uint16_t* hbuf, int D, int H) {
+  const int gk = p.r > 0 ? p.r : D;  // W1 [H, D] or U [H, r]
+  int rc = encode_2d(&m->w1, W1, (uint64_t)H, (uint64_t)gk, (uint64_t)gk * 2, (uint32_t)p.NU);
+  if (!rc && p.r > 0) rc = encode_2d(&m->v, V, (uint64_t)p.r, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NUt);
   if (!rc) rc = encode_2d(&m->w3, W3, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NU);
   if (!rc) rc = encode_2d(&m->w2, W2t, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, TC_UCH);
   for (int i = 0; i < 8 && !rc; ++i)  // h boxes of 2 NB rows, NB = 16 (i + 1)
@@ -534,61 +671,98 @@ int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, c
 }
 
 cudaError_t ffn_tc_prepare(size_t max_smem) {
-  cudaError_t e =
-      cudaFuncSetAttribute(ffn_tc_gateup_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
-  if (!e)
-    e = cudaFuncSetAttribute(ffn_tc_gateup_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  void (*ks[2])(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcGateArgs) = {
+      ffn_tc_gateup_kernel<128, false>, ffn_tc_gateup_kernel<128, true>};
+  cudaError_t e = cudaSuccess;
+  for (auto k : ks)
+    if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   if (!e) e = cudaFuncSetAttribute(ffn_tc_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   return e;
 }
 
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
-                  cudaError_t* cuda_err) {
+                  cudaError_t* cuda_err, bool tpair_ready) {
   *cuda_err = cudaSuccess;
-  if (!plan.ok || B < 1 || B > 128) return -1;
+  const bool lopa = plan.r > 0;
+  if (!plan.ok || B < 1 || B > 128 || (lopa && !buf.tpair)) return -1;
   const int NB = (B + 15) / 16 * 16;
-  CUtensorMap mx;
+  CUtensorMap mx, mt;
   if (int rc = encode_2d(&mx, x, (uint64_t)B, (uint64_t)D, (uint64_t)D * 2, (uint32_t)NB)) return rc;
-
-  TcGateArgs g;
-  g.D = D;
-  g.H = H;
-  g.B = B;
-  g.NB = NB;
-  g.NU = plan.NU;
-  g.KC = plan.KC;
-  // four K chunks per stage; two once x makes up a large part of a stage (measured)
-  g.C = plan.gate_chunks > 0 ? plan.gate_chunks : (NB >= 48 ? 2 : 4);
-  while (g.C > 1 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, 2) > std::min(max_smem, (size_t)TC_SMEM_BUDGET)) g.C >>= 1;
-  g.NCG = (plan.KC + g.C - 1) / g.C;
-  g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.gate_smem_budget / gate_stage_bytes(g.C, plan.NU, NB)));
-  while (g.NS > 2 && gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS) > max_smem) --g.NS;
-  g.act = act;
-  g.flags = flags;
-  g.thr = thr;
-  g.Hs = plan.Hs;
-  {
-    const int cols = 2 * plan.NU <= 128 ? NB : 2 * NB;  // one accumulator
-    g.nacc = cols <= 128 ? 4 : 2;  // MMA warps = accumulators, nacc * cols <= 512
-    g.tmem_cols = tmem_cols_for(g.nacc * cols);
+  if (lopa) {  // the t pair of every token: rows [0, NB) t_hi, [NB, 2 NB) t_lo
+    if (int rc = encode_2d(&mt, buf.tpair, (uint64_t)(2 * NB), (uint64_t)plan.r, (uint64_t)plan.r * 2,
+                           (uint32_t)(2 * NB)))
+      return rc;
+  } else {
+    mt = mx;  // not read
   }
-  g.ctrl = buf.ctrl;
-  g.mask = buf.mask;
-  g.hbuf = buf.hbuf;
-  g.timeout_ns = timeout_ns;
-  const size_t smem1 = gate_smem_bytes(g.C, plan.MT, plan.NU, NB, g.NS);
-  // the epilogue stages the accumulator [128][2 NB + 1] fp32 over the pipeline stages
-  if ((size_t)g.NS * gate_stage_bytes(g.C, plan.NU, NB) < (size_t)128 * (2 * NB + 1) * 4 || smem1 > max_smem) {
+  // gate-up arguments for slices of NU rows of a [Hg, .] matrix (the t kernel: V's r rows, no U chunks).
+  // More slices than SMs: two blocks per SM (half the shared memory and TMEM each), so that the
+  // slices run in one wave; not with NB = 128, whose accumulator copy needs 132 KB.
+  auto gate_args = [&](int NU, int Hg, bool with_u, uint16_t* tout, TcGateArgs& g, size_t& smem) {
+    const bool two = (Hg + NU - 1) / NU > plan.num_sms && NB <= 64;
+    const size_t cap = two ? std::min(max_smem, (size_t)110 * 1024) : max_smem;
+    const size_t budget = two ? std::min(plan.gate_smem_budget, (size_t)100 * 1024) : plan.gate_smem_budget;
+    auto stage_bytes = [&](int C) { return lopa ? lopa_stage_bytes(C, NU, NB) : gate_stage_bytes(C, NU, NB); };
+    auto smem_bytes = [&](int C, int NS) {
+      return lopa ? lopa_smem_bytes(C, plan.MT, NU, NB, NS) : gate_smem_bytes(C, plan.MT, NU, NB, NS);
+    };
+    g.D = D;
+    g.H = Hg;
+    g.B = B;
+    g.NB = NB;
+    g.NU = NU;
+    g.KC = plan.KC;
+    // four K chunks per stage; two once x makes up a large part of a stage (measured)
+    g.C = plan.gate_chunks > 0 ? plan.gate_chunks : (NB >= 48 ? 2 : 4);
+    while (g.C > 1 && smem_bytes(g.C, 2) > std::min(cap, (size_t)TC_SMEM_BUDGET)) g.C >>= 1;
+    g.KCZ = with_u ? plan.KCZ : 0;
+    g.NCZ = (g.KCZ + g.C - 1) / g.C;
+    g.NCG = g.NCZ + (plan.KC + g.C - 1) / g.C;
+    g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, budget / stage_bytes(g.C)));
+    while (g.NS > 2 && smem_bytes(g.C, g.NS) > cap) --g.NS;
+    g.act = act;
+    g.flags = flags;
+    g.thr = thr;
+    g.Hs = plan.Hs;
+    g.x = static_cast<const uint16_t*>(x);
+    g.tout = tout;
+    const int cols = !lopa && 2 * NU <= 128 ? NB : 2 * NB;  // one accumulator
+    g.nacc = cols <= 128 ? 4 : 2;  // MMA warps = accumulators, nacc * cols <= 512
+    if (two) g.nacc = std::min(g.nacc, 256 / cols);  // <= 256 columns per block
+    g.tmem_cols = tmem_cols_for(g.nacc * cols);
+    g.ctrl = buf.ctrl;
+    g.mask = buf.mask;
+    g.hbuf = buf.hbuf;
+    g.timeout_ns = timeout_ns;
+    smem = smem_bytes(g.C, g.NS);
+    // the epilogue stages the accumulator [128][2 NB + 1] fp32 over the pipeline stages
+    return (size_t)g.NS * stage_bytes(g.C) >= (size_t)128 * (2 * NB + 1) * 4 && smem <= cap;
+  };
+  const dim3 gb(TC_GATE_THREADS);
+  cudaError_t e = cudaSuccess;
+  if (lopa && !tpair_ready) {
+    TcGateArgs gt;
+    size_t smt = 0;
+    if (!gate_args(plan.NUt, plan.r, false, buf.tpair, gt, smt)) {
+      *cuda_err = cudaErrorInvalidConfiguration;
+      return 0;
+    }
+    e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t), gb, smt, s, maps.v, maps.v, mx, mx, gt);
+    if (e) {
+      *cuda_err = e;
+      return 0;
+    }
+  }
+  TcGateArgs g;
+  size_t smem1 = 0;
+  if (!gate_args(plan.NU, H, lopa, nullptr, g, smem1)) {
     *cuda_err = cudaErrorInvalidConfiguration;
     return 0;
   }
-  cudaError_t e =
-      plan.MT == 64
-          ? launch_pdl(ffn_tc_gateup_kernel<64>, dim3(plan.ntiles), dim3(TC_GATE_THREADS), smem1, s, maps.w1, maps.w3,
-                       mx, g)
-          : launch_pdl(ffn_tc_gateup_kernel<128>, dim3(plan.ntiles), dim3(TC_GATE_THREADS), smem1, s, maps.w1, maps.w3, mx,
-                       g);
+  const dim3 gg(plan.ntiles);
+  e = lopa ? launch_pdl(ffn_tc_gateup_kernel<128, true>, gg, gb, smem1, s, maps.w1, maps.w3, mx, mt, g)
+           : launch_pdl(ffn_tc_gateup_kernel<128, false>, gg, gb, smem1, s, maps.w1, maps.w3, mx, mt, g);
   if (e) {
     *cuda_err = e;
     return 0;

@@ -83,14 +83,18 @@ cudaError_t launch_ffn_batch(const B1Params& p, int nb, int dtype, bool lopa, in
 struct TcPlan {
   bool ok = false;
   int NU = 0, MT = 0, ntiles = 0, KC = 0;
+  int r = 0, KCZ = 0;  // low-rank gate: rank and its 64-wide K chunks (0: standard gate)
+  int NUt = 0, ntiles_t = 0;  // low-rank gate: rows of V per block of the t kernel, and its blocks
+  int num_sms = 0;
   int ndt = 0, nch = 0, nsplit = 0;
   int Hs = 0;  // row stride (elements) of the h buffer
   size_t gate_smem_budget = 0, down_smem_budget = 0;  // pipeline-stage bytes per block
   int gate_chunks = 0;                                // 64-wide K chunks per gate-up stage (0: 4)
 };
 struct TcMaps {
-  CUtensorMap w1, w3;  // W1, W3 [H, D]: boxes of 64 columns x NU rows
+  CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
   CUtensorMap w2;      // W2^T [H, D]: boxes of 64 columns x 64 rows
+  CUtensorMap v;       // V [r, D] (low-rank gate): boxes of 64 columns x NUt rows
   CUtensorMap h[8];    // h buffer [256, H]: boxes of 64 columns x 2 NB rows, NB = 16 (i + 1)
 };
 struct TcBuffers {
@@ -100,9 +104,10 @@ struct TcBuffers {
   uint8_t* mask;   // [B_max, H]
   int* counts;     // [B_max] published live counts
   int* tickets;    // [TC_TICKETS] zero between calls
+  uint16_t* tpair; // low-rank gate: [2 NB, r] bf16, t_hi rows then t_lo rows (the t kernel); else null
 };
 constexpr int TC_TICKETS = 64;  // >= slices of 128 y values (D <= 8192)
-TcPlan plan_ffn_tc(int D, int H, int num_sms);
+TcPlan plan_ffn_tc(int D, int H, int r, int num_sms);
 // Tensor map of a bf16 matrix [rows, cols] (row stride in bytes): boxes of 64
 // columns x box_rows rows, 128-byte swizzle.  0 on success, else a driver
 // status (-1: the encoder entry point is unavailable).
@@ -110,14 +115,20 @@ int encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
               uint32_t box_rows);
 size_t ffn_tc_hbuf_elems(const TcPlan& p);
 // 0 on success, else a driver status (or -1: tensor-map encoder unavailable)
-int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* W3, const void* W2t, uint16_t* hbuf,
-                   int D, int H);
+int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, const void* W3, const void* W2t,
+                   uint16_t* hbuf, int D, int H);
 cudaError_t ffn_tc_prepare(size_t max_smem);
-// Whole forward (y and counts written; no finalize kernel).  Returns 0 and sets
+// Whole forward (y and counts written; no finalize kernel).  Low-rank gate:
+// tpair_ready says the caller already wrote the t pair (launch_lopa_t_pair);
+// otherwise the t kernel runs on the tensor cores first.  Returns 0 and sets
 // *cuda_err to the launch status, or a non-zero encode status.
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
-                  cudaError_t* cuda_err);
+                  cudaError_t* cuda_err, bool tpair_ready = false);
+// Low-rank batches of up to this many tokens take the CUDA-core t kernel
+// (measured: 33.5 against 36.0 us per call at B = 4 on the low-rank workload;
+// from B = 8 the tensor-core t kernel is faster).
+constexpr int TC_T_CUDA_CORE_MAX_B = 4;
 
 // Small batches (2..8 tokens, bf16, standard gate; ffn_tcu.cu): the gate on the
 // tensor cores, the union of the live sets gathered on the CUDA cores, fp32
@@ -146,6 +157,12 @@ cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,
                           cudaStream_t s);
+// The same for bf16 tensor-core batches, written as a bf16 pair into tpair
+// [2 NB, r]: t_hi of token b in row b, t_lo in row NB + b, zero rows for b >= B.
+// lopa_t_prepare raises the batch kernel's shared-memory limit (once per process).
+cudaError_t lopa_t_prepare();
+cudaError_t launch_lopa_t_pair(const void* V, const void* x, uint16_t* tpair, int r, int D, int B, int NB,
+                               cudaStream_t s);
 
 // W2[D, H] -> W2t[H, D] (element size 1, 2 or 4 bytes).
 cudaError_t launch_transpose(const void* src, void* dst, int rows, int cols, int elt_bytes,

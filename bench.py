@@ -15,10 +15,14 @@ peak and of the nominal 8 TB/s, the same figures for the dense bf16 FFN
 (cuBLAS through torch), and for the variants: the low-rank gate layer
 (D=2560, H'=9787, r=400, 32 rotated sets) alone and in the full form (tiled
 identity G, RMSNorm, double activation), the smooth SiLU gate with a live
-threshold, weight-only int8 weights, and batches of 4 / 16 / 64 tokens on the
-tensor cores; an end-to-end figure with host buffers, SM clocks sampled during
-the timed region, and the fp64 CPU oracle timed on a bounded sample of the
-same workload.
+threshold, weight-only int8 weights, batches of 2 tokens (union gathers) and
+of 4 / 16 / 64 tokens on the tensor cores for both gates; an end-to-end figure
+with host buffers, SM clocks sampled during the timed region, and the fp64 CPU
+oracle timed on a bounded sample of the same workload.
+
+--sweep runs the D=4096 sparsity x batch sweep instead (standard gate H=14336
+and low-rank gate H'=19649, r=640; s in {0.5, 0.75, 0.9, 0.95}; B in {1, 8,
+32, 128}; each point next to the dense bf16 FFN), one JSON line per point.
 
 --impl reference times the reference arm: the fp64 CPU oracle, as it stands,
 on the host cores (rank 0 only), on a bounded sample of the same workload.
@@ -374,6 +378,41 @@ def batched_extras(ffns, layers, x, stream, args, peak):
     return out
 
 
+def lopa_batched_extras(ffns, x, stream, args, peak, D, Hp, r):
+    """Batched decode of the low-rank layer sets on the tensor cores: t as a bf16 pair, the gate
+    U t and the up projection in one gate-up kernel, the down kernel; B tokens per call."""
+    import torch
+    import activation_sparse_gated_gb300 as sffn
+    out = {}
+    n_sets = len(ffns)
+    for B in (4, 16, 64):
+        calls = x.shape[0] // B
+        y = torch.empty_like(x)
+        unions = []
+        with torch.cuda.stream(stream):
+            for t in range(min(calls, 64)):
+                f = ffns[t % n_sets]
+                sffn.sffn_forward(f.h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+                unions.append(int(f.active_mask(B).any(axis=0).sum()))
+        stream.synchronize()
+        mean_union = sum(unions) / len(unions)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(calls):
+                sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+        us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
+        del g
+        # streamed: U, V and every slice of W3 and W2^T, plus x, y, the t pair and the h pair
+        streamed = 2 * r * (D + Hp) + 2 * 2 * Hp * D + 2 * 2 * B * D + 2 * 2 * B * r + 2 * 2 * 2 * B * Hp
+        union_bytes = 2 * r * (D + Hp) + 2 * 2 * mean_union * D + 2 * 2 * B * D
+        out[f"B{B}"] = {"path": "tensor cores: t pair, gate-up (U t and W3 x) + down kernels",
+                        "us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,
+                        "union_fraction": mean_union / Hp, "bytes_per_call": streamed,
+                        "union_gather_bytes": union_bytes, "gbs": streamed / (us * 1e3),
+                        "frac_of_measured": streamed / (us * 1e3) / peak, "gpu_launches_per_call": 3}
+    return out
+
+
 def run_gpu(args):
     import torch
     import activation_sparse_gated_gb300 as sffn
@@ -482,7 +521,9 @@ def run_gpu(args):
                           "speedup_vs_dense_bf16": us_dense / lus, "gpu_launches_per_call": 3,
                           "flop_ratio_eq4": flops.dense_macs(D, H) /
                           flops.lopa_macs(D, Hp, r, sum(lcounts) / len(lcounts))}
-        del lffns, lg
+        del lg
+        lopa_batched = lopa_batched_extras(lffns, lx, stream, args, peak, D, Hp, r)
+        del lffns
         # the pages' complete low-rank form: W1(x) = Gx + U RMSNorm(Vx), double activation
         import activation_sparse_gated_gb300 as sffn_mod
         full = sffn_mod.SFFN_GATE_TILED_G | sffn_mod.SFFN_GATE_RMSNORM | sffn_mod.SFFN_DOUBLE_ACT
@@ -532,6 +573,11 @@ def run_gpu(args):
                                   "speedup_vs_dense_bf16": us_dense / qus, "gpu_launches_per_call": 2}
         del qffns, qg
         extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
+        for k, v in lopa_batched.items():  # against the dense standard layer at the same batch (iso-parameter)
+            dus = extras["batched"][k]["dense_bf16_us_per_call"]
+            v["dense_bf16_us_per_call"] = dus
+            v["speedup_vs_dense_bf16"] = dus / v["us_per_call"]
+        extras["lopa_batched"] = lopa_batched
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -575,6 +621,141 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+SWEEP_WORKLOAD = "sweep-bf16-D4096-H14336"
+
+
+def dense_us(ld, x, B, stream, steps, warmup):
+    """Dense bf16 FFN via cuBLAS (torch), B tokens per call, call t through set t mod len(ld): the
+    faster of the three-GEMM and the concatenated [W1; W3] forms, us per call."""
+    import torch
+    import torch.nn.functional as F
+    calls = x.shape[0] // B
+    H = ld[0]["W1"].shape[0]
+    y = torch.empty_like(x)
+    best = None
+    for form in ("three", "concat"):
+        def body():
+            for t in range(calls):
+                L = ld[t % len(ld)]
+                xt = x[t * B:(t + 1) * B]
+                if form == "three":
+                    h = F.relu(F.linear(xt, L["W1"])) * F.linear(xt, L["W3"])
+                else:
+                    zu = F.linear(xt, L["W13"])
+                    h = F.relu(zu[:, :H]) * zu[:, H:]
+                y[t * B:(t + 1) * B] = F.linear(h, L["W2"])
+        with torch.cuda.stream(stream):
+            body()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body()
+        us = 1e6 * time_graph(g, stream, steps, warmup) / (steps * calls)
+        best = us if best is None else min(best, us)
+        del g
+    return best
+
+
+def run_sweep(args):
+    """Sparsity x batch sweep at D=4096: standard gate (H=14336) and low-rank gate (H'=19649, r=640),
+    s in {0.5, 0.75, 0.9, 0.95}, B in {1, 8, 32, 128}, 1024 tokens per point, each point next to the
+    dense bf16 FFN of the standard shape.  One JSON line per point.
+
+    Weight sets: the four generated sets of each gate.  The standard gate rotates four handles (gate
+    matrices 470 MB, 3.6x L2).  The low-rank gate matrices of four sets are only 122 MB, so the
+    low-rank points rotate sixteen handles (each set loaded into four, every handle a separate copy in
+    HBM: 491 MB of gate weights, 3.8x L2).  A sparsity is set by rewriting the bias column (W1[:, D-1]
+    or U[:, r-1]) with -Phi^{-1}(s), which gives the same weights as generating the set at that s."""
+    import time
+    import torch
+    import activation_sparse_gated_gb300 as sffn
+    from activation_sparse_gated_gb300 import build as libbuild
+    from activation_sparse_gated_gb300 import synthetic as syn
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    libbuild.build()
+    sffn.load()
+    t_start = time.time()
+    w = syn.WORKLOADS[SWEEP_WORKLOAD]
+    D, H, r, Hp, n_sets = w["D"], w["H"], w["r"], w["Hp"], w["sets"]
+    x = syn.workload_tokens(SWEEP_WORKLOAD).to(dev)
+    n_tok = x.shape[0]
+    stream = torch.cuda.Stream(device=dev)
+    peak, _ = measured_peaks()
+    elt = 2
+    tc_min = int(os.environ.get("SFFN_TC_MIN_BATCH", "2"))
+    points = 0
+    dense = {}
+    for gate in ("standard", "lopa"):
+        layers = syn.workload_layers(SWEEP_WORKLOAD, sets=n_sets, gate=gate, s=0.9)
+        for lw in layers:
+            for k in ("W1", "U", "V", "W3", "W2"):
+                if getattr(lw, k) is not None:
+                    setattr(lw, k, getattr(lw, k).to(dev))
+        if gate == "standard":
+            ld = [{"W1": lw.W1, "W3": lw.W3, "W2": lw.W2, "W13": torch.cat([lw.W1, lw.W3], 0)} for lw in layers]
+            for B in w["B"]:
+                dense[B] = dense_us(ld, x, B, stream, args.steps, args.warmup)
+            del ld
+        handles = layers if gate == "standard" else layers * 4
+        Hg = H if gate == "standard" else Hp
+        for s in w["s"]:
+            shift = torch.tensor(syn.shift_for_sparsity(s), dtype=torch.float32).to(torch.bfloat16)
+            for lw in layers:
+                if gate == "standard":
+                    lw.W1[:, D - 1] = shift.to(dev)
+                else:
+                    lw.U[:, r - 1] = shift.to(dev)
+            ffns = build_ffns(handles, dev)
+            torch.cuda.synchronize()
+            for B in w["B"]:
+                calls = n_tok // B
+                y = torch.empty_like(x)
+                lives, unions = [], []
+                with torch.cuda.stream(stream):
+                    for t in range(min(calls, 256)):
+                        f = ffns[t % len(ffns)]
+                        sffn.sffn_forward(f.h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+                        m = f.active_mask(B)
+                        lives.append(float(m.sum(axis=1).mean()))
+                        unions.append(int(m.any(axis=0).sum()))
+                stream.synchronize()
+                live, union = sum(lives) / len(lives), sum(unions) / len(unions)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for t in range(calls):
+                        sffn.sffn_forward(ffns[t % len(ffns)].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B],
+                                          B, stream)
+                us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
+                del g
+                gate_bytes = elt * H * D if gate == "standard" else elt * r * (D + Hp)
+                bytes_call = gate_bytes + 2 * elt * union * D + 2 * elt * B * D
+                if B == 1:
+                    path = "stream kernel" + (" + low-rank t kernel" if gate == "lopa" else "")
+                elif B >= tc_min:
+                    path = ("tensor cores: gate-up + down kernels (streams every unit slice)" if gate == "standard"
+                            else "tensor cores: t pair, gate-up (U t and W3 x) + down kernels")
+                else:
+                    path = "CUDA cores, union gathers, <= 8 tokens per pass"
+                gbs = bytes_call / (us * 1e3)
+                print(json.dumps({
+                    "sweep": SWEEP_WORKLOAD, "gate": gate, "s": s, "B": B, "D": D, "H": Hg,
+                    "r": r if gate == "lopa" else 0, "weight_sets": len(ffns), "path": path,
+                    "us_per_call": us, "tokens_per_s": B * 1e6 / us,
+                    "measured_sparsity": 1 - live / Hg, "union_fraction": union / Hg,
+                    "bytes_per_call": bytes_call, "gbs": gbs, "frac_of_measured": gbs / peak,
+                    "dense_bf16_us_per_call": dense[B], "speedup_vs_dense_bf16": dense[B] / us,
+                    "dense_bf16_gbs": (3 * elt * H * D + 2 * elt * B * D) / (dense[B] * 1e3)}), flush=True)
+                points += 1
+            del ffns
+            torch.cuda.synchronize()
+        del layers, handles
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": SWEEP_WORKLOAD, "points": points, "seconds": time.time() - t_start,
+                      "peak_gbs": peak}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,6 +765,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the dense and low-rank comparisons")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the D=4096 sparsity x batch sweep (both gates, one JSON line per point) instead of the step")
     ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
                     help="(internal) time the oracle on this process's OpenMP threads for SECONDS, print JSON")
     args = ap.parse_args()
@@ -594,7 +777,9 @@ def main():
                                    args.oracle_one_thread, 64)
         print(json.dumps({"tokens": n, "seconds": dt, "cores": cores}), flush=True)
         return
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

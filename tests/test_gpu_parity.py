@@ -251,6 +251,18 @@ def test_sweep_batch8_d4096(gate):
     check(lw, x, y, c, m)
 
 
+@pytest.mark.parametrize("gate,s,B", [("standard", 0.95, 128), ("standard", 0.5, 32), ("lopa", 0.9, 32),
+                                      ("lopa", 0.95, 1)])
+def test_sweep_points_d4096(gate, s, B):
+    """Corners of the D = 4096 sparsity x batch sweep, in the launch configuration the sweep times."""
+    name = "sweep-bf16-D4096-H14336"
+    lw = syn.workload_layers(name, sets=1, gate=gate, s=s)[0]
+    x = syn.workload_tokens(name, max(B, 2))
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
 def test_live_set_is_deterministic():
     lw = syn.standard_layer(1024, 4096, dtype="bf16", seed=41)
     x = syn.tokens(3, 1024, dtype="bf16", seed=42)
@@ -427,6 +439,45 @@ def test_union_gather_kernel(monkeypatch, B, act, thr, flags):
     A = check_thr(lw, x, y_s, c_s, m_s, act, thr, flags)
     sure = np.abs(A - thr) > 1e-3
     assert np.array_equal(m_u[sure], m_s[sure])
+
+
+@pytest.mark.parametrize("D,H,r,B", [
+    (512, 2000, 64, 16),     # one K chunk of r
+    (520, 1500, 40, 5),      # r < 64 (zero-filled K tail), D not a multiple of 64
+    (512, 3000, 400, 33),    # r = 400: seven K chunks, the second group partial
+    (384, 1000, 8, 128),     # the smallest rank, the largest batch (two accumulators)
+    (64, 151, 16, 2),        # a tiny layer, two tokens
+    (256, 19649, 64, 8),     # more than 128 units per SM: two blocks per SM
+    (256, 19649, 64, 100),   # ... with NB = 128: a second wave of slices
+    (1024, 4000, 128, 12),   # t on the tensor cores (B > 8)
+])
+def test_batched_lopa_tensor_cores(D, H, r, B):
+    """Low-rank batches on the tensor cores: t as a bf16 pair (CUDA cores up to 8 tokens, tensor
+    cores above), U t_hi + U t_lo in one accumulator."""
+    lw = syn.lopa_layer(D, H, r, dtype="bf16", seed=D + r)
+    x = syn.tokens(B, D, dtype="bf16", seed=H)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("B", [4, 64])
+def test_batched_lopa_workload_full_size(B):
+    name = "lopa-bf16-D2560-H9787-r400-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    x = syn.workload_tokens(name, B)
+    y, c, m = run_tokens(make_ffn(lw), x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("B", [16, 128])
+def test_batched_standard_more_slices_than_sms(B):
+    """A standard gate with more than 128 units per SM on the tensor cores: two blocks per SM
+    (B = 16) or a second wave (B = 128)."""
+    lw = syn.standard_layer(256, 20000, dtype="bf16", seed=91)
+    x = syn.tokens(B, 256, dtype="bf16", seed=92)
+    y, c, m = run_tokens(make_ffn(lw), x, B=B)
+    check(lw, x, y, c, m)
 
 
 # --------------------------------------------------------------------------- the full low-rank gate
