@@ -76,6 +76,7 @@ struct sffn_s {
   uint16_t* hbuf = nullptr;
   int* tickets = nullptr;
   uint16_t* tpair = nullptr;  // low-rank gate: [256, r] bf16 t pairs of a tensor-core batch
+  float* tacc = nullptr;      // low-rank gate: [128, r] fp32 partial sums of the t kernel
   // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
   float* qs1 = nullptr;
   float* qs3 = nullptr;
@@ -100,6 +101,7 @@ void release(sffn_s* h) {
   cudaFree(h->hbuf);
   cudaFree(h->tickets);
   cudaFree(h->tpair);
+  cudaFree(h->tacc);
   cudaFree(h->qs1);
   cudaFree(h->qs3);
   cudaFree(h->qs2);
@@ -321,14 +323,16 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     h->tc = plan_ffn_tc(D, H, r, h->num_sms);
     if (h->tc.ok && r > 0) {
       h->tcu_max_batch = 0;  // the union-gather kernel computes a standard gate only
-      if ((e = cudaMalloc(&h->tpair, sizeof(uint16_t) * 256 * r))) return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
-      if ((e = cudaMemset(h->tpair, 0, sizeof(uint16_t) * 256 * r))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+      if ((e = cudaMalloc(&h->tpair, sizeof(uint16_t) * 256 * r)) || (e = cudaMalloc(&h->tacc, sizeof(float) * 128 * r)))
+        return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
+      if ((e = cudaMemset(h->tpair, 0, sizeof(uint16_t) * 256 * r)) || (e = cudaMemset(h->tacc, 0, sizeof(float) * 128 * r)))
+        return bail(SFFN_ERR_CUDA, "cudaMemset", e);
     }
     if (h->tc.ok) {
       if ((e = cudaMalloc(&h->hbuf, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))) ||
-          (e = cudaMalloc(&h->tickets, sizeof(int) * TC_TICKETS)))
+          (e = cudaMalloc(&h->tickets, sizeof(int) * 2 * TC_TICKETS)))  // down kernel, then t kernel
         return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
-      if ((e = cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+      if ((e = cudaMemset(h->tickets, 0, sizeof(int) * 2 * TC_TICKETS))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if (const char* env = std::getenv("SFFN_TC_GATE_KB")) h->tc.gate_smem_budget = (size_t)std::atoi(env) * 1024;
       if (const char* env = std::getenv("SFFN_TC_DOWN_KB")) h->tc.down_smem_budget = (size_t)std::atoi(env) * 1024;
       if (const char* env = std::getenv("SFFN_TC_GATE_CHUNKS")) h->tc.gate_chunks = std::max(1, std::min(4, std::atoi(env)));
@@ -340,6 +344,7 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
         if (r == 0) h->tcu_max_batch = std::max(0, std::min(8, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TC_MIN_BATCH")) h->tc_min_batch = std::max(1, std::atoi(env));
       if (const char* env = std::getenv("SFFN_TC_T_CUDA_MAX_B")) h->tc_t_cuda_max = std::max(0, std::atoi(env));
+      if (const char* env = std::getenv("SFFN_TC_T_SPLIT_TOKENS")) h->tc.t_split_tokens = std::max(16, std::atoi(env));
     }
   }
   if ((e = cudaDeviceSynchronize())) return bail(SFFN_ERR_CUDA, "cudaDeviceSynchronize", e);
@@ -471,7 +476,8 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     // whole batch on the tensor cores: (t kernel,) gate-up kernel, down kernel
     const bool t_cuda_cores = lopa && B <= h->tc_t_cuda_max;
     if (t_cuda_cores) SFFN_CUDA(launch_lopa_t_pair(h->V, x, h->tpair, h->r, h->D, B, (B + 15) / 16 * 16, s));
-    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, h->tpair};
+    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, h->tpair, h->tacc,
+                  h->tickets + TC_TICKETS};
     cudaError_t ce = cudaSuccess;
     if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, h->thr, kTimeoutNs,
                                h->max_smem, s, &ce, t_cuda_cores))

@@ -30,9 +30,11 @@
 //
 // Low-rank gate ("LoPA Gating: moving the ceiling", W1 = UV), three kernels:
 //   t kernel: the gate-up kernel's low-rank form with no U chunks and V in
-//             place of W3, so it computes T = V X^T (one block per slice of
-//             the r rows of V); its epilogue stores t_b as a bf16 pair, t_hi
-//             in rows [0, NB) and t_lo in rows [NB, 2 NB) of one buffer;
+//             place of W3, so it computes T = V X^T; its blocks split K: one
+//             block per (128 rows of V, range of D), partial sums added into
+//             an fp32 accumulator, and the last block of a row tile (a
+//             ticket) stores t_b as a bf16 pair, t_hi in rows [0, NB) and
+//             t_lo in rows [NB, 2 NB) of one buffer, and clears the sums;
 //   gate-up:  the first K chunk groups run over the r columns of U, two MMAs
 //             per K step into the Z accumulator (U t_hi, then U t_lo), the
 //             remaining groups over the D columns of W3 into the P accumulator;
@@ -81,6 +83,9 @@ struct TcGateArgs {
   int KCZ, NCZ;          // low-rank gate: K chunks of r and the chunk groups they fill (the first NCZ)
   const uint16_t* x;     // [B, D] bf16 bits (the tiled identity G of the low-rank gate)
   uint16_t* tout;        // t kernel: the t pair [2 NB, H] (H = r) instead of h, masks and counts
+  int ksplit;            // blocks per slice, each over a range of the K chunks (the t kernel; else 1)
+  float* tacc;           // t kernel: [B, H] fp32 partial sums, zero between calls
+  int* tickets;          // t kernel: [slices] blocks done, zero between calls
   float thr;  // live iff |A(z)| > thr
   uint32_t tmem_cols;
   int* ctrl;
@@ -174,7 +179,11 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   int* s_cnt = reinterpret_cast<int*>(tslot + 2);  // [NB] live counts of this slice
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int u0 = blockIdx.x * p.NU;
+  const int tile = blockIdx.x / p.ksplit, split = blockIdx.x - tile * p.ksplit;
+  const int u0 = tile * p.NU;
+  // this block's K chunks of the D-wide product: a range when the t kernel splits K, else all of them
+  const int kc0 = (int)((long long)split * p.KC / p.ksplit), kc1 = (int)((long long)(split + 1) * p.KC / p.ksplit);
+  const int NCG = p.NCZ + (kc1 - kc0 + C - 1) / C;
   int* err = p.ctrl + CTRL_ERR;
 
   if (tid == 0) {
@@ -212,10 +221,10 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
     if constexpr (LOPA) {
       // groups [0, NCZ): U and t chunks (K over r); then W3 and x chunks (K over D)
       auto zgroup = [&](int q) { return q < p.NCZ; };
-      auto nchunks = [&](int q) { return zgroup(q) ? min(C, p.KCZ - q * C) : min(C, p.KC - (q - p.NCZ) * C); };
-      auto kbase = [&](int q) { return (zgroup(q) ? q : q - p.NCZ) * C; };
+      auto kbase = [&](int q) { return zgroup(q) ? q * C : kc0 + (q - p.NCZ) * C; };
+      auto nchunks = [&](int q) { return zgroup(q) ? min(C, p.KCZ - q * C) : min(C, kc1 - kbase(q)); };
       auto tx = [&](int q) { return (uint32_t)nchunks(q) * (wreg + (zgroup(q) ? 2u : 1u) * xreg); };
-      const int npre = min(NS, p.NCG);
+      const int npre = min(NS, NCG);
       for (int q = 0; q < npre; ++q) {  // weights first, before the dependency wait
         uint8_t* st = sm + (size_t)q * st_bytes;
         if (lane == 0) mbar_arrive_expect_tx(&full[q], tx(q));
@@ -229,7 +238,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           tma_tile_2d(sm + (size_t)q * st_bytes + C * wreg + lane * 2 * xreg, zgroup(q) ? &mT : &mX,
                       (kbase(q) + lane) * 64, 0, &full[q]);
       int issued = npre;
-      for (int q = npre; q < p.NCG; ++q) {
+      for (int q = npre; q < NCG; ++q) {
         const int s = q % NS;
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&empty[s], ((q / NS) - 1) & 1, abort_flag, err, p.timeout_ns);
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       bool started = false;
       if constexpr (LOPA) {
         bool started_p = false;
-        for (int q = 0; q < p.NCG; ++q) {
+        for (int q = 0; q < NCG; ++q) {
           const int s = q % NS;
           if (!mbar_wait(&full[s], (q / NS) & 1, abort_flag, err, p.timeout_ns)) break;
           tc_fence_after();
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           const uint64_t a0 = smem_desc(sa, 16, 1024, SMEM_LAYOUT_SW128);
           const uint64_t b0 = smem_desc(sa + C * wreg, 16, 1024, SMEM_LAYOUT_SW128);
           const bool zq = q < p.NCZ;
-          const int nc = zq ? min(C, p.KCZ - q * C) : min(C, p.KC - (q - p.NCZ) * C);
+          const int nc = zq ? min(C, p.KCZ - q * C) : min(C, kc1 - (kc0 + (q - p.NCZ) * C));
           for (int c = 0; c < nc; ++c) {
             const uint64_t ac = a0 + ((c * wreg) >> 4), bc = b0 + ((c * 2 * xreg) >> 4);
             for (int kk = mw; kk < 4; kk += p.nacc) {
@@ -369,21 +378,61 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // tokens g, g + 4, ... (units in rounds of 64); a warp shares each token, so
   // the counts are ballots
   if (LOPA && p.tout) {
-    // t kernel: P = V X^T of this slice of V's rows, stored as a bf16 pair
-    // (zero rows for the padding tokens, so the gate's MMA columns stay finite)
+    // t kernel: this block's partial of T = V X^T (its rows of V, its range of
+    // D) into the fp32 sums; the last block of the row tile stores the sums as
+    // bf16 pairs (zero rows for the padding tokens, so the gate's MMA columns
+    // stay finite) and clears them
     if (__syncthreads_and(stage_ok) && warp < 8) {
-      for (int r0 = 0; r0 < p.NU; r0 += 64) {
-        const int r = r0 + (tid & 63), u = u0 + r;
-        if (r < p.NU && u < p.H) {
-          for (int b = tid >> 6; b < NB; b += 4) {
-            const float tv = b < p.B ? s_acc[(size_t)r * ldc + NB + b] : 0.f;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
-            p.tout[(size_t)b * p.H + u] = __bfloat16_as_ushort(hi);
-            p.tout[(size_t)(NB + b) * p.H + u] = __bfloat16_as_ushort(lo);
+      // four consecutive rows of one token per 128-bit atomic (r and the slice starts are multiples of 8)
+      const int nq = p.NU / 4;
+      for (int i = tid; i < p.B * nq; i += 256) {
+        const int b = i / nq, r = 4 * (i - b * nq), u = u0 + r;
+        if (u < p.H) {
+          const float* sa = s_acc + (size_t)r * ldc + NB + b;
+          atomicAdd(reinterpret_cast<float4*>(p.tacc + (size_t)b * p.H + u),
+                    make_float4(sa[0], sa[ldc], sa[2 * ldc], sa[3 * ldc]));
+        }
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    volatile int* s_last = s_cnt;
+    if (tid == 0) *s_last = atomicAdd(p.tickets + tile, 1) == p.ksplit - 1;
+    __syncthreads();
+    if (*s_last) {
+      __threadfence();
+      // four consecutive rows per item, four items' loads in flight per thread (a loop that
+      // waited on each load in turn took one L2 round trip per item)
+      const int nq = p.NU / 4, items = NB * nq;
+      for (int i0 = tid; i0 < items; i0 += 4 * TC_GATE_THREADS) {
+        float4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * TC_GATE_THREADS, b = i / nq, u = u0 + 4 * (i - b * nq);
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (i < items && b < p.B && u < p.H) v[j] = __ldcg(reinterpret_cast<const float4*>(p.tacc + (size_t)b * p.H + u));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * TC_GATE_THREADS, b = i / nq, u = u0 + 4 * (i - b * nq);
+          if (i < items && u < p.H) {
+            if (b < p.B) __stcg(reinterpret_cast<float4*>(p.tacc + (size_t)b * p.H + u), make_float4(0.f, 0.f, 0.f, 0.f));
+            const float tv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint16_t hi[4], lo[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(tv[k]);
+              hi[k] = __bfloat16_as_ushort(h);
+              lo[k] = __bfloat16_as_ushort(__float2bfloat16_rn(tv[k] - __bfloat162float(h)));
+            }
+            *reinterpret_cast<uint2*>(p.tout + (size_t)b * p.H + u) =
+                make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+            *reinterpret_cast<uint2*>(p.tout + (size_t)(NB + b) * p.H + u) =
+                make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
           }
         }
       }
+      if (tid == 0) p.tickets[tile] = 0;
     }
   } else if (__syncthreads_and(stage_ok) && warp < 8) {
     for (int r0 = 0; r0 < p.NU; r0 += 64) {
@@ -641,9 +690,11 @@ TcPlan plan_ffn_tc(int D, int H, int r, int num_sms) {
   p.r = r;
   p.KCZ = (r + 63) / 64;
   p.num_sms = num_sms;
-  if (r > 0) {  // the t kernel: slices of V's rows
-    p.NUt = std::min(128, std::max(8, ((r + num_sms - 1) / num_sms + 7) / 8 * 8));
+  if (r > 0) {  // the t kernel: slices of up to 128 rows of V, each over ksplit_t ranges of D
+    p.NUt = std::min(128, (r + 7) / 8 * 8);
     p.ntiles_t = (r + p.NUt - 1) / p.NUt;
+    p.ksplit_t = std::max(1, std::min(p.KC, num_sms / p.ntiles_t));
+    if (p.ntiles_t > TC_TICKETS) return p;
   }
   p.ndt = (D + TC_DTILE - 1) / TC_DTILE;
   p.nch = (H + TC_UCH - 1) / TC_UCH;
@@ -699,7 +750,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   // gate-up arguments for slices of NU rows of a [Hg, .] matrix (the t kernel: V's r rows, no U chunks).
   // More slices than SMs: two blocks per SM (half the shared memory and TMEM each), so that the
   // slices run in one wave; not with NB = 128, whose accumulator copy needs 132 KB.
-  auto gate_args = [&](int NU, int Hg, bool with_u, uint16_t* tout, TcGateArgs& g, size_t& smem) {
+  auto gate_args = [&](int NU, int Hg, bool with_u, uint16_t* tout, int ksplit, TcGateArgs& g, size_t& smem) {
     const bool two = (Hg + NU - 1) / NU > plan.num_sms && NB <= 64;
     const size_t cap = two ? std::min(max_smem, (size_t)110 * 1024) : max_smem;
     const size_t budget = two ? std::min(plan.gate_smem_budget, (size_t)100 * 1024) : plan.gate_smem_budget;
@@ -720,6 +771,13 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     g.NCZ = (g.KCZ + g.C - 1) / g.C;
     g.NCG = g.NCZ + (plan.KC + g.C - 1) / g.C;
     g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, budget / stage_bytes(g.C)));
+    {  // a K-split block has few chunk groups: no more stages than it fills or the epilogue's copy needs
+      const int kc_blk = (plan.KC + ksplit - 1) / ksplit;
+      const int groups = g.NCZ + (kc_blk + g.C - 1) / g.C;
+      const size_t acc_copy = (size_t)128 * (2 * NB + 1) * 4;
+      const int need = (int)((acc_copy + stage_bytes(g.C) - 1) / stage_bytes(g.C));
+      g.NS = std::min(g.NS, std::max(2, std::max(groups, need)));
+    }
     while (g.NS > 2 && smem_bytes(g.C, g.NS) > cap) --g.NS;
     g.act = act;
     g.flags = flags;
@@ -727,6 +785,9 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     g.Hs = plan.Hs;
     g.x = static_cast<const uint16_t*>(x);
     g.tout = tout;
+    g.ksplit = ksplit;
+    g.tacc = buf.tacc;
+    g.tickets = buf.tickets_t;
     const int cols = !lopa && 2 * NU <= 128 ? NB : 2 * NB;  // one accumulator
     g.nacc = cols <= 128 ? 4 : 2;  // MMA warps = accumulators, nacc * cols <= 512
     if (two) g.nacc = std::min(g.nacc, 256 / cols);  // <= 256 columns per block
@@ -744,11 +805,13 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   if (lopa && !tpair_ready) {
     TcGateArgs gt;
     size_t smt = 0;
-    if (!gate_args(plan.NUt, plan.r, false, buf.tpair, gt, smt)) {
+    const int ksplit = std::max(1, std::min(plan.ksplit_t, plan.t_split_tokens / NB));
+    if (!gate_args(plan.NUt, plan.r, false, buf.tpair, ksplit, gt, smt)) {
       *cuda_err = cudaErrorInvalidConfiguration;
       return 0;
     }
-    e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t), gb, smt, s, maps.v, maps.v, mx, mx, gt);
+    e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t * gt.ksplit), gb, smt, s, maps.v, maps.v,
+                   mx, mx, gt);
     if (e) {
       *cuda_err = e;
       return 0;
@@ -756,7 +819,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   }
   TcGateArgs g;
   size_t smem1 = 0;
-  if (!gate_args(plan.NU, H, lopa, nullptr, g, smem1)) {
+  if (!gate_args(plan.NU, H, lopa, nullptr, 1, g, smem1)) {
     *cuda_err = cudaErrorInvalidConfiguration;
     return 0;
   }

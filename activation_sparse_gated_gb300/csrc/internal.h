@@ -84,7 +84,8 @@ struct TcPlan {
   bool ok = false;
   int NU = 0, MT = 0, ntiles = 0, KC = 0;
   int r = 0, KCZ = 0;  // low-rank gate: rank and its 64-wide K chunks (0: standard gate)
-  int NUt = 0, ntiles_t = 0;  // low-rank gate: rows of V per block of the t kernel, and its blocks
+  int NUt = 0, ntiles_t = 0, ksplit_t = 0;  // low-rank gate, t kernel: rows of V per slice, slices, K ranges
+  int t_split_tokens = 1024;  // t kernel: K ranges x padded tokens <= this (its partial sums grow with both)
   int num_sms = 0;
   int ndt = 0, nch = 0, nsplit = 0;
   int Hs = 0;  // row stride (elements) of the h buffer
@@ -105,6 +106,8 @@ struct TcBuffers {
   int* counts;     // [B_max] published live counts
   int* tickets;    // [TC_TICKETS] zero between calls
   uint16_t* tpair; // low-rank gate: [2 NB, r] bf16, t_hi rows then t_lo rows (the t kernel); else null
+  float* tacc;     // low-rank gate: [128, r] fp32 partial sums of t, zero between calls
+  int* tickets_t;  // low-rank gate: [TC_TICKETS] slices of the t kernel, zero between calls
 };
 constexpr int TC_TICKETS = 64;  // >= slices of 128 y values (D <= 8192)
 TcPlan plan_ffn_tc(int D, int H, int r, int num_sms);
