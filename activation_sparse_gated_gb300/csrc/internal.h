@@ -129,9 +129,9 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
                   cudaError_t* cuda_err, bool tpair_ready = false);
 // Low-rank batches of up to this many tokens take the CUDA-core t kernel
-// (measured: 33.5 against 36.0 us per call at B = 4 on the low-rank workload;
-// from B = 8 the tensor-core t kernel is faster).
-constexpr int TC_T_CUDA_CORE_MAX_B = 4;
+// (measured per call on the low-rank workload: 31.5 against 31.6 us at B = 2;
+// at B = 4 the split tensor-core t kernel is faster, 31.9 against 33.9 us).
+constexpr int TC_T_CUDA_CORE_MAX_B = 2;
 
 // Small batches (2..8 tokens, bf16, standard gate; ffn_tcu.cu): the gate on the
 // tensor cores, the union of the live sets gathered on the CUDA cores, fp32
