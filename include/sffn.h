@@ -86,6 +86,17 @@ enum {
  * Returns NULL on error (see sffn_last_error()).  Allocates device memory:
  * 3*H*D (+ r*D + H*r) elements of weights plus O(B_max * (D + r + H)) bytes of
  * accumulators.
+ * Kernel selection reads these environment variables once, here (tuning and
+ * measurement only; the defaults are the measured best, the results are the
+ * same up to fp32 summation order): SFFN_STREAM_BLOCKS_PER_SM (1..4, default
+ * 1), SFFN_TC_MIN_BATCH (smallest bf16 batch on the tensor cores, default 2),
+ * SFFN_TCU_MAX_BATCH (largest standard-gate batch taking the union-gather
+ * kernel, 0..8, default 2), SFFN_TC_T_CUDA_MAX_B (largest low-rank batch whose
+ * t runs on the CUDA cores, default 2), SFFN_TC_T_SPLIT_TOKENS (K ranges of
+ * the tensor-core t kernel times padded tokens, default 1024),
+ * SFFN_TC_GATE_KB / SFFN_TC_DOWN_KB (pipeline-stage bytes per block of the
+ * tensor-core kernels, default 200), SFFN_TC_GATE_CHUNKS (64-wide K chunks per
+ * gate-up stage, 1..4, default by batch).
  */
 sffn_t sffn_create(int D, int H, int r, int act, int dtype);
 
