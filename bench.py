@@ -656,6 +656,17 @@ def dense_us(ld, x, B, stream, steps, warmup):
     return best
 
 
+def set_sparsity(lw, s):
+    """Rewrite a layer's bias column (W1[:, D-1], or U[:, r-1] for the low-rank gate) with -Phi^{-1}(s),
+    rounded as the generator rounds it (float32, then the storage dtype), on whatever device it lives."""
+    import torch
+    from activation_sparse_gated_gb300 import synthetic as syn
+    W = lw.W1 if lw.r == 0 else lw.U
+    col = lw.D - 1 if lw.r == 0 else lw.r - 1
+    W[:, col] = torch.tensor(syn.shift_for_sparsity(s), dtype=torch.float32).to(W.dtype).to(W.device)
+    return lw
+
+
 def run_sweep(args):
     """Sparsity x batch sweep at D=4096: standard gate (H=14336) and low-rank gate (H'=19649, r=640),
     s in {0.5, 0.75, 0.9, 0.95}, B in {1, 8, 32, 128}, 1024 tokens per point, each point next to the
@@ -701,12 +712,8 @@ def run_sweep(args):
         handles = layers if gate == "standard" else layers * 4
         Hg = H if gate == "standard" else Hp
         for s in w["s"]:
-            shift = torch.tensor(syn.shift_for_sparsity(s), dtype=torch.float32).to(torch.bfloat16)
             for lw in layers:
-                if gate == "standard":
-                    lw.W1[:, D - 1] = shift.to(dev)
-                else:
-                    lw.U[:, r - 1] = shift.to(dev)
+                set_sparsity(lw, s)
             ffns = build_ffns(handles, dev)
             torch.cuda.synchronize()
             for B in w["B"]:
