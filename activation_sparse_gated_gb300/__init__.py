@@ -24,7 +24,7 @@ SFFN_F32, SFFN_BF16, SFFN_I8W = 0, 1, 2
 SFFN_ACT_RELU, SFFN_ACT_RSP, SFFN_ACT_SILU = 0, 1, 2
 SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
-SFFN_ERR_TIMEOUT, SFFN_ERR_STATE, SFFN_ERR_NOMEM = -5, -6, -7
+SFFN_ERR_TIMEOUT, SFFN_ERR_STATE, SFFN_ERR_NOMEM, SFFN_ERR_DEVICE = -5, -6, -7, -8
 SFFN_MAX_BATCH = 128
 SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT = 1, 2, 4
 

@@ -59,8 +59,6 @@ struct sffn_s {
   int last_B = 0;
   cudaEvent_t ev = nullptr;
   bool ev_valid = false;
-  int b1_grid = 0, b1_ns1 = 0, b1_ns2 = 0;
-  size_t b1_smem = 0;
   int stream_grid = 0;  // blocks of the streaming standard-gate kernel
   int stream_rows_cap = 0;
   StreamPlan stream_plan;
@@ -82,6 +80,8 @@ struct sffn_s {
   float* qs3 = nullptr;
   float* qs2 = nullptr;
   StreamPlan i8_plan;
+  bool b1_bf16 = true;    // bf16 single tokens: ffn_b1_bf16.cu (false: the fp32 streaming kernel's bf16 form)
+  StreamPlan bf16_plan;
 };
 
 namespace {
@@ -108,29 +108,6 @@ void release(sffn_s* h) {
   if (h->ev) cudaEventDestroy(h->ev);
 }
 
-int plan_b1(sffn_s* h) {
-  const bool lopa = h->r > 0;
-  const int gk = gate_k(h);
-  h->b1_grid = std::min(h->num_sms, h->H);
-  const int rows_max = (h->H + h->b1_grid - 1) / h->b1_grid;
-  const size_t grow = (size_t)gk * h->elt;
-  const int ns2 = 8;  // >= the number of gate warps (slot ownership rule of the kernel)
-  const size_t base = ffn_b1_smem_bytes(h->D, gk, h->elt, lopa, 0, ns2);
-  if (base + 128 + (size_t)B1_NWG * grow > h->max_smem)
-    return fail(SFFN_ERR_DTYPE, "D=%d, gate width %d do not fit the fused kernel's shared memory",
-                h->D, gk);
-  int ns1 = (int)((h->max_smem - base - 128) / grow);
-  ns1 = std::min(ns1, B1_NS1_MAX);
-  ns1 = std::min(ns1, (rows_max + B1_NWG - 1) / B1_NWG * B1_NWG);
-  ns1 = ns1 / B1_NWG * B1_NWG;  // each gate warp owns whole slots
-  if (ns1 < B1_NWG) ns1 = B1_NWG;
-  h->b1_ns1 = ns1;
-  h->b1_ns2 = ns2;
-  h->b1_smem = ffn_b1_smem_bytes(h->D, gk, h->elt, lopa, ns1, ns2);
-  if (h->b1_smem > h->max_smem) return fail(SFFN_ERR_DTYPE, "shared-memory plan exceeds the device limit");
-  return SFFN_OK;
-}
-
 int check_device(const sffn_s* h) {
   int dev = -1;
   SFFN_CUDA(cudaGetDevice(&dev));
@@ -153,6 +130,9 @@ int sync_and_check(sffn_s* h) {
     SFFN_CUDA(cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS));
     SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * h->D));
     if (h->tickets) SFFN_CUDA(cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS));
+    if (err & DEV_ERR_CHECK)
+      return fail(SFFN_ERR_DEVICE, "a device-side bounds or alignment check failed (error word 0x%x); outputs "
+                  "of the affected forward are invalid", err);
     return fail(SFFN_ERR_TIMEOUT, "a device-side wait ran out of time (error word 0x%x); outputs of "
                 "the affected forward are invalid", err);
   }
@@ -182,6 +162,7 @@ const char* sffn_strerror(int code) {
     case SFFN_ERR_TIMEOUT: return "device-side wait timed out";
     case SFFN_ERR_STATE: return "call out of order";
     case SFFN_ERR_NOMEM: return "device memory allocation failed";
+    case SFFN_ERR_DEVICE: return "device-side bounds or alignment check failed";
     default: return "unknown status";
   }
 }
@@ -266,21 +247,17 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     return bail(SFFN_ERR_CUDA, "cudaMemset", e);
   if ((e = cudaEventCreateWithFlags(&h->ev, cudaEventDisableTiming)))
     return bail(SFFN_ERR_CUDA, "cudaEventCreate", e);
-  if (plan_b1(h) != SFFN_OK) {
-    char keep[sizeof g_msg];
-    std::memcpy(keep, g_msg, sizeof keep);
-    release(h);
-    delete h;
-    std::memcpy(g_msg, keep, sizeof keep);
-    return nullptr;
-  }
-  if ((e = ffn_b1_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
   {
     // blocks per SM of the streaming kernel (1 leaves room for the next call's blocks)
     int mult = 1;
     if (const char* env = std::getenv("SFFN_STREAM_BLOCKS_PER_SM")) mult = std::max(1, std::min(4, std::atoi(env)));
     h->stream_grid = std::min(h->num_sms * mult, H);
     h->stream_rows_cap = (H + h->stream_grid - 1) / h->stream_grid;
+    if (const char* env = std::getenv("SFFN_B1_KERNEL")) h->b1_bf16 = std::strcmp(env, "stream") != 0;
+    if (dtype == SFFN_BF16) {
+      h->bf16_plan = plan_ffn_b1_bf16(D, gate_k(h), r > 0, (H + std::min(h->num_sms, H) - 1) / std::min(h->num_sms, H));
+      if ((e = ffn_b1_bf16_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+    }
     h->stream_plan = plan_ffn_b1_stream(D, gate_k(h), h->elt, r > 0, h->stream_rows_cap);
     if (h->stream_plan.smem > h->max_smem) {
       fail(SFFN_ERR_DTYPE, "shared-memory plan of the streaming kernel exceeds the device limit");
@@ -505,7 +482,6 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       p.rows_cap = h->stream_rows_cap;
       p.pref_rows = h->i8_plan.pref_rows;
       p.gather_rows = h->i8_plan.gather_rows;
-      p.timeout_ns = kTimeoutNs;
       p.flags = h->flags;
       p.thr = h->thr;
       p.s1 = h->qs1;
@@ -533,18 +509,22 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.D = h->D;
     p.H = h->H;
     p.gate_k = gate_k(h);
-    p.ns1 = h->b1_ns1;
-    p.ns2 = h->b1_ns2;
     p.act = h->act;
     p.count_slot = b;
     p.rows_cap = h->stream_rows_cap;
-    p.timeout_ns = kTimeoutNs;
     p.flags = h->flags;
     p.thr = h->thr;
     if (nb == 1) {
-      p.pref_rows = h->stream_plan.pref_rows;
-      p.gather_rows = h->stream_plan.gather_rows;
-      SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, lopa, h->stream_grid, h->stream_plan.smem, s));
+      if (h->dtype == SFFN_BF16 && h->b1_bf16) {
+        const int grid = std::min(h->num_sms, h->H);
+        p.rows_cap = (h->H + grid - 1) / grid;
+        p.pref_rows = h->bf16_plan.pref_rows;
+        SFFN_CUDA(launch_ffn_b1_bf16(p, lopa, grid, h->bf16_plan.smem, s));
+      } else {
+        p.pref_rows = h->stream_plan.pref_rows;
+        p.gather_rows = h->stream_plan.gather_rows;
+        SFFN_CUDA(launch_ffn_b1_stream(p, h->dtype, lopa, h->stream_grid, h->stream_plan.smem, s));
+      }
     } else {
       p.pref_rows = h->batch_plan.pref_rows;
       p.gather_rows = h->batch_plan.gather_rows;

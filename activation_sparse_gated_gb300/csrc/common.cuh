@@ -11,6 +11,7 @@ namespace sffn {
 
 // device error word bits (the handle's ctrl[CTRL_ERR])
 constexpr int DEV_ERR_TIMEOUT = 1;
+constexpr int DEV_ERR_CHECK = 2;  // a device-side bounds or alignment check failed (the access was skipped)
 
 // ctrl[] layout: one small int array per handle
 constexpr int CTRL_TICKET = 0;   // blocks finished in the current forward
@@ -93,6 +94,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// The same by shared-window addresses (destination and mbarrier as 32-bit shared addresses).
+__device__ __forceinline__ void bulk_g2s_a(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst), "l"(src),
+      "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_a(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return v;
+}
+
 // Same, with an L2 eviction-priority policy (createpolicy).
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
                                               uint64_t* bar, uint64_t policy) {
@@ -107,6 +124,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Request `bytes` (a multiple of 16) starting at a 16-byte aligned address into
+// L2, one bulk-copy-engine operation.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding kernel in the stream

@@ -22,33 +22,17 @@ struct B1Params {
   int* counts;            // [1] live count of this call
   uint8_t* mask;          // [H] live flags of this call (nullptr: not recorded)
   int D, H, gate_k;       // gate_k = D (standard) or r (low-rank)
-  int ns1, ns2;           // gate-row ring slots, gather ring slots
   int act;
   int count_slot;         // index of this token's live-count accumulator
   int rows_cap;           // streaming kernel: max units per block (live-list capacity)
   int pref_rows;          // streaming kernel: gate rows per block prefetched into shared memory
   int gather_rows;        // streaming kernel: W3 rows per gather batch (shared area / row)
-  unsigned long long timeout_ns;
   int flags = 0;          // FLAG_TILED_G | FLAG_RMSNORM (low-rank gate) | FLAG_DOUBLE_ACT
   float thr = 0.f;        // live iff |A(z)| > thr
   const float* s1 = nullptr;  // int8 weights: per-unit scales of the W1 and W3 codes,
   const float* s3 = nullptr;  // per-output scales of the W2 codes
   const float* s2 = nullptr;
 };
-
-constexpr int B1_NWG = 8;                               // gate warps
-constexpr int B1_NGA = 4;                               // gather warps
-constexpr int B1_THREADS = (1 + B1_NWG + B1_NGA) * 32;  // + one producer warp
-constexpr int B1_NS1_MAX = 128;
-constexpr int B1_NS2_MAX = 16;
-constexpr int B1_MAXC = 4;  // 16-byte chunks of a D-row per gather thread (D*elt <= 8 KB)
-
-// Shared-memory bytes of the fused kernel for a given ring configuration.
-size_t ffn_b1_smem_bytes(int D, int gate_k, int elt_bytes, bool lopa, int ns1, int ns2);
-// Raise the kernels' dynamic shared-memory limit (once per device).
-cudaError_t ffn_b1_prepare(size_t max_smem);
-cudaError_t launch_ffn_b1(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
-                          cudaStream_t s);
 
 // Streaming form of the fused forward (16 warps, no spin-waits); grid =
 // blocks, each owning a slice of units.  The plan fixes the shared-memory
@@ -62,6 +46,12 @@ cudaError_t ffn_b1_stream_prepare(size_t max_smem);
 int ffn_b1_stream_threads();
 cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int grid, size_t smem,
                                  cudaStream_t s);
+
+// bf16 form of the single-token forward (ffn_b1_bf16.cu): gate rows through
+// two refilled shared halves, packed fp32x2 dot products, register gathers.
+StreamPlan plan_ffn_b1_bf16(int D, int gate_k, bool lopa, int rows_cap);
+cudaError_t ffn_b1_bf16_prepare(size_t max_smem);
+cudaError_t launch_ffn_b1_bf16(const B1Params& p, bool lopa, int grid, size_t smem, cudaStream_t s);
 
 // Small-batch form (2..8 tokens per launch, CUDA cores): one pass over the
 // gate slice serves every token; gathers follow the union of live sets.

@@ -5,10 +5,15 @@
 // allocation would synchronise the device or break a latency budget, or an
 // embedding host that only lends out buffers it owns.  sffn_forward_noalloc
 // serves them.  The caller passes the weights, x and y (and optionally a
-// counts buffer); the only scratch the fused kernel needs -- the fp32 partial
-// sum of y, the block ticket, the error word and the live-count accumulators
-// -- lives in the fixed static device array below, which the library image
-// brings with it (every GPU that loads the library holds it until exit).
+// counts buffer); the only scratch the forward needs -- the fp32 accumulator
+// copies of y, the control words and the live-count accumulators -- lives in
+// the fixed static device array below, which the library image brings with it
+// (every GPU that loads the library holds it until exit).
+//
+// Each token runs the handle path's single-token streaming kernel followed by
+// the finalize kernel (the same two launches sffn_forward makes for B = 1).
+// Neither kernel waits on anything on the device, so no device-side timeout
+// can leave y half-written.
 #include <cstdio>
 #include <mutex>
 
@@ -20,14 +25,15 @@ using namespace sffn;
 
 namespace {
 
-// Scratch layout (bytes): [0, 16384) fp32 accumulator for D <= 4096;
-// [16384, 16384 + 4*CTRL_INTS) control words; then SFFN_MAX_BATCH ints of
-// live counts used when the caller passes no counts buffer.
+// Scratch layout (bytes): YACC_COPIES fp32 accumulator copies of D <= 4096
+// values; the control words (256-byte aligned); SFFN_MAX_BATCH ints of live
+// counts used when the caller passes no counts buffer.
 constexpr int kMaxD = SFFN_MAX_D_BF16;
 constexpr size_t kYaccOff = 0;
-constexpr size_t kCtrlOff = sizeof(float) * kMaxD;
+constexpr size_t kCtrlOff = sizeof(float) * YACC_COPIES * kMaxD;
 constexpr size_t kCountsOff = kCtrlOff + ((sizeof(int) * CTRL_INTS + 255) / 256) * 256;
-constexpr size_t kScratchBytes = kCountsOff + sizeof(int) * SFFN_MAX_BATCH;  // 17,664 bytes
+constexpr size_t kScratchBytes = kCountsOff + sizeof(int) * SFFN_MAX_BATCH;  // 66,816 bytes
+static_assert(kScratchBytes == 66816, "the header states this size");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -54,7 +60,8 @@ int fail(int code, const char* msg, cudaError_t e = cudaSuccess) {
 }
 
 // Once per device, with that device current: look up the scratch array's
-// device address and raise the fused kernel's shared-memory limit.
+// device address (in host code the array's name is only a host-side stand-in)
+// and raise the streaming kernel's shared-memory limit.
 int setup(int dev, DeviceSetup** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceSetup& d = g_dev[dev];
@@ -66,7 +73,7 @@ int setup(int dev, DeviceSetup** out) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return fail(SFFN_ERR_CUDA, "cudaDeviceGetAttribute", e);
-    if ((e = ffn_b1_prepare((size_t)optin)) != cudaSuccess)
+    if ((e = ffn_b1_stream_prepare((size_t)optin)) != cudaSuccess)
       return fail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     d.scratch = static_cast<unsigned char*>(ptr);
     d.num_sms = sms;
@@ -91,9 +98,11 @@ extern "C" int sffn_forward_noalloc(const void* W1, const void* W3, const void* 
   if (H < 1) return fail(SFFN_ERR_ARG, "H must be >= 1");
   if (B < 1 || B > SFFN_MAX_BATCH) return fail(SFFN_ERR_ARG, "B must be in [1, 128]");
   if (!W1 || !W3 || !W2t || !x || !y) return fail(SFFN_ERR_ARG, "null pointer");
-  const uintptr_t a = (uintptr_t)W1 | (uintptr_t)W3 | (uintptr_t)W2t | (uintptr_t)x | (uintptr_t)y |
-                      (uintptr_t)counts;
-  if (a & 15) return fail(SFFN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  // weights, x and y are read and written with 16-byte vector accesses; the
+  // kernels store one int per token into counts
+  const uintptr_t a = (uintptr_t)W1 | (uintptr_t)W3 | (uintptr_t)W2t | (uintptr_t)x | (uintptr_t)y;
+  if (a & 15) return fail(SFFN_ERR_ALIGN, "W1, W3, W2t, x and y must be 16-byte aligned");
+  if ((uintptr_t)counts & 3) return fail(SFFN_ERR_ALIGN, "counts must be 4-byte aligned");
   const int elt = dtype == SFFN_BF16 ? 2 : 4;
   const size_t xbytes = (size_t)B * D * elt;
   const uintptr_t px = (uintptr_t)x, py = (uintptr_t)y;
@@ -106,29 +115,20 @@ extern "C" int sffn_forward_noalloc(const void* W1, const void* W3, const void* 
   DeviceSetup* d = nullptr;
   if (int rc = setup(dev, &d)) return rc;
 
-  // the fused kernel's launch plan (same rules as a handle's plan)
+  // the streaming kernel's launch plan (the rules of a handle's plan)
   const int grid = d->num_sms < H ? d->num_sms : H;
-  const int rows_max = (H + grid - 1) / grid;
-  const size_t grow = (size_t)D * elt;
-  const int ns2 = 8;
-  const size_t base = ffn_b1_smem_bytes(D, D, elt, false, 0, ns2);
-  if (base + 128 + (size_t)B1_NWG * grow > d->max_smem)
-    return fail(SFFN_ERR_DTYPE, "D does not fit the fused kernel's shared memory");
-  int ns1 = (int)((d->max_smem - base - 128) / grow);
-  ns1 = ns1 < B1_NS1_MAX ? ns1 : B1_NS1_MAX;
-  const int want = (rows_max + B1_NWG - 1) / B1_NWG * B1_NWG;
-  ns1 = ns1 < want ? ns1 : want;
-  ns1 = ns1 / B1_NWG * B1_NWG;
-  if (ns1 < B1_NWG) ns1 = B1_NWG;
-  const size_t smem = ffn_b1_smem_bytes(D, D, elt, false, ns1, ns2);
+  const int rows_cap = (H + grid - 1) / grid;
+  const StreamPlan plan = plan_ffn_b1_stream(D, D, elt, false, rows_cap);
+  if (plan.smem > d->max_smem) return fail(SFFN_ERR_DTYPE, "D does not fit the streaming kernel's shared memory");
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* yacc = reinterpret_cast<float*>(d->scratch + kYaccOff);
   int* ctrl = reinterpret_cast<int*>(d->scratch + kCtrlOff);
   int* own_counts = reinterpret_cast<int*>(d->scratch + kCountsOff);
-  // The scratch keeps whatever the previous call left; clear what must start
-  // at zero (accumulator, ticket, error word, count accumulators).
-  if ((e = cudaMemsetAsync(yacc, 0, sizeof(float) * D, s)) != cudaSuccess ||
+  // The scratch keeps whatever the previous call left (the finalize kernel
+  // clears the accumulators and count words it used); clear what must start
+  // at zero anyway, so that a call never depends on an earlier one.
+  if ((e = cudaMemsetAsync(yacc, 0, sizeof(float) * YACC_COPIES * D, s)) != cudaSuccess ||
       (e = cudaMemsetAsync(ctrl, 0, sizeof(int) * CTRL_INTS, s)) != cudaSuccess)
     return fail(SFFN_ERR_CUDA, "cudaMemsetAsync", e);
   const size_t row = (size_t)D * elt;
@@ -147,15 +147,14 @@ extern "C" int sffn_forward_noalloc(const void* W1, const void* W3, const void* 
     p.D = D;
     p.H = H;
     p.gate_k = D;
-    p.ns1 = ns1;
-    p.ns2 = ns2;
     p.act = act;
     p.count_slot = b;
-    p.rows_cap = 0;
-    p.pref_rows = 0;
-    p.gather_rows = 1;
-    p.timeout_ns = 250000000ull;
-    if ((e = launch_ffn_b1(p, dtype, false, grid, smem, s)) != cudaSuccess)
+    p.rows_cap = rows_cap;
+    p.pref_rows = plan.pref_rows;
+    p.gather_rows = plan.gather_rows;
+    if ((e = launch_ffn_b1_stream(p, dtype, false, grid, plan.smem, s)) != cudaSuccess)
+      return fail(SFFN_ERR_CUDA, "kernel launch", e);
+    if ((e = launch_finalize(yacc, p.y, ctrl, p.counts, b, D, 1, dtype, s)) != cudaSuccess)
       return fail(SFFN_ERR_CUDA, "kernel launch", e);
   }
   return SFFN_OK;

@@ -763,6 +763,39 @@ def run_sweep(args):
                       "peak_gbs": peak}), flush=True)
 
 
+PROFILE_CASES = {
+    "std": ("std-bf16-D2560-H7168-B1", None),
+    "lopa": ("lopa-bf16-D2560-H9787-r400-B1", None),
+    "std4096": ("sweep-bf16-D4096-H14336", "standard"),
+    "lopa4096": ("sweep-bf16-D4096-H14336", "lopa"),
+    "tiny": ("tiny-f32-D384-H1024", None),
+}
+
+
+def run_profile_case(args):
+    """A short forward loop for profiler captures: ONE full-size layer of the named
+    workload, `--calls` forwards of `--batch` tokens, each followed by a
+    synchronisation.  Device memory stays near one layer (110-130 MB at D=2560,
+    350 MB at D=4096); the profiler flushes caches between replays, so its DRAM
+    figures are cold-cache figures.  Prints one line, times nothing."""
+    import torch
+    from activation_sparse_gated_gb300 import synthetic as syn
+    import activation_sparse_gated_gb300 as sffn
+    name, gate = PROFILE_CASES[args.profile_case]
+    lw = syn.workload_layers(name, sets=1, gate=gate)[0]
+    dtype = {"int8": "int8", "bf16": "bf16", "f32": "f32"}.get(args.dtype or "", lw.dtype)
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", dtype)
+    w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
+    ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
+    x = syn.workload_tokens(name, args.calls * args.batch).cuda()
+    for c in range(args.calls):
+        ffn(x[c * args.batch:(c + 1) * args.batch])
+        ffn.synchronize()
+    torch.cuda.synchronize()
+    print(f"profile case {args.profile_case}: {args.calls} calls of {args.batch} tokens, live units of the "
+          f"last call: {ffn.active_counts(args.batch)}", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -774,6 +807,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
     ap.add_argument("--sweep", action="store_true",
                     help="the D=4096 sparsity x batch sweep (both gates, one JSON line per point) instead of the step")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="run a short forward loop on one layer of this workload for a profiler capture (no timing)")
+    ap.add_argument("--calls", type=int, default=8, help="--profile-case: forwards to run")
+    ap.add_argument("--batch", type=int, default=1, help="--profile-case: tokens per forward")
+    ap.add_argument("--dtype", choices=["bf16", "f32", "int8"], default=None,
+                    help="--profile-case: handle dtype (default: the workload's; int8 quantises on the device)")
     ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
                     help="(internal) time the oracle on this process's OpenMP threads for SECONDS, print JSON")
     args = ap.parse_args()
@@ -784,7 +823,9 @@ def main():
                                    args.oracle_one_thread, 64)
         print(json.dumps({"tokens": n, "seconds": dt, "cores": cores}), flush=True)
         return
-    if args.sweep:
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)

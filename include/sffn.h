@@ -64,7 +64,10 @@ enum {
   SFFN_ERR_TIMEOUT = -5,  /* a device-side wait ran out of time; the kernel
                              returned early and its outputs are invalid      */
   SFFN_ERR_STATE = -6,    /* call out of order (e.g. forward before weights) */
-  SFFN_ERR_NOMEM = -7     /* device allocation failed                        */
+  SFFN_ERR_NOMEM = -7,    /* device allocation failed                        */
+  SFFN_ERR_DEVICE = -8    /* a device-side bounds or alignment check failed:
+                             the checked access was skipped, outputs of the
+                             affected forward are invalid                     */
 };
 
 /* limits of this build */
@@ -235,17 +238,24 @@ int sffn_debug_timeout_probe(sffn_t h, int limit_us, void* stream);
  *   W2t      W2 transposed, [H, D] row-major (row i = column i of W2), device
  *   x, y     [B, D] device pointers, must not overlap; y fully overwritten
  *   counts   optional device int[B] receiving |S_b| per token, or NULL
- *   D, H, B, act, dtype as for sffn_create / sffn_forward (standard gate only)
- * All pointers 16-byte aligned.  The kernels' scratch (an fp32 accumulator of
- * D floats, the block ticket, an error word, count accumulators) is one static
- * device array of 17,664 bytes inside the library, so D is limited to 4096
- * (bf16) / 2048 (f32); larger D is rejected with SFFN_ERR_ARG and a message.
+ *   D, H, B, act, dtype as for sffn_create / sffn_forward (standard gate,
+ *            ReLU or R-S+ only)
+ * W1, W3, W2t, x and y must be 16-byte aligned, counts 4-byte aligned
+ * (SFFN_ERR_ALIGN otherwise).  The scratch (four fp32 accumulator copies of D
+ * floats, control words, count accumulators) is one static device array of
+ * 66,816 bytes inside the library, so D is limited to 4096 (bf16) / 2048
+ * (f32); larger D is rejected with SFFN_ERR_ARG and a message.
+ * Each token is one pass of the single-token streaming kernel plus the
+ * finalize kernel, so the cost grows linearly with B (a full read of W1 per
+ * token): the entry point is meant for B = 1, batches belong on a handle.
+ * The kernels wait on nothing on the device, so there is no device-side
+ * timeout to report.
  * The first call on a device looks up that array's address and sets kernel
  * attributes for the device, so make it before any stream capture.  Every
  * call clears the scratch it needs on `stream` and then launches; calls that
  * overlap on the GPU (different streams, or several threads) share the one
- * array and race, so serialise them.  Device-side timeouts are not reported
- * by this entry point.  Returns SFFN_OK once the work is enqueued.
+ * array and race, so serialise them.  Returns SFFN_OK once the work is
+ * enqueued.
  */
 int sffn_forward_noalloc(const void* W1, const void* W3, const void* W2t, const void* x, void* y,
                          int* counts, int D, int H, int B, int act, int dtype, void* stream);

@@ -41,7 +41,7 @@ def test_constants_match_header():
     text = open(HEADER).read()
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
-                 "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
+                 "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_ERR_DEVICE", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
                  "SFFN_DOUBLE_ACT", "SFFN_ACT_SILU", "SFFN_I8W"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
@@ -52,6 +52,7 @@ def test_host_only_calls(lib):
     assert sffn.sffn_version() == 100
     assert sffn.sffn_strerror(0) == "success"
     assert "timed out" in sffn.sffn_strerror(sffn.SFFN_ERR_TIMEOUT)
+    assert "check failed" in sffn.sffn_strerror(sffn.SFFN_ERR_DEVICE)
     assert sffn.sffn_strerror(12345) == "unknown status"
 
 

@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
 BAND = 1e-2
+K_ELEM = 1.0  # element-wise bar: max |y - y*| <= K_ELEM * TOL * rms(y*) (derivation in test_gpu_parity.py)
 ACTS = {"relu": oracle.RELU, "rsp": oracle.RSP, "silu": oracle.SILU}
 
 
@@ -63,6 +64,24 @@ def run(ffn, x, B=1):
     return np.concatenate(ys), np.array(counts), np.concatenate(masks)
 
 
+def act_val(act, z):
+    if act == "silu":
+        return z / (1.0 + np.exp(-z))
+    return np.maximum(z, 0.0) if act == "relu" else np.where(z > 0, z / (1.0 + np.exp(-z)), 0.0)
+
+
+def flip_adjusted(yref, z, gpu_live, ref_live, W3, W2, xb, act, flags):
+    """y* moved to the GPU's live set (units inside the decision band may go either
+    way; each flip moves a few elements of y by its whole term).  W3, W2 are the
+    dequantised weights."""
+    flips = np.nonzero(gpu_live != ref_live)[0]
+    if flips.size == 0:
+        return yref
+    u = W3[flips] @ xb
+    h = act_val(act, z[flips]) * (act_val(act, u) if flags & sffn.SFFN_DOUBLE_ACT else u)
+    return yref + W2[:, flips] @ (np.where(gpu_live[flips], 1.0, -1.0) * h)
+
+
 def act_abs(act, z):
     if act == "silu":
         return np.abs(z / (1.0 + np.exp(-z)))
@@ -75,14 +94,22 @@ def check(lw, x, y, counts, masks, act="relu", flags=0, thr=0.0, codes=None):
     yref, z, n = oracle.ffn_dense_q8(lw.D, lw.H, ACTS[act], flags, q1, s1, q3, s3, q2, s2,
                                      syn.oracle_view(x), thr=thr)
     A = act_abs(act, z)
+    W3 = q3.astype(np.float64) * np.asarray(s3, np.float64)[:, None]
+    W2 = q2.astype(np.float64) * np.asarray(s2, np.float64)[:, None]
+    xv = x.double().numpy()
     for b in range(x.shape[0]):
         den = np.linalg.norm(yref[b])
+        live = A[b] > thr
         if den == 0:
             assert (y[b] == 0).all(), f"token {b}: no live unit but y != 0"
         else:
             err = np.linalg.norm(y[b] - yref[b]) / den
             assert err <= TOL, f"token {b}: relative L2 {err:.3e} > {TOL}"
-        live = A[b] > thr
+            # element by element too: max |y - y*| <= K_ELEM * TOL * rms(y*), as in the bf16 parity tests
+            ya = flip_adjusted(yref[b], z[b], masks[b].astype(bool), live, W3, W2, xv[b], act, flags)
+            rms = np.sqrt(np.mean(yref[b] ** 2))
+            worst = np.abs(y[b] - ya).max()
+            assert worst <= K_ELEM * TOL * rms, f"token {b}: element error {worst:.3e} > {K_ELEM * TOL * rms:.3e}"
         sure = (np.abs(z[b]) > BAND) if thr == 0 else (np.abs(A[b] - thr) > 1e-3)
         bad = np.nonzero(sure & (masks[b].astype(bool) != live))[0]
         assert bad.size == 0, f"token {b}: live set differs at units {bad[:10]}"
