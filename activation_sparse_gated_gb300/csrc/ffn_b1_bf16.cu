@@ -17,11 +17,13 @@
 // than ~25 instructions per 16 bytes falls behind the memory).
 //   * Gate rows.  The block's slice of W1 (or U) is contiguous.  Two halves of
 //     a shared area are filled by one bulk copy each (the TMA engine's
-//     non-tensor form, completion on an mbarrier) before the wait, and every
-//     warp holds the first pieces of one more row in registers.  After the
+//     non-tensor form, completion on an mbarrier) before the wait.  After the
 //     wait the halves are consumed in turn, and each is refilled with the next
 //     rows of the slice as soon as it has been read, so the rest of the slice
-//     is requested within a few hundred nanoseconds of the wait.
+//     is requested within a few hundred nanoseconds of the wait.  Nothing else
+//     is held across the wait: at 384 threads x 80 registers (two blocks per
+//     SM) every register given to prefetched rows is taken from the dot
+//     products (measured 1 us per call slower with 12 rows held that way).
 //   * Dot products.  Two rows per warp share every load of x; each lane widens
 //     bf16 pairs with one shift or mask per value and accumulates with packed
 //     fp32x2 FMAs; shared memory is read through explicit shared-window loads.
@@ -48,19 +50,11 @@ namespace {
 
 constexpr int NW = 12;          // warps per block (two blocks and a finalize block fit an SM)
 constexpr int NT = NW * 32;     // threads per block
-constexpr int PIECE = 5;        // 16-byte chunks per lane per register piece
 constexpr int MG = 5;           // units per gather round (registers: 2 chunks per unit and thread-chunk)
 constexpr unsigned long long kCopyLimitNs = 250000000ull;
 
 __host__ __device__ constexpr size_t al16(size_t v) { return (v + 15) & ~size_t(15); }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 __device__ __forceinline__ uint4 ld_l2(const uint4* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
@@ -175,31 +169,6 @@ __device__ __forceinline__ void dot2_t(uint32_t ra, uint32_t rb, uint32_t ts, in
   zb = warp_sum(hsum(b));
 }
 
-// Load piece `pc` of a row (chunks pc*32*PIECE + lane + 32k) into registers.
-__device__ __forceinline__ void load_piece(uint4 (&w)[PIECE], const uint4* row, int pc, int lane, int nch) {
-#pragma unroll
-  for (int k = 0; k < PIECE; ++k) {
-    const int c = pc * 32 * PIECE + lane + 32 * k;
-    w[k] = (c < nch) ? ld_stream(row + c) : make_uint4(0, 0, 0, 0);
-  }
-}
-template <bool LOPA>
-__device__ __forceinline__ void dot_piece(float2& acc, const uint4 (&w)[PIECE], uint32_t vs, int pc, int lane,
-                                          int nch) {
-#pragma unroll
-  for (int k = 0; k < PIECE; ++k) {
-    const int c = pc * 32 * PIECE + lane + 32 * k;
-    if (c < nch) {
-      float2 f[4];
-      if constexpr (LOPA)
-        tpairs(vs, c, f);
-      else
-        unpack4(lda16(vs + (uint32_t)c * 16u), f);
-      fma8(acc, w[k], f);
-    }
-  }
-}
-
 // One bulk copy of `bytes` of consecutive gate rows into shared memory at
 // `dst`, completing on the mbarrier at `bar` (both shared-window addresses).
 // The copy is checked first -- 16-byte alignment of both ends and of the size,
@@ -256,7 +225,6 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
   const int D = p.D;
   const int nch = D / 8;          // 16-byte chunks of x, W3 and W2^T rows
   const int nchg = p.gate_k / 8;  // ... of a gate row (W1 or U)
-  const int npg = (nchg + 32 * PIECE - 1) / (32 * PIECE);
   const int row0 = (int)(((long long)blockIdx.x * p.H) / gridDim.x);
   const int row1 = (int)(((long long)(blockIdx.x + 1) * p.H) / gridDim.x);
   const int cap = p.rows_cap;  // >= units of this block
@@ -283,12 +251,11 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
   int* err = p.ctrl + CTRL_ERR;
 
   // ---- gate rows: [0, RA) half A, [RA, R) half B (bulk copies before the wait),
-  // [R, R + nreg) one per warp in registers, the rest refilled into A and B.
-  // Shared addresses below are 32-bit offsets in the shared window.
+  // the rest refilled into A and B after it.  Shared addresses below are 32-bit
+  // offsets in the shared window.
   const int nrows = row1 - row0;
   const int R = min(p.pref_rows, nrows);
   const int RA = (R + 1) / 2, RB = R - RA;
-  const int nreg = max(0, min(NW, nrows - R));
   const uint32_t rowb = (uint32_t)nchg * 16u;  // bytes of a gate row
   const uint32_t s_lo = smem_u32(smem), s_hi = s_lo + dynamic_smem_bytes();
   const uint32_t hA_a = smem_u32(srows), hB_a = hA_a + (uint32_t)RA * rowb;
@@ -307,11 +274,6 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
     if (RB > 0) fill_rows(hB_a, barB, G + (size_t)(row0 + RA) * nchg, (uint32_t)RB * rowb, s_lo, s_hi, misc + 1, err);
     prefetch_l2_bulk(p.x, (uint32_t)nch * 16u);
   }
-  const int n_seq = warp < nreg ? npg : 0;
-  const uint4* my_row = G + (size_t)(row0 + R + warp) * nchg;
-  uint4 wa[PIECE], wb[PIECE];
-  if (n_seq > 0) load_piece(wa, my_row, 0, lane, nchg);
-  if (n_seq > 1) load_piece(wb, my_row, 1, lane, nchg);
 
   pdl_wait();  // x, t, the outputs and the accumulators follow stream order
   for (int i = tid; i < nch; i += NT) xs[i] = __ldcg(static_cast<const uint4*>(p.x) + i);
@@ -372,27 +334,13 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
 
   // Each half holds one batch of consecutive slice rows at a time: it is
   // waited on, read, and (after a barrier) refilled with the next rows of the
-  // slice still to copy, which start at `next`.  The order is: half A, the
-  // register rows, half B, then the refilled halves in turn.  All of this
-  // state is uniform over the block.
-  int next = R + nreg;
+  // slice still to copy, which start at `next`.  The halves alternate, A
+  // first.  All of this state is uniform over the block.
+  int next = R;
   uint32_t phA = 0, phB = 0;
   int firstA = 0, nA = RA, firstB = RA, nB = RB;
   for (int step = 0;; ++step) {
-    if (step == 1) {  // the register rows
-      float2 acc = make_float2(0.f, 0.f);
-      for (int pc = 0; pc < n_seq; pc += 2) {
-        dot_piece<LOPA>(acc, wa, vs_a, pc, lane, nchg);
-        if (pc + 2 < n_seq) load_piece(wa, my_row, pc + 2, lane, nchg);
-        if (pc + 1 < n_seq) {
-          dot_piece<LOPA>(acc, wb, vs_a, pc + 1, lane, nchg);
-          if (pc + 3 < n_seq) load_piece(wb, my_row, pc + 3, lane, nchg);
-        }
-      }
-      if (n_seq > 0) decide(row0 + R + warp, warp_sum(hsum(acc)));
-      continue;
-    }
-    const bool b = step == 2 || (step > 2 && ((step - 3) & 1));  // this step's half: A (false) or B
+    const bool b = step & 1;  // this step's half: A (false) or B
     const int n = b ? nB : nA;
     if (n > 0) {
       if (!bar_wait_a(b ? barB : barA, b ? phB : phA, misc + 1, err)) misc[1] = 1;  // timed out: rows as they are
@@ -418,7 +366,7 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
         next += m;
       }
     }
-    if (step >= 2 && nA == 0 && nB == 0) break;
+    if (step >= 1 && nA == 0 && nB == 0) break;
   }
   __syncthreads();
   const int n_live = misc[0];
