@@ -26,7 +26,7 @@ SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
 SFFN_ERR_TIMEOUT, SFFN_ERR_STATE, SFFN_ERR_NOMEM, SFFN_ERR_DEVICE = -5, -6, -7, -8
 SFFN_MAX_BATCH = 128
-SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT = 1, 2, 4
+SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT, SFFN_DETERMINISTIC = 1, 2, 4, 8
 
 #: every symbol include/sffn.h declares
 EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_live_threshold", "sffn_set_weights", "sffn_forward", "sffn_active_counts",

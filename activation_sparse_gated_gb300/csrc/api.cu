@@ -73,6 +73,7 @@ struct sffn_s {
                            // from B = 3 its per-block partial sums of all B x D outputs cost more)
   uint16_t* hbuf = nullptr;
   int* tickets = nullptr;
+  float* ypart = nullptr;     // deterministic option: [blocks, D] partial y rows of the single-token kernel
   uint16_t* tpair = nullptr;  // low-rank gate: [256, r] bf16 t pairs of a tensor-core batch
   float* tacc = nullptr;      // low-rank gate: [128, r] fp32 partial sums of the t kernel
   // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
@@ -102,6 +103,7 @@ void release(sffn_s* h) {
   cudaFree(h->tickets);
   cudaFree(h->tpair);
   cudaFree(h->tacc);
+  cudaFree(h->ypart);
   cudaFree(h->qs1);
   cudaFree(h->qs3);
   cudaFree(h->qs2);
@@ -174,7 +176,8 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
   static_assert(SFFN_GATE_TILED_G == FLAG_TILED_G && SFFN_GATE_RMSNORM == FLAG_RMSNORM &&
                     SFFN_DOUBLE_ACT == FLAG_DOUBLE_ACT,
                 "option bits of the ABI and of the kernels agree");
-  if (flags & ~(SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT)) {
+  static_assert(SFFN_DETERMINISTIC == FLAG_DETERMINISTIC, "option bits of the ABI and of the kernels agree");
+  if (flags & ~(SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT | SFFN_DETERMINISTIC)) {
     fail(SFFN_ERR_ARG, "flags 0x%x has unknown bits", flags);
     return nullptr;
   }
@@ -188,6 +191,10 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
   }
   if (dtype == SFFN_I8W && (r != 0 || D % 16 != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
     fail(SFFN_ERR_DTYPE, "int8 weights need the standard gate (r = 0), D %% 16 == 0 and no low-rank option");
+    return nullptr;
+  }
+  if ((flags & SFFN_DETERMINISTIC) && dtype != SFFN_BF16) {
+    fail(SFFN_ERR_DTYPE, "the deterministic option is available for bf16 handles");
     return nullptr;
   }
   if (act != SFFN_ACT_RELU && act != SFFN_ACT_RSP && act != SFFN_ACT_SILU) {
@@ -255,8 +262,19 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     h->stream_rows_cap = (H + h->stream_grid - 1) / h->stream_grid;
     if (const char* env = std::getenv("SFFN_B1_KERNEL")) h->b1_bf16 = std::strcmp(env, "stream") != 0;
     if (dtype == SFFN_BF16) {
-      h->bf16_plan = plan_ffn_b1_bf16(D, gate_k(h), r > 0, (H + std::min(h->num_sms, H) - 1) / std::min(h->num_sms, H));
+      const int g = std::min(h->num_sms, H), cap = (H + g - 1) / g;
+      h->bf16_plan = plan_ffn_b1_bf16(D, gate_k(h), r > 0, cap);
       if ((e = ffn_b1_bf16_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if (flags & SFFN_DETERMINISTIC) {
+        if (cap > ffn_b1_bf16_threads()) {
+          fail(SFFN_ERR_DTYPE, "the deterministic option needs at most %d units per block (H <= %d)",
+               ffn_b1_bf16_threads(), ffn_b1_bf16_threads() * g);
+          release(h);
+          delete h;
+          return nullptr;
+        }
+        if ((e = cudaMalloc(&h->ypart, sizeof(float) * (size_t)g * D))) return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
+      }
     }
     h->stream_plan = plan_ffn_b1_stream(D, gate_k(h), h->elt, r > 0, h->stream_rows_cap);
     if (h->stream_plan.smem > h->max_smem) {
@@ -438,8 +456,9 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   const bool lopa = h->r > 0;
   const size_t row = (size_t)h->D * h->elt;
 
+  const bool det = (h->flags & FLAG_DETERMINISTIC) != 0;  // one single-token pass per token, ordered sums
   // batches on the tensor cores (the low-rank gate's RMSNorm needs all of t first: CUDA-core path)
-  const bool tc_batch = h->tc_ready && B >= h->tc_min_batch && !(lopa && (h->flags & FLAG_RMSNORM));
+  const bool tc_batch = !det && h->tc_ready && B >= h->tc_min_batch && !(lopa && (h->flags & FLAG_RMSNORM));
   const bool tcu = tc_batch && !lopa && B <= h->tcu_max_batch;
   if (tcu) {
     // small batch: the gate on the tensor cores, the union of the live sets gathered, then finalize
@@ -494,7 +513,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   if (lopa && !tc_batch) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
   for (int b = 0; b < B && h->dtype != SFFN_I8W && !tc_batch;) {
-    const int nb = std::min(8, B - b);
+    const int nb = det ? 1 : std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;
     p.W3 = h->W3;
@@ -512,13 +531,14 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     p.act = h->act;
     p.count_slot = b;
     p.rows_cap = h->stream_rows_cap;
-    p.flags = h->flags;
+    p.flags = h->flags & ~FLAG_DETERMINISTIC;
     p.thr = h->thr;
     if (nb == 1) {
-      if (h->dtype == SFFN_BF16 && h->b1_bf16) {
+      if (h->dtype == SFFN_BF16 && (h->b1_bf16 || det)) {  // (the partial-row output is this kernel's)
         const int grid = std::min(h->num_sms, h->H);
         p.rows_cap = (h->H + grid - 1) / grid;
         p.pref_rows = h->bf16_plan.pref_rows;
+        p.ypart = h->ypart;  // null unless deterministic
         SFFN_CUDA(launch_ffn_b1_bf16(p, lopa, grid, h->bf16_plan.smem, s));
       } else {
         p.pref_rows = h->stream_plan.pref_rows;
@@ -530,7 +550,10 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       p.gather_rows = h->batch_plan.gather_rows;
       SFFN_CUDA(launch_ffn_batch(p, nb, h->dtype, lopa, h->stream_grid, h->batch_plan.smem, s));
     }
-    SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, nb, h->dtype, s));
+    if (det)
+      SFFN_CUDA(launch_finalize_ordered(h->ypart, std::min(h->num_sms, h->H), p.y, h->ctrl, p.counts, b, h->D, s));
+    else
+      SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, nb, h->dtype, s));
     b += nb;
   }
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;

@@ -233,6 +233,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 constexpr int FLAG_TILED_G = 1;
 constexpr int FLAG_RMSNORM = 2;
 constexpr int FLAG_DOUBLE_ACT = 4;
+constexpr int FLAG_DETERMINISTIC = 8;  // blocks write partial y rows, summed in block order
 constexpr float RMSNORM_EPS = 1e-6f;
 
 // Element e of a vector staged as 16-byte chunks of its storage type.

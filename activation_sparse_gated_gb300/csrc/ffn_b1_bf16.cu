@@ -169,6 +169,15 @@ __device__ __forceinline__ void dot2_t(uint32_t ra, uint32_t rb, uint32_t ts, in
   zb = warp_sum(hsum(b));
 }
 
+// SFFN_DEBUG builds check every live-list append and every gathered unit
+// index (against the list capacity and the block's own slice of units) and
+// record a violation as DEV_ERR_CHECK instead of making the access.
+#ifdef SFFN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
 // One bulk copy of `bytes` of consecutive gate rows into shared memory at
 // `dst`, completing on the mbarrier at `bar` (both shared-window addresses).
 // The copy is checked first -- 16-byte alignment of both ends and of the size,
@@ -305,6 +314,10 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
       l_mask[q - row0] = live ? 1 : 0;  // written out once at the end
       if (live) {  // compaction: append to the block's list; both gathered rows start moving into L2
         const int j = atomicAdd(misc, 1);
+        if (kDebugChecks && (j >= cap || q < row0 || q >= row1)) {
+          atomicOr(err, DEV_ERR_CHECK);
+          return;
+        }
         l_unit[j] = q;
         l_a[j] = a;
         prefetch_l2_bulk(W3 + (size_t)q * nch, (uint32_t)nch * 16u);
@@ -369,7 +382,25 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
     if (step >= 1 && nA == 0 && nB == 0) break;
   }
   __syncthreads();
-  const int n_live = misc[0];
+  const int n_live = min(misc[0], cap);
+  if (p.ypart) {
+    // deterministic option: the list in ascending unit order, so that the fold
+    // order does not depend on which warp decided first (cap <= NT is checked
+    // when the handle is created)
+    int u = 0, rank = 0;
+    float a = 0.f;
+    if (tid < n_live) {
+      u = l_unit[tid];
+      a = l_a[tid];
+      for (int k = 0; k < n_live; ++k) rank += l_unit[k] < u;
+    }
+    __syncthreads();
+    if (tid < n_live) {
+      l_unit[rank] = u;
+      l_a[rank] = a;
+    }
+    __syncthreads();
+  }
 
   // ---- gathers: thread t owns chunks t and t + NT of x, of the gathered rows and of y
   const int c0 = tid, c1 = tid + NT;
@@ -388,8 +419,13 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
     uint4 w3[M], w2[M], w3b[CPT > 1 ? M : 1], w2b[CPT > 1 ? M : 1];
 #pragma unroll
     for (int u = 0; u < M; ++u) {
-      const size_t rowo = (size_t)l_unit[b0 + (u < m ? u : 0)] * nch;
-      const bool ok = u < m;
+      const int q = l_unit[b0 + (u < m ? u : 0)];
+      const size_t rowo = (size_t)q * nch;
+      bool ok = u < m;
+      if (kDebugChecks && ok && (q < row0 || q >= row1)) {
+        if (lane == 0) atomicOr(err, DEV_ERR_CHECK);
+        ok = false;  // the unit contributes nothing
+      }
       w3[u] = (ok && h0) ? ld_l2(W3 + rowo + c0) : make_uint4(0, 0, 0, 0);
       w2[u] = (ok && h0) ? ld_l2(W2t + rowo + c0) : make_uint4(0, 0, 0, 0);
       if constexpr (CPT > 1) {
@@ -432,9 +468,20 @@ __global__ void __launch_bounds__(NT, 2) ffn_b1_bf16_kernel(const B1Params p) {
     }
     // part[] and hval[] are rewritten by the next round only after its first barrier
   }
+  if (p.ypart) {  // deterministic option: the block's partial y, every element, into its own row
+    float* yr = p.ypart + (size_t)blockIdx.x * D;
+    if (h0) {
+      __stcg(reinterpret_cast<float4*>(yr + (size_t)c0 * 8), make_float4(y0[0].x, y0[0].y, y0[1].x, y0[1].y));
+      __stcg(reinterpret_cast<float4*>(yr + (size_t)c0 * 8 + 4), make_float4(y0[2].x, y0[2].y, y0[3].x, y0[3].y));
+    }
+    if (CPT > 1 && h1) {
+      __stcg(reinterpret_cast<float4*>(yr + (size_t)c1 * 8), make_float4(y1[0].x, y1[0].y, y1[1].x, y1[1].y));
+      __stcg(reinterpret_cast<float4*>(yr + (size_t)c1 * 8 + 4), make_float4(y1[2].x, y1[2].y, y1[3].x, y1[3].y));
+    }
+  }
   // into accumulator copy (block mod YACC_COPIES): fewer blocks per address
   float* yc = p.yacc + (size_t)(blockIdx.x % YACC_COPIES) * D;
-  if (n_live > 0) {
+  if (n_live > 0 && !p.ypart) {
     if (h0) {
       atomicAdd(reinterpret_cast<float4*>(yc + (size_t)c0 * 8), make_float4(y0[0].x, y0[0].y, y0[1].x, y0[1].y));
       atomicAdd(reinterpret_cast<float4*>(yc + (size_t)c0 * 8 + 4), make_float4(y0[2].x, y0[2].y, y0[3].x, y0[3].y));
@@ -478,6 +525,8 @@ cudaError_t ffn_b1_bf16_prepare(size_t max_smem) {
   }
   return cudaSuccess;
 }
+
+int ffn_b1_bf16_threads() { return NT; }
 
 cudaError_t launch_ffn_b1_bf16(const B1Params& p, bool lopa, int grid, size_t smem, cudaStream_t s) {
   const dim3 g(grid), b(NT);

@@ -243,6 +243,12 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
       l_mask[q - row0] = live ? 1 : 0;  // written out once at the end
       if (live) {  // compaction: append to the block's live list
         const int j = atomicAdd(misc, 1);
+#ifdef SFFN_DEBUG
+        if (j >= cap) {  // debug builds: the list capacity is checked
+          atomicOr(p.ctrl + CTRL_ERR, DEV_ERR_CHECK);
+          return;
+        }
+#endif
         l_unit[j] = q;
         l_a[j] = a;
       }
@@ -330,7 +336,19 @@ __global__ void __launch_bounds__(ST, 2) ffn_b1_stream_kernel(const B1Params p) 
     if (nb1 > 0) copy_rows(next, nb1);
   }
   __syncthreads();
-  const int n_live = misc[0];
+  const int n_live = min(misc[0], cap);
+#ifdef SFFN_DEBUG
+  // debug builds: every listed unit must belong to this block's slice; one that
+  // does not is recorded and replaced by a unit of the slice with A(z) = 0, so
+  // it contributes nothing
+  for (int i = tid; i < n_live; i += ST)
+    if (l_unit[i] < row0 || l_unit[i] >= row1) {
+      atomicOr(p.ctrl + CTRL_ERR, DEV_ERR_CHECK);
+      l_unit[i] = row0;
+      l_a[i] = 0.f;
+    }
+  __syncthreads();
+#endif
 
   // ---- gathers (both rows of every live unit were prefetched into L2), in as
   // few round trips as possible.  Warp w owns chunks [cs0, cs0 + cs_n) of y,

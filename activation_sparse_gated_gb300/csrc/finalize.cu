@@ -55,7 +55,41 @@ __global__ void __launch_bounds__(FT) finalize_kernel(float* __restrict__ yacc, 
   }
 }
 
+// One thread per float4 of y: the blocks' partial rows summed in block order
+// (one fixed order, hence bitwise reproducible), rounded once.
+__global__ void __launch_bounds__(FT) finalize_ordered_kernel(const float* __restrict__ ypart, int nblocks,
+                                                              uint2* __restrict__ y, int* __restrict__ ctrl,
+                                                              int* __restrict__ counts, int count_slot, int D) {
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();
+  const int n4 = D / 4;
+  const int i = blockIdx.x * FT + threadIdx.x;
+  if (i < n4) {
+    const float4* yp = reinterpret_cast<const float4*>(ypart) + i;
+    float4 v = __ldcg(yp);
+    for (int b = 1; b < nblocks; ++b) {
+      const float4 w = __ldcg(yp + (size_t)b * n4);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    y[i] = make_uint2(pack_bf16x2_rn(v.x, v.y), pack_bf16x2_rn(v.z, v.w));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    counts[0] = __ldcg(ctrl + CTRL_COUNT + count_slot);
+    __stcg(ctrl + CTRL_COUNT + count_slot, 0);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_finalize_ordered(const float* ypart, int nblocks, void* y, int* ctrl, int* counts, int count_slot,
+                                    int D, cudaStream_t s) {
+  const dim3 g((D / 4 + FT - 1) / FT), b(FT);
+  return launch_pdl(finalize_ordered_kernel, g, b, 0, s, ypart, nblocks, static_cast<uint2*>(y), ctrl, counts,
+                    count_slot, D);
+}
 
 cudaError_t launch_finalize(float* yacc, void* y, int* ctrl, int* counts, int count_slot, int D, int nb,
                             int dtype, cudaStream_t s) {

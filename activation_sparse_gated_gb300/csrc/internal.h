@@ -32,6 +32,7 @@ struct B1Params {
   const float* s1 = nullptr;  // int8 weights: per-unit scales of the W1 and W3 codes,
   const float* s3 = nullptr;  // per-output scales of the W2 codes
   const float* s2 = nullptr;
+  float* ypart = nullptr;  // deterministic option: [grid, D] partial y of every block (plain stores)
 };
 
 // Streaming form of the fused forward (16 warps, no spin-waits); grid =
@@ -52,6 +53,7 @@ cudaError_t launch_ffn_b1_stream(const B1Params& p, int dtype, bool lopa, int gr
 StreamPlan plan_ffn_b1_bf16(int D, int gate_k, bool lopa, int rows_cap);
 cudaError_t ffn_b1_bf16_prepare(size_t max_smem);
 cudaError_t launch_ffn_b1_bf16(const B1Params& p, bool lopa, int grid, size_t smem, cudaStream_t s);
+int ffn_b1_bf16_threads();
 
 // Small-batch form (2..8 tokens per launch, CUDA cores): one pass over the
 // gate slice serves every token; gathers follow the union of live sets.
@@ -131,6 +133,11 @@ cudaError_t ffn_tcu_prepare(size_t max_smem);
 int launch_ffn_tcu(const TcPlan& plan, const TcMaps& maps, const void* W3, const void* W2t, float* yacc, int* ctrl,
                    uint8_t* mask, const void* x, int D, int H, int B, int act, int flags, float thr,
                    unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
+
+// Deterministic option: y = round(sum over blocks b = 0 .. nblocks-1, in that
+// order, of ypart[b, :]) for one token, and its live count published.
+cudaError_t launch_finalize_ordered(const float* ypart, int nblocks, void* y, int* ctrl, int* counts, int count_slot,
+                                    int D, cudaStream_t s);
 
 // y[b] = round(sum of the accumulator copies of token b) for b < nb; clears the
 // copies and publishes the nb live counts (chained behind a forward kernel).

@@ -49,9 +49,9 @@ LOPA_WORKLOAD = "lopa-bf16-D2560-H9787-r400-B1"
 METRIC = "sparse-FFN tokens/s & µs/call at B=1 (HBM GB/s vs 8 TB/s) vs dense bf16 FFN"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("activation_sparse_gated_gb300/csrc/ffn_b1_stream.cu",
+KERNEL_SOURCES = ("activation_sparse_gated_gb300/csrc/ffn_b1_bf16.cu",
                   "activation_sparse_gated_gb300/csrc/common.cuh")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffn_b1_stream_std_bf16_D2560_H7168.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ffn_b1_bf16_std_D2560_H7168.md")
 
 
 def kernel_hash() -> str:
@@ -606,7 +606,7 @@ def run_gpu(args):
                      "frac": achieved / peak, "traffic": ncu_traffic_per_launch(),
                      "peak_source": ("measured copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                                      if peak_kind == "measured" else "fallback 6.8 TB/s"),
-                     "kernel": "ffn_b1_stream_kernel<bf16>",
+                     "kernel": "ffn_b1_bf16_kernel<standard gate>",
                      "algorithmic_bytes_per_launch": bytes_step / n_tok, "kernel_source_hash": kernel_hash()},
         "gpu_launches": args.steps * n_tok * 2,  # forward kernel + finalize kernel per call
         "clocks": clocks,

@@ -31,8 +31,9 @@
  *     counters).  It is not thread-safe and must not be used by two streams
  *     at once; concurrent layers need separate handles.
  *   - Numerical sums over live units are accumulated across thread blocks with
- *     fp32 atomics, so y can differ from run to run in its last bits; the live
- *     set and the counts are deterministic.
+ *     fp32 atomics, so y can differ from run to run in its last bits (unless
+ *     the handle is created with SFFN_DETERMINISTIC); the live set and the
+ *     counts are deterministic.
  */
 #ifndef SFFN_H
 #define SFFN_H
@@ -119,8 +120,22 @@ sffn_t sffn_create(int D, int H, int r, int act, int dtype);
 enum { SFFN_GATE_TILED_G = 1, SFFN_GATE_RMSNORM = 2, SFFN_DOUBLE_ACT = 4 };
 
 /*
+ * SFFN_DETERMINISTIC (bf16 handles): y is bitwise reproducible run to run.
+ * The pages are silent on summation order; by default each thread block adds
+ * its partial y into an fp32 accumulator with atomics, so the last bits of y
+ * follow the order in which blocks finish.  With this option every token runs
+ * the single-token kernel, a block folds its live units in ascending unit
+ * order and writes its partial y to a row of its own, and a finalize kernel
+ * sums the rows in block order.  Costs a [blocks, D] fp32 buffer in the handle
+ * and one single-token pass per token (batches do not use the batched paths).
+ * SFFN_ERR_DTYPE for fp32 and int8 handles.
+ */
+enum { SFFN_DETERMINISTIC = 8 };
+
+/*
  * sffn_create with options: flags is 0 or a combination of the values above.
- * SFFN_ERR_ARG (NULL return) for unknown bits or a low-rank option with r == 0.
+ * SFFN_ERR_ARG (NULL return) for unknown bits or a low-rank option with r == 0;
+ * SFFN_ERR_DTYPE for SFFN_DETERMINISTIC on a handle that is not bf16.
  * sffn_create(D, H, r, act, dtype) is sffn_create_ex(D, H, r, act, dtype, 0).
  */
 sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags);

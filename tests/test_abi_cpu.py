@@ -42,7 +42,7 @@ def test_constants_match_header():
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
                  "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_ERR_DEVICE", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
-                 "SFFN_DOUBLE_ACT", "SFFN_ACT_SILU", "SFFN_I8W"):
+                 "SFFN_DOUBLE_ACT", "SFFN_DETERMINISTIC", "SFFN_ACT_SILU", "SFFN_I8W"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
     assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
@@ -92,12 +92,20 @@ def test_noalloc_rejects_bad_sizes_on_host(lib):
         assert "sffn_forward_noalloc" in sffn.sffn_last_error()
 
 
-@pytest.mark.parametrize("r,flags", [(64, 8), (64, -1), (0, sffn.SFFN_GATE_TILED_G), (0, sffn.SFFN_GATE_RMSNORM)])
+@pytest.mark.parametrize("r,flags", [(64, 16), (64, -1), (0, sffn.SFFN_GATE_TILED_G), (0, sffn.SFFN_GATE_RMSNORM)])
 def test_create_ex_rejects_bad_options_before_touching_the_device(lib, r, flags):
     """Unknown option bits, or a low-rank option without a low-rank gate."""
     h = lib.sffn_create_ex(512, 1024, r, sffn.SFFN_ACT_RELU, sffn.SFFN_BF16, flags)
     assert not h
     assert "flags" in sffn.sffn_last_error() or "low-rank" in sffn.sffn_last_error()
+
+
+@pytest.mark.parametrize("dtype", [sffn.SFFN_F32, sffn.SFFN_I8W])
+def test_deterministic_option_is_bf16_only_checked_on_host(lib, dtype):
+    h = lib.sffn_create_ex(512, 1024, 0, sffn.SFFN_ACT_RELU, dtype, sffn.SFFN_DETERMINISTIC)
+    assert not h
+    msg = sffn.sffn_last_error()
+    assert "deterministic" in msg or (dtype == sffn.SFFN_I8W and "int8" in msg), msg
 
 
 def test_live_threshold_rejects_bad_values_on_host(lib):

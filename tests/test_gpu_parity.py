@@ -669,3 +669,73 @@ def test_threshold_with_relu_fp32_and_full_lowrank_form():
     for B in (1, 4):
         y, c, m = run_tokens(f2, x2, B=B)
         check_thr(lw2, x2, y, c, m, "silu", thr, flags=full)
+
+
+# --------------------------------------------------------------------------- deterministic option
+@pytest.mark.parametrize("gate,B", [("standard", 1), ("standard", 3), ("lopa", 1), ("lopa", 3)])
+def test_deterministic_option_is_bitwise_reproducible(gate, B):
+    """SFFN_DETERMINISTIC: the same tokens through two handles, twice each, give bitwise identical y
+    (ordered per-block partial sums), and y matches the oracle like the default path."""
+    lw = (syn.standard_layer(1024, 3000, dtype="bf16", seed=81) if gate == "standard" else
+          syn.lopa_layer(1024, 3300, 128, dtype="bf16", seed=81))
+    x = syn.tokens(2 * B, 1024, dtype="bf16", seed=82)
+    outs = []
+    for _ in range(2):
+        ffn = make_ffn_ex(lw, sffn.SFFN_DETERMINISTIC)
+        for _ in range(2):
+            y, c, m = run_tokens(ffn, x, B=B)
+            outs.append(y)
+        ffn.close()
+    for y in outs[1:]:
+        assert np.array_equal(y, outs[0]), "y differs between runs with the deterministic option"
+    check(lw, x, outs[0], c, m)
+
+
+def test_deterministic_option_needs_bf16():
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.SparseFFN(64, 100, 0, "relu", "f32", flags=sffn.SFFN_DETERMINISTIC)
+    assert "deterministic option" in str(e.value)
+
+
+# --------------------------------------------------------------------------- bounds-checking build
+DEBUG_SCRIPT = r"""
+import sys
+import numpy as np
+sys.path.insert(0, {root!r})
+import oracle
+import activation_sparse_gated_gb300 as sffn
+from activation_sparse_gated_gb300 import build, synthetic as syn
+lib = sffn.load(build.build(debug=True))
+import torch
+cases = [(syn.standard_layer(512, 1500, dtype="bf16", seed=91), 1), (syn.standard_layer(512, 1500, dtype="bf16", seed=91), 4),
+         (syn.lopa_layer(512, 1700, 64, dtype="bf16", seed=92), 1), (syn.standard_layer(256, 700, dtype="f32", seed=93), 1),
+         (syn.standard_layer(4096, 2000, dtype="bf16", seed=94), 1)]
+for lw, B in cases:
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", lw.dtype)
+    w = {{k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}}
+    ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
+    x = syn.tokens(2 * B, lw.D, dtype=lw.dtype, seed=95)
+    ys = [ffn(x[i:i + B].cuda()).float().cpu().numpy() for i in range(0, 2 * B, B)]
+    ffn.synchronize()  # raises SffnError(SFFN_ERR_DEVICE) if a device-side check failed
+    v = {{k: syn.oracle_view(t) for k, t in lw.tensors().items()}}
+    ref, z, n = oracle.ffn_dense(lw.D, lw.H, lw.r, oracle.RELU, oracle.F32 if lw.dtype == "f32" else oracle.BF16,
+                                 v["W1"], v["U"], v["V"], v["W3"], v["W2"], syn.oracle_view(x))
+    y = np.concatenate(ys)
+    err = np.linalg.norm(y - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert (err <= (1e-5 if lw.dtype == "f32" else 2e-2)).all(), err
+    ffn.close()
+print("debug build ok")
+"""
+
+
+def test_bounds_checking_build_runs_clean():
+    """The SFFN_DEBUG build (every gathered unit index and list length checked on the device) runs
+    single tokens, a batch, the low-rank gate, fp32 and D = 4096 without a recorded violation and
+    with the oracle's results.  It runs in a child process: a process loads one library."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", DEBUG_SCRIPT.format(root=root)], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "debug build ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
