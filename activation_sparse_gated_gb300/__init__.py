@@ -5,7 +5,7 @@ kernels of ``libsffn.so`` (built in-tree by ``build.py``).  PyTorch supplies
 device memory and streams.  There is no CPU fallback: if the library is missing
 or fails to load, every entry point raises.
 
-The functions mirror the C ABI one to one (``sffn_create``, ``sffn_set_weights``,
+The functions mirror the C ABI one to one (``sffn_create``, ``sffn_set_live_fraction_hint``, ``sffn_set_weights``,
 ``sffn_forward``, ``sffn_active_counts``, ``sffn_active_mask``,
 ``sffn_synchronize``, ``sffn_destroy``, ``sffn_strerror``, ``sffn_last_error``,
 ``sffn_version``, ``sffn_debug_timeout_probe``, ``sffn_forward_noalloc``,
@@ -29,7 +29,7 @@ SFFN_MAX_BATCH = 128
 SFFN_GATE_TILED_G, SFFN_GATE_RMSNORM, SFFN_DOUBLE_ACT, SFFN_DETERMINISTIC = 1, 2, 4, 8
 
 #: every symbol include/sffn.h declares
-EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_live_threshold", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
+EXPORTS = ("sffn_create", "sffn_create_ex", "sffn_set_live_threshold", "sffn_set_live_fraction_hint", "sffn_set_weights", "sffn_forward", "sffn_active_counts",
            "sffn_active_mask", "sffn_synchronize", "sffn_destroy", "sffn_strerror",
            "sffn_last_error", "sffn_version", "sffn_debug_timeout_probe", "sffn_forward_noalloc",
            "sffn_set_weights_int8", "sffn_get_weights_int8")
@@ -57,6 +57,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "sffn_create": (vp, [ip, ip, ip, ip, ip]),
         "sffn_create_ex": (vp, [ip, ip, ip, ip, ip, ip]),
         "sffn_set_live_threshold": (ip, [vp, ctypes.c_float]),
+        "sffn_set_live_fraction_hint": (ip, [vp, ctypes.c_float]),
         "sffn_set_weights": (ip, [vp, vp, vp, vp, vp, vp]),
         "sffn_forward": (ip, [vp, vp, vp, ip, vp]),
         "sffn_active_counts": (ip, [vp, vp, ip]),
@@ -135,6 +136,10 @@ def sffn_create_ex(D: int, H: int, r: int, act: int, dtype: int, flags: int) -> 
 
 def sffn_set_live_threshold(h, thr: float):
     return _check(load().sffn_set_live_threshold(h, float(thr)))
+
+
+def sffn_set_live_fraction_hint(h, rho: float):
+    return _check(load().sffn_set_live_fraction_hint(h, float(rho)))
 
 
 def sffn_set_weights(h, W1_or_U, V, W3, W2, stream=None):
@@ -253,6 +258,10 @@ class SparseFFN:
     def set_live_threshold(self, thr: float):
         """Units with |A(z)| <= thr are skipped (0: the exact skip of ReLU / R-S+)."""
         sffn_set_live_threshold(self.h, thr)
+
+    def set_live_fraction_hint(self, rho: float):
+        """Expected live fraction per token (negative: unknown); picks the kernels of 3..16-token batches."""
+        sffn_set_live_fraction_hint(self.h, rho)
 
     def close(self):
         if getattr(self, "h", None):

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <new>
 
@@ -34,6 +35,7 @@ int fail(int code, const char* fmt, ...) {
   } while (0)
 
 constexpr unsigned long long kTimeoutNs = 250000000ull;  // 250 ms per device-side wait
+constexpr int kTicketInts = 2 * TC_TICKETS + 2;  // down-kernel slices, t-kernel slices, union count and ticket
 
 }  // namespace
 
@@ -71,8 +73,11 @@ struct sffn_s {
   int tc_t_cuda_max = TC_T_CUDA_CORE_MAX_B;  // low-rank batches up to this many tokens: t on the CUDA cores
   int tcu_max_batch = 2;   // ... and up to this many gather the union of their live sets (ffn_tcu.cu;
                            // from B = 3 its per-block partial sums of all B x D outputs cost more)
+  int tcg_force = -1;      // >= 0: batches of 3 .. tcg_force tokens take the union-skip kernels (ffn_tcg.cu)
+  float live_frac = -1.f;  // expected live fraction per token (< 0: unknown), for the batch-path choice
   uint16_t* hbuf = nullptr;
-  int* tickets = nullptr;
+  int* tickets = nullptr;  // [2 TC_TICKETS + 2]: down-kernel slices, t-kernel slices, union count, union ticket
+  int* ulist = nullptr;    // [H] the union of a small batch's live sets
   float* ypart = nullptr;     // deterministic option: [blocks, D] partial y rows of the single-token kernel
   uint16_t* tpair = nullptr;  // low-rank gate: [256, r] bf16 t pairs of a tensor-core batch
   float* tacc = nullptr;      // low-rank gate: [128, r] fp32 partial sums of the t kernel
@@ -101,6 +106,7 @@ void release(sffn_s* h) {
   cudaFree(h->mask);
   cudaFree(h->hbuf);
   cudaFree(h->tickets);
+  cudaFree(h->ulist);
   cudaFree(h->tpair);
   cudaFree(h->tacc);
   cudaFree(h->ypart);
@@ -131,7 +137,7 @@ int sync_and_check(sffn_s* h) {
     // the aborted kernel may have left partial sums and counters behind
     SFFN_CUDA(cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS));
     SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * h->D));
-    if (h->tickets) SFFN_CUDA(cudaMemset(h->tickets, 0, sizeof(int) * TC_TICKETS));
+    if (h->tickets) SFFN_CUDA(cudaMemset(h->tickets, 0, sizeof(int) * kTicketInts));
     if (err & DEV_ERR_CHECK)
       return fail(SFFN_ERR_DEVICE, "a device-side bounds or alignment check failed (error word 0x%x); outputs "
                   "of the affected forward are invalid", err);
@@ -325,9 +331,10 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     }
     if (h->tc.ok) {
       if ((e = cudaMalloc(&h->hbuf, sizeof(uint16_t) * ffn_tc_hbuf_elems(h->tc))) ||
-          (e = cudaMalloc(&h->tickets, sizeof(int) * 2 * TC_TICKETS)))  // down kernel, then t kernel
+          (e = cudaMalloc(&h->tickets, sizeof(int) * kTicketInts)) ||
+          (e = cudaMalloc(&h->ulist, sizeof(int) * (size_t)H)))
         return bail(SFFN_ERR_NOMEM, "cudaMalloc", e);
-      if ((e = cudaMemset(h->tickets, 0, sizeof(int) * 2 * TC_TICKETS))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
+      if ((e = cudaMemset(h->tickets, 0, sizeof(int) * kTicketInts))) return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if (const char* env = std::getenv("SFFN_TC_GATE_KB")) h->tc.gate_smem_budget = (size_t)std::atoi(env) * 1024;
       if (const char* env = std::getenv("SFFN_TC_DOWN_KB")) h->tc.down_smem_budget = (size_t)std::atoi(env) * 1024;
       if (const char* env = std::getenv("SFFN_TC_GATE_CHUNKS")) h->tc.gate_chunks = std::max(1, std::min(4, std::atoi(env)));
@@ -335,6 +342,10 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
         return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
       if ((e = ffn_tcu_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if ((e = ffn_tcg_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if (const char* env = std::getenv("SFFN_TCG_ACC")) h->tc.tcg_acc = std::max(1, std::min(4, std::atoi(env)));
+      if (const char* env = std::getenv("SFFN_TCG_MAX_BATCH"))
+        h->tcg_force = std::max(0, std::min(TCG_MAX_BATCH, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TCU_MAX_BATCH"))
         if (r == 0) h->tcu_max_batch = std::max(0, std::min(8, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TC_MIN_BATCH")) h->tc_min_batch = std::max(1, std::atoi(env));
@@ -443,6 +454,22 @@ int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* 
   return SFFN_OK;
 }
 
+namespace {
+// Batches of 3..16 tokens (bf16, standard gate) read only the union of the live sets when that pays:
+// the expected union u = 1 - (1 - rho)^B is at most a quarter of the units and the W3 and W2 bytes of
+// the other units come to at least 128 MB.  Below that the streaming kernels win on this GPU: they
+// stream every slice at close to the copy bandwidth, while the union's scattered rows arrive at a
+// fraction of it and the gate must finish before they can be requested.
+bool use_union_skip(const sffn_s* h, int B) {
+  if (h->r > 0 || B > TCG_MAX_BATCH) return false;
+  if (h->tcg_force >= 0) return B <= h->tcg_force;
+  if (h->live_frac < 0.f || B > 16) return false;
+  const double u = 1.0 - std::pow(1.0 - (double)h->live_frac, B);
+  const double saved = (1.0 - u) * 2.0 * 2.0 * (double)h->H * (double)h->D;
+  return u <= 0.25 && saved >= 128e6;
+}
+}  // namespace
+
 int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   if (!h) return fail(SFFN_ERR_ARG, "null handle");
   if (!x || !y) return fail(SFFN_ERR_ARG, "null x or y");
@@ -460,7 +487,17 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   // batches on the tensor cores (the low-rank gate's RMSNorm needs all of t first: CUDA-core path)
   const bool tc_batch = !det && h->tc_ready && B >= h->tc_min_batch && !(lopa && (h->flags & FLAG_RMSNORM));
   const bool tcu = tc_batch && !lopa && B <= h->tcu_max_batch;
-  if (tcu) {
+  const bool tcg = tc_batch && !tcu && !lopa && B >= 3 && use_union_skip(h, B);
+  if (tcg) {
+    // small batch, union skip: gate kernel (W1, then the union's W3 rows), down kernel (the union's W2 columns)
+    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, nullptr, nullptr, nullptr};
+    TcgBuffers ub{h->ulist, h->tickets + 2 * TC_TICKETS, h->tickets + 2 * TC_TICKETS + 1};
+    cudaError_t ce = cudaSuccess;
+    if (int rc = launch_ffn_tcg(h->tc, h->tcm, buf, ub, h->W3, h->W2t, x, y, h->D, h->H, B, h->act, h->flags, h->thr,
+                                kTimeoutNs, h->max_smem, s, &ce))
+      return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
+    SFFN_CUDA(ce);
+  } else if (tcu) {
     // small batch: the gate on the tensor cores, the union of the live sets gathered, then finalize
     cudaError_t ce = cudaSuccess;
     if (int rc = launch_ffn_tcu(h->tc, h->tcm, h->W3, h->W2t, h->yacc, h->ctrl, h->mask, x, h->D, h->H, B, h->act,
@@ -574,6 +611,16 @@ int sffn_active_counts(sffn_t h, int* counts_host, int B) {
   if (B != h->last_B) return fail(SFFN_ERR_ARG, "B=%d but the last forward had B=%d", B, h->last_B);
   if (int rc = sync_and_check(h)) return rc;
   SFFN_CUDA(cudaMemcpy(counts_host, h->counts, sizeof(int) * B, cudaMemcpyDeviceToHost));
+  double sum = 0;
+  for (int b = 0; b < B; ++b) sum += counts_host[b];
+  h->live_frac = (float)(sum / ((double)B * h->H));  // the batch-path choice follows the observed sparsity
+  return SFFN_OK;
+}
+
+int sffn_set_live_fraction_hint(sffn_t h, float rho) {
+  if (!h) return fail(SFFN_ERR_ARG, "null handle");
+  if (!(rho <= 1.f) || rho != rho) return fail(SFFN_ERR_ARG, "live fraction %g must be <= 1", (double)rho);
+  h->live_frac = rho < 0.f ? -1.f : rho;
   return SFFN_OK;
 }
 

@@ -83,6 +83,7 @@ struct TcPlan {
   int Hs = 0;  // row stride (elements) of the h buffer
   size_t gate_smem_budget = 0, down_smem_budget = 0;  // pipeline-stage bytes per block
   int gate_chunks = 0;                                // 64-wide K chunks per gate-up stage (0: 4)
+  int tcg_acc = 1;  // union-skip gate kernel: TMEM accumulators per MMA warp
 };
 struct TcMaps {
   CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
@@ -132,6 +133,23 @@ constexpr int TC_T_CUDA_CORE_MAX_B = 2;
 cudaError_t ffn_tcu_prepare(size_t max_smem);
 int launch_ffn_tcu(const TcPlan& plan, const TcMaps& maps, const void* W3, const void* W2t, float* yacc, int* ctrl,
                    uint8_t* mask, const void* x, int D, int H, int B, int act, int flags, float thr,
+                   unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
+
+// Small batches with the union skip (bf16, standard gate; ffn_tcg.cu): a gate
+// kernel (Z = W1 X^T on the tensor cores, live flags, the union of the live
+// sets compacted into a list, then P = W3[union] X^T from gathered rows and
+// h = A(z) * p at the union positions) and a down kernel (y^T += the union's
+// gathered W2^T rows^T h; the last block of a y slice rounds y).  Returns 0
+// and sets *cuda_err to the launch status, or a non-zero encode status.
+constexpr int TCG_MAX_BATCH = 32;
+struct TcgBuffers {
+  int* ulist;    // [H] the union's units, in the order the gate blocks reserved them
+  int* ucount;   // [1] units in the union, zero between calls
+  int* dticket;  // [1] down blocks done, zero between calls
+};
+cudaError_t ffn_tcg_prepare(size_t max_smem);
+int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const TcgBuffers& ub, const void* W3,
+                   const void* W2t, const void* x, void* y, int D, int H, int B, int act, int flags, float thr,
                    unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);
 
 // Deterministic option: y = round(sum over blocks b = 0 .. nblocks-1, in that

@@ -322,7 +322,7 @@ def batched_extras(ffns, layers, x, stream, args, peak):
     n_sets = len(ffns)
     ld = [{"W1": lw.W1.to(dev), "W3": lw.W3.to(dev), "W2": lw.W2.to(dev)} for lw in layers]
     out = {}
-    for B in (2, 4, 16, 64):
+    for B in (2, 4, 8, 16, 64):
         calls = x.shape[0] // B
         y = torch.empty_like(x)
         # union of the tokens' live sets per call (untimed)
@@ -341,14 +341,18 @@ def batched_extras(ffns, layers, x, stream, args, peak):
         tt = time_graph(g, stream, args.steps, args.warmup)
         us = 1e6 * tt / (args.steps * calls)
         # B = 2 gathers the union of the live sets (gate on the tensor cores, union rows of W3 and
-        # W2^T on the CUDA cores): W1 + the union rows + x, y.  From B = 3 the tensor-core path
-        # streams every unit slice of W1, W3 and W2 (the union covers most units) plus x, y and h
-        # (bf16 pair, written once, read once); union_gather_bytes is what a row-gathering design
-        # would read.
+        # W2^T on the CUDA cores): W1 + the union rows + x, y.  Larger batches of this shape stream
+        # every unit slice of W1, W3 and W2 plus x, y and h (bf16 pair, written once, read once): here
+        # the union-skip kernels would save less than 128 MB a call, below what pays on this GPU (they
+        # run when forced through SFFN_TCG_MAX_BATCH: W1, the union rows of W3 and W2^T, x, y, the
+        # union's h pair and the union list).  union_gather_bytes is what a row-gathering design reads.
         union_path = 2 <= B <= int(os.environ.get("SFFN_TCU_MAX_BATCH", "2"))
-        tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2")) and not union_path
+        skip_path = not union_path and 3 <= B <= int(os.environ.get("SFFN_TCG_MAX_BATCH", "0"))
+        tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2")) and not union_path and not skip_path
         union_bytes = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
-        bytes_call = (3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H) if tc_path else union_bytes
+        skip_bytes = union_bytes + 2 * 2 * 2 * B * mean_union + 2 * 4 * mean_union
+        bytes_call = ((3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H) if tc_path else
+                      skip_bytes if skip_path else union_bytes)
         yd = torch.empty_like(x)
 
         def body():
@@ -365,6 +369,8 @@ def batched_extras(ffns, layers, x, stream, args, peak):
         td = time_graph(gd, stream, args.steps, args.warmup)
         usd = 1e6 * td / (args.steps * calls)
         path = ("tensor cores: gate-up + down kernels" if tc_path else
+                "tensor cores, union skip: gate kernel (W1, then the union's W3 rows) + down kernel"
+                if skip_path else
                 "union gathers: gate on the tensor cores, union rows on the CUDA cores" if union_path else
                 "CUDA cores, union gathers")
         out[f"B{B}"] = {"path": path,
@@ -375,6 +381,52 @@ def batched_extras(ffns, layers, x, stream, args, peak):
                         "dense_bf16_us_per_call": usd, "speedup_vs_dense_bf16": usd / us,
                         "gpu_launches_per_call": 2 if tc_path else 2 * ((B + 7) // 8)}
         del g, gd
+    return out
+
+
+def union_skip_extras(stream, args, peak, dev):
+    """The union-skip kernels where they pay: the D = 4096 sweep shape (standard gate, H = 14336) at
+    95 % sparsity, B = 4 (the union is ~19 % of the units), four rotated weight sets (1.4 GB), against
+    the streaming kernels on the same weights; the live-fraction hint picks the path."""
+    import torch
+    import activation_sparse_gated_gb300 as sffn
+    from activation_sparse_gated_gb300 import synthetic as syn
+    B, s, n_sets = 4, 0.95, 4
+    w = syn.WORKLOADS[SWEEP_WORKLOAD]
+    D, H = w["D"], w["H"]
+    layers = syn.workload_layers(SWEEP_WORKLOAD, sets=n_sets, gate="standard", s=s)
+    x = syn.workload_tokens(SWEEP_WORKLOAD).to(dev)
+    calls = x.shape[0] // B
+    out = {"workload": f"{SWEEP_WORKLOAD} standard gate, s = {s}, B = {B}, {n_sets} rotated weight sets"}
+    for name, rho in (("union_skip", 1.0 - s), ("streaming", -1.0)):
+        ffns = build_ffns(layers, dev)
+        for f in ffns:
+            f.set_live_fraction_hint(rho)
+        y = torch.empty_like(x)
+        unions = []
+        with torch.cuda.stream(stream):
+            for t in range(min(calls, 32)):
+                f = ffns[t % n_sets]
+                sffn.sffn_forward(f.h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+                unions.append(int(f.active_mask(B).any(axis=0).sum()))
+        stream.synchronize()
+        for f in ffns:  # active_mask leaves the estimate alone; keep the path fixed
+            f.set_live_fraction_hint(rho)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(calls):
+                sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
+        us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
+        u = sum(unions) / len(unions)
+        if name == "union_skip":
+            nbytes = 2 * H * D + 2 * 2 * u * D + 2 * 2 * B * D + 2 * 2 * 2 * B * u + 2 * 4 * u
+        else:
+            nbytes = 3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H
+        out[name] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": u,
+                     "union_fraction": u / H, "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e3),
+                     "frac_of_measured": nbytes / (us * 1e3) / peak, "gpu_launches_per_call": 2}
+        del g, ffns
+    out["speedup_union_skip_vs_streaming"] = out["streaming"]["us_per_call"] / out["union_skip"]["us_per_call"]
     return out
 
 
@@ -578,6 +630,7 @@ def run_gpu(args):
             v["dense_bf16_us_per_call"] = dus
             v["speedup_vs_dense_bf16"] = dus / v["us_per_call"]
         extras["lopa_batched"] = lopa_batched
+        extras["union_skip"] = union_skip_extras(stream, args, peak, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -111,3 +111,8 @@ def test_deterministic_option_is_bf16_only_checked_on_host(lib, dtype):
 def test_live_threshold_rejects_bad_values_on_host(lib):
     import ctypes
     assert lib.sffn_set_live_threshold(None, ctypes.c_float(0.1)) == sffn.SFFN_ERR_ARG
+
+
+def test_live_fraction_hint_rejects_a_null_handle_on_host(lib):
+    import ctypes
+    assert lib.sffn_set_live_fraction_hint(None, ctypes.c_float(0.1)) == sffn.SFFN_ERR_ARG

@@ -423,6 +423,115 @@ def test_union_gather_full_size_and_d4096():
     check(lw, x, y, c, m)
 
 
+# --------------------------------------------------------------------------- union-skip kernels
+# bf16 standard-gate batches of 3..16 tokens (up to 32 with SFFN_TCG_MAX_BATCH)
+# read W1 in full and then only the union of the live sets: the union's W3
+# rows gathered into the gate kernel's second product, its W2 columns into
+# the down kernel.  The cases cover both token paddings (16, 32), ragged D and
+# H, a slice per SM and more, unions that are empty or every unit, and a
+# buffer left holding non-finite values by an earlier call.
+@pytest.mark.parametrize("B", [3, 4, 9, 16, 17, 32])
+@pytest.mark.parametrize("act,thr,flags", [("relu", 0.0, 0), ("silu", 0.3, 0), ("relu", 0.0, sffn.SFFN_DOUBLE_ACT)])
+def test_union_skip_kernels(monkeypatch, B, act, thr, flags):
+    """Against the oracle and against the streaming tensor-core path (same live sets outside the band)."""
+    kw = {"shift": 0.0} if act == "silu" else {}
+    lw = syn.standard_layer(640, 2300, dtype="bf16", seed=61, **kw)
+    x = syn.tokens(2 * B, 640, dtype="bf16", seed=62)
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "32")  # read when a handle is created
+    un = make_ffn_ex(lw, flags, act)
+    if thr:
+        un.set_live_threshold(thr)
+    y_u, c_u, m_u = run_tokens(un, x, B=B)
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "0")
+    st = make_ffn_ex(lw, flags, act)
+    if thr:
+        st.set_live_threshold(thr)
+    y_s, c_s, m_s = run_tokens(st, x, B=B)
+    check_thr(lw, x, y_u, c_u, m_u, act, thr, flags)
+    A = check_thr(lw, x, y_s, c_s, m_s, act, thr, flags)
+    sure = np.abs(A - thr) > 1e-3
+    assert np.array_equal(m_u[sure], m_s[sure])
+
+
+@pytest.mark.parametrize("D,H,B", [
+    (16, 40, 3),        # one K chunk, D far below a 64-wide tile: zero-filled K and y tails
+    (64, 151, 5),       # slices of 8 units, fewer units than SMs
+    (520, 1500, 7),     # D not a multiple of 64
+    (384, 1000, 16),    # ragged H, D not a multiple of 128
+    (256, 20000, 12),   # slices of 128 units, more slices than SMs
+    (1032, 777, 4),
+])
+def test_union_skip_shapes(monkeypatch, D, H, B):
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")  # read when a handle is created
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=D + 3 * H, shift=-0.8)
+    x = syn.tokens(2 * B, D, dtype="bf16", seed=D + 1)
+    y, c, m = run_tokens(make_ffn(lw), x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("shift", [+30.0, -30.0])
+def test_union_skip_every_unit_and_none(monkeypatch, shift):
+    """A union of all H units (its last chunk ragged) and an empty one (y == 0 exactly)."""
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
+    lw = syn.standard_layer(512, 3001, dtype="bf16", seed=63, shift=shift)
+    x = syn.tokens(8, 512, dtype="bf16", seed=64)
+    y, c, m = run_tokens(make_ffn(lw), x, B=4)
+    check(lw, x, y, c, m)
+    assert (c == (3001 if shift > 0 else 0)).all()
+    if shift < 0:
+        assert (y == 0).all()
+
+
+def test_union_skip_after_an_overflowing_call(monkeypatch):
+    """A call whose h overflows to inf (and h_lo = inf - inf to NaN) leaves those values in the h
+    buffer past the next call's union; the next calls must not pick them up (0 * NaN)."""
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
+    lw = syn.standard_layer(640, 2300, dtype="bf16", seed=65)
+    x = syn.tokens(12, 640, dtype="bf16", seed=66)
+    ffn = make_ffn(lw)
+    big = (x[:4].float() * 1e20).bfloat16().cuda()
+    ffn(big)
+    torch.cuda.synchronize()
+    for B in (4, 3, 5):
+        y, c, m = run_tokens(ffn, x[:B], B=B)
+        check(lw, x[:B], y, c, m)
+
+
+def test_union_skip_workload_sizes(monkeypatch):
+    """The standard workload (D = 2560, H = 7168) at B = 4 and 32, the D = 4096 sweep shape at B = 12."""
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "32")
+    name = "std-bf16-D2560-H7168-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    ffn = make_ffn(lw)
+    for B in (4, 32):
+        x = syn.workload_tokens(name, B)
+        y, c, m = run_tokens(ffn, x, B=B)
+        check(lw, x, y, c, m)
+    lw = syn.workload_layers("sweep-bf16-D4096-H14336", sets=1, s=0.9)[0]
+    x = syn.workload_tokens("sweep-bf16-D4096-H14336", 12)
+    y, c, m = run_tokens(make_ffn(lw), x, B=12)
+    check(lw, x, y, c, m)
+
+
+def test_union_skip_chosen_from_the_live_fraction():
+    """With no environment override, a handle at the D = 4096 sweep shape picks the kernels of a
+    4-token batch from its live-fraction estimate: the hint, then the counts sffn_active_counts
+    returns.  Every choice matches the oracle, and an out-of-range hint is refused."""
+    name = "sweep-bf16-D4096-H14336"
+    lw = syn.workload_layers(name, sets=1, s=0.95, gate="standard")[0]
+    x = syn.workload_tokens(name, 8)
+    ffn = make_ffn(lw)
+    for rho in (0.05, 0.5, -1.0):
+        ffn.set_live_fraction_hint(rho)
+        y, c, m = run_tokens(ffn, x[:4], B=4)
+        check(lw, x[:4], y, c, m)
+    # the counts of the last call (about 5 % live) now drive the choice
+    y, c, m = run_tokens(ffn, x[4:], B=4)
+    check(lw, x[4:], y, c, m)
+    with pytest.raises(sffn.SffnError):
+        ffn.set_live_fraction_hint(1.5)
+
+
 def test_tc_batched_rsp_and_changing_batch():
     """R-S+ activation, and consecutive calls whose token count changes the padded width."""
     lw = syn.standard_layer(512, 3000, dtype="bf16", seed=53)
