@@ -835,11 +835,13 @@ def run_profile_case(args):
     from activation_sparse_gated_gb300 import synthetic as syn
     import activation_sparse_gated_gb300 as sffn
     name, gate = PROFILE_CASES[args.profile_case]
-    lw = syn.workload_layers(name, sets=1, gate=gate)[0]
+    lw = syn.workload_layers(name, sets=1, gate=gate, **({} if args.sparsity is None else {"s": args.sparsity}))[0]
     dtype = {"int8": "int8", "bf16": "bf16", "f32": "f32"}.get(args.dtype or "", lw.dtype)
     ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", dtype)
     w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
     ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
+    if args.live_fraction is not None:
+        ffn.set_live_fraction_hint(args.live_fraction)
     x = syn.workload_tokens(name, args.calls * args.batch).cuda()
     for c in range(args.calls):
         ffn(x[c * args.batch:(c + 1) * args.batch])
@@ -864,6 +866,10 @@ def main():
                     help="run a short forward loop on one layer of this workload for a profiler capture (no timing)")
     ap.add_argument("--calls", type=int, default=8, help="--profile-case: forwards to run")
     ap.add_argument("--batch", type=int, default=1, help="--profile-case: tokens per forward")
+    ap.add_argument("--sparsity", type=float, default=None,
+                    help="--profile-case: rewrite the gate's bias for this sparsity (default: the workload's)")
+    ap.add_argument("--live-fraction", type=float, default=None,
+                    help="--profile-case: the handle's live-fraction hint (picks the kernels of 3..16-token batches)")
     ap.add_argument("--dtype", choices=["bf16", "f32", "int8"], default=None,
                     help="--profile-case: handle dtype (default: the workload's; int8 quantises on the device)")
     ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
