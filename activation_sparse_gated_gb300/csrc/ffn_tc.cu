@@ -17,13 +17,11 @@
 //                                                   serves both products (NU <= 64;
 //                                                   two MMAs otherwise)
 //     epilogue: live = z > 0, per-token counts and flags, and
-//               h = A(z) * p where live, else exactly 0, stored as a bf16 pair
-//               (h_hi + h_lo = h to about 16 bits): hbuf rows b (h_hi) and
-//               NB + b (h_lo), so one TMA box of 2 NB rows fetches both
+//               h = A(z) * p where live, else exactly 0, rounded to bf16 (the
+//               precision of a dense bf16 FFN's intermediate): hbuf row b
 //   down kernel, one block per (128-wide slice of y, range of units):
-//     y^T[d-slice, :] += W2^T[units, d-slice]^T [h_hi ; h_lo]   MN-major A
-//               (W2^T rows as stored); h_hi and h_lo sit back to back as one
-//               N = 2 NB operand, the epilogue adds the two column halves;
+//     y^T[d-slice, :] += W2^T[units, d-slice]^T h   MN-major A (W2^T rows as
+//               stored), h the N = NB operand (one TMA box of NB rows);
 //               fp32 atomics into an accumulator; the last block of a y slice
 //               (a ticket per slice) rounds it into y and clears it, and block
 //               0 publishes the per-token live counts.
@@ -90,7 +88,7 @@ struct TcGateArgs {
   uint32_t tmem_cols;
   int* ctrl;
   uint8_t* mask;
-  uint16_t* hbuf;  // [256][Hs] bf16 bits: h_hi in rows [0, NB), h_lo in rows [NB, 2 NB)
+  uint16_t* hbuf;  // [256][Hs] bf16 bits: h of token b in row b
   unsigned long long timeout_ns;
 };
 
@@ -108,7 +106,7 @@ struct TcDownArgs {
 __host__ __device__ constexpr uint32_t gate_stage_bytes(int C, int NU, int NB) {
   return (uint32_t)C * 128u * (uint32_t)(2 * NU + NB);
 }
-__host__ __device__ constexpr uint32_t down_chunk_bytes(int NB) { return 2u * TC_UCH * 128u + 2u * (uint32_t)NB * 128u; }
+__host__ __device__ constexpr uint32_t down_chunk_bytes(int NB) { return 2u * TC_UCH * 128u + (uint32_t)NB * 128u; }
 
 // Bytes an MMA may read past the last A region of the last stage: it reads
 // 128 rows (2 NU <= 128, W1 and W3 stacked) or MT rows from a chunk's start,
@@ -452,10 +450,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           if (p.mask) p.mask[(size_t)b * p.H + u] = lv ? 1 : 0;
           const float up = (p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, pv) : pv;
           const float hv = lv ? az * up : 0.f;
-          const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-          p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(hi);
-          p.hbuf[(size_t)(NB + b) * p.Hs + u] = __bfloat16_as_ushort(lo);
+          p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
         }
       }
     }
@@ -472,8 +467,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
 
 // --------------------------------------------------------------------------- down kernel
 // Stage layout, per unit chunk (64 units): W2^T rows for y values d0..d0+63
-// and d0+64..d0+127 (two 8 KB MN-major atom columns), then h_hi and h_lo
-// ([NB rows x 128 B] each).
+// and d0+64..d0+127 (two 8 KB MN-major atom columns), then h ([NB rows x 128 B]).
 __global__ void __launch_bounds__(TC_THREADS, 1)
     ffn_tc_down_kernel(const __grid_constant__ CUtensorMap mW2, const __grid_constant__ CUtensorMap mH,
                        const TcDownArgs p) {
@@ -559,7 +553,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncwarp();
   } else if (warp == TC_MMA_WARP) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(TC_DTILE, 2 * NB, true, false);  // N = [h_hi ; h_lo]
+      const uint32_t idesc = idesc_bf16_f32(TC_DTILE, NB, true, false);  // N = the tokens of h
       int gk = 0;  // K step over the block's units
       for (int q = 0; q < nst; ++q) {
         const int s = q % NS;
@@ -573,7 +567,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint64_t bd0 = smem_desc(cb + 2 * half, 16, 1024, SMEM_LAYOUT_SW128);
 #pragma unroll
           for (int k = 0; k < TC_UCH / 16; ++k, ++gk)
-            tc_mma(tmem + (uint32_t)(gk & (p.nacc - 1)) * (2u * NB), ad0 + (k * 2048 >> 4), bd0 + 2 * k, idesc,
+            tc_mma(tmem + (uint32_t)(gk & (p.nacc - 1)) * (uint32_t)NB, ad0 + (k * 2048 >> 4), bd0 + 2 * k, idesc,
                    gk >= p.nacc);
         }
         tc_commit(&empty[s]);
@@ -599,13 +593,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
       float* ya = p.yacc + d;
       for (int cc = 0; cc < NB; cc += 16) {
-        float v[16], v2[16];
-        tmem_ld_sum(tl + cc, 2 * NB, used, v);
-        tmem_ld_sum(tl + (uint32_t)NB + cc, 2 * NB, used, v2);  // the h_lo half
+        float v[16];
+        tmem_ld_sum(tl + cc, NB, used, v);
         if (d < p.D) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
-            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * p.D, v[jj] + v2[jj]);
+            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * p.D, v[jj]);
         }
       }
     }
@@ -717,7 +710,7 @@ int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, co
   if (!rc) rc = encode_2d(&m->w3, W3, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, (uint32_t)p.NU);
   if (!rc) rc = encode_2d(&m->w2, W2t, (uint64_t)H, (uint64_t)D, (uint64_t)D * 2, TC_UCH);
   for (int i = 0; i < 8 && !rc; ++i)  // h boxes of 2 NB rows, NB = 16 (i + 1)
-    rc = encode_2d(&m->h[i], hbuf, 256, (uint64_t)H, (uint64_t)p.Hs * 2, (uint32_t)(32 * (i + 1)));
+    rc = encode_2d(&m->h[i], hbuf, 256, (uint64_t)H, (uint64_t)p.Hs * 2, (uint32_t)(16 * (i + 1)));
   return rc;
 }
 
@@ -840,8 +833,8 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   d.nsplit = plan.nsplit;
   d.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.down_smem_budget / (TC_DC * down_chunk_bytes(NB))));
   while (d.NS > 2 && down_smem_bytes(NB, d.NS) > max_smem) --d.NS;
-  d.nacc = NB <= 64 ? 4 : 2;  // a power of two, nacc * 2 NB <= 512
-  d.tmem_cols = tmem_cols_for(d.nacc * 2 * NB);
+  d.nacc = NB <= 64 ? 4 : 2;  // a power of two, nacc * NB <= 256
+  d.tmem_cols = tmem_cols_for(d.nacc * NB);
   d.y = y;
   d.counts = buf.counts;
   d.tickets = buf.tickets;

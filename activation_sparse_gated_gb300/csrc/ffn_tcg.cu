@@ -25,10 +25,10 @@
 //              MMA thread fences the slot to the async proxy before reading;
 //     epilogue 2: one atomic on a global counter reserves the slice's
 //              positions in the batch's union list; h = A(z) * p (exactly 0
-//              for a dead pair) as a bf16 pair (h_hi + h_lo ~ 16 significant
-//              bits) at those positions: hbuf rows b (h_hi) and NB + b (h_lo).
+//              for a dead pair), rounded to bf16, at those positions of hbuf
+//              row b.
 //   down kernel, one block per (128-wide slice of y, range of the union):
-//     y^T[d-slice, :] += W2^T[union, d-slice]^T [h_hi ; h_lo]: the union's
+//     y^T[d-slice, :] += W2^T[union, d-slice]^T h: the union's
 //     W2^T row segments gathered the same way into the MN-major operand
 //     layout, a 64-position chunk per ring slot; h by TMA (the chunk that
 //     holds the end of the union by cp.async, zero past it); fp32 atomics
@@ -69,7 +69,7 @@ struct GateArgs {
   const uint16_t* x;   // [B, D] bf16
   int* ctrl;
   uint8_t* mask;       // [B_max, H]
-  uint16_t* hbuf;      // [256][Hs]: h_hi rows [0, NB), h_lo rows [NB, 2 NB), columns = union positions
+  uint16_t* hbuf;      // [256][Hs]: h of token b in row b, columns = union positions
   int* ulist;          // [H] the batch's union
   int* ucount;         // [1] units in the union (zero between calls)
   unsigned long long timeout_ns;
@@ -79,7 +79,7 @@ struct DownArgs {
   int D, H, B, NB, ndt, nsplit, RD, nacc, Hs, maxpos;
   uint32_t tmem_cols;
   const uint16_t* W2t;   // [H, D] bf16 (gathered row segments)
-  const uint16_t* hbuf;  // the gate kernel's h pairs (the union's last chunk is read directly)
+  const uint16_t* hbuf;  // the gate kernel's h (the union's last chunk is read directly)
   const int* ulist;
   int* ucount;           // reset by the last block
   int* dticket;          // [1] blocks done (for that reset), zero between calls
@@ -122,7 +122,7 @@ size_t g_smem_bytes(int C, int NU, int NB, int NS) {
   return 1024 + (size_t)NS * g_stage_bytes(C, NU, NB) + g_slack_bytes(C, NU, NB) + 8 * (2 * NS + 2 * NBUF + 1) +
          16 + 4 * (size_t)NB + 8 * (size_t)NU + 4 * (size_t)NU * (NB + 1) + 64;
 }
-__host__ __device__ constexpr uint32_t d_slot_bytes(int NB) { return 2u * UCH * 128u + 2u * (uint32_t)NB * 128u; }
+__host__ __device__ constexpr uint32_t d_slot_bytes(int NB) { return 2u * UCH * 128u + (uint32_t)NB * 128u; }
 // ring, 2 DRING_MAX + 2 mbarriers, tslot, abort flag, last-block flag, the block's union units [maxpos]
 size_t d_smem_bytes(int NB, int RD, int maxpos) {
   return 1024 + (size_t)RD * d_slot_bytes(NB) + 8 * (2 * DRING_MAX + 2) + 16 + 4 * (size_t)maxpos + 64;
@@ -468,10 +468,7 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           for (int k = 0; k < KW; ++k) pv += red[(size_t)(g * KW + k) * 16 * ldr + r * ldr + b];
           if (dbl) pv = activation(p.act, pv);
           const float hv = s_a[s_list[j] * lda + b] * pv;  // exactly 0 for a dead pair
-          const __nv_bfloat16 hi = __float2bfloat16_rn(hv);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(hv - __bfloat162float(hi));
-          p.hbuf[(size_t)b * p.Hs + base + j] = __bfloat16_as_ushort(hi);
-          p.hbuf[(size_t)(NB + b) * p.Hs + base + j] = __bfloat16_as_ushort(lo);
+          p.hbuf[(size_t)b * p.Hs + base + j] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
         }
       }
     }
@@ -487,14 +484,14 @@ __global__ void __launch_bounds__(G_THREADS, 1)
 // --------------------------------------------------------------------------- down kernel
 // Ring slot, one chunk of UCH union positions: the gathered W2^T row segments
 // for y values d0..d0+63 and d0+64..d0+127 (two 8 KB MN-major atom columns:
-// row = position, 128 B = 64 y values, swizzled), then the h pair rows
-// [2 NB rows x 128 B] (K-major: row = token, 64 positions).
+// row = position, 128 B = 64 y values, swizzled), then the h rows
+// [NB rows x 128 B] (K-major: row = token, 64 positions).
 __global__ void __launch_bounds__(D_THREADS, 1)
     ffn_tcg_down_kernel(const __grid_constant__ CUtensorMap mH, const DownArgs p) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int NB = p.NB;
-  const uint32_t half = UCH * 128u, slot_b = d_slot_bytes(NB), hbytes = 2u * (uint32_t)NB * 128u;
+  const uint32_t half = UCH * 128u, slot_b = d_slot_bytes(NB), hbytes = (uint32_t)NB * 128u;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)p.RD * slot_b);
   uint64_t* empty = full + DRING_MAX;
   uint64_t* done = empty + DRING_MAX;
@@ -608,7 +605,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         if (ragged) {
           const int c = cb + ncg - 1, pb = (c0 + c) * UCH;
           const uint32_t hb = ring + slot_addr(c) + 2 * half;
-          for (int t = lane; t < 2 * NB * 8; t += 32) {
+          for (int t = lane; t < NB * 8; t += 32) {
             const int n = t >> 3, kk = t & 7, pp = pb + 8 * kk;
             const int keep = min(8, max(0, U - pp));  // values of the piece inside the union
             cp_async16_zfill(hb + (uint32_t)n * 128u + ((uint32_t)(kk ^ (n & 7)) << 4),
@@ -623,7 +620,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
       for (int q = max(0, g - RSD); q < g; ++q) mbar_wait_drain(&full[q % RSD], (q / RSD) & 1, p.timeout_ns);
   } else if (lane == 0) {
     // warp 5: the MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(DT, 2 * NB, true, false);  // N = [h_hi ; h_lo]
+    const uint32_t idesc = idesc_bf16_f32(DT, NB, true, false);  // N = the tokens of h
     int gk = 0;
     for (int g = 0; g < NGD; ++g) {
       const int slot = g % RSD, cb = g * GCD, ncg = min(GCD, nch - cb);
@@ -637,7 +634,7 @@ __global__ void __launch_bounds__(D_THREADS, 1)
         const uint64_t bd0 = smem_desc(sb + 2 * half, 16, 1024, SMEM_LAYOUT_SW128);
 #pragma unroll
         for (int kk = 0; kk < UCH / 16; ++kk, ++gk)
-          tc_mma(tmem + (uint32_t)(gk & (p.nacc - 1)) * (2u * NB), ad0 + (kk * 2048 >> 4), bd0 + 2 * kk, idesc,
+          tc_mma(tmem + (uint32_t)(gk & (p.nacc - 1)) * (uint32_t)NB, ad0 + (kk * 2048 >> 4), bd0 + 2 * kk, idesc,
                  gk >= p.nacc);
       }
       tc_commit(&empty[slot]);
@@ -661,13 +658,12 @@ __global__ void __launch_bounds__(D_THREADS, 1)
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
       float* ya = p.yacc + d;
       for (int cc = 0; cc < NB; cc += 16) {
-        float v[16], v2[16];
-        tmem_ld_sum(tl + cc, 2 * NB, used, v);
-        tmem_ld_sum(tl + (uint32_t)NB + cc, 2 * NB, used, v2);  // the h_lo half
+        float v[16];
+        tmem_ld_sum(tl + cc, NB, used, v);
         if (d < D) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
-            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * D, v[jj] + v2[jj]);
+            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * D, v[jj]);
         }
       }
     }
@@ -793,8 +789,8 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
   d.maxpos = (plan.nch + plan.nsplit - 1) / plan.nsplit * UCH;  // the union has at most nch chunks
   d.RD = 2;
   while (d.RD < DRING_MAX && d.RD * UCH < d.maxpos && d_smem_bytes(NB, d.RD + 1, d.maxpos) <= budget) ++d.RD;
-  d.nacc = NB <= 16 ? 8 : 4;  // a power of two, nacc * 2 NB <= 256 TMEM columns
-  d.tmem_cols = tmem_cols_pow2(d.nacc * 2 * NB);
+  d.nacc = 8;  // a power of two, nacc * NB <= 256 TMEM columns (NB <= 32)
+  d.tmem_cols = tmem_cols_pow2(d.nacc * NB);
   d.W2t = static_cast<const uint16_t*>(W2t);
   d.hbuf = buf.hbuf;
   d.ulist = ub.ulist;

@@ -89,10 +89,10 @@ struct TcMaps {
   CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
   CUtensorMap w2;      // W2^T [H, D]: boxes of 64 columns x 64 rows
   CUtensorMap v;       // V [r, D] (low-rank gate): boxes of 64 columns x NUt rows
-  CUtensorMap h[8];    // h buffer [256, H]: boxes of 64 columns x 2 NB rows, NB = 16 (i + 1)
+  CUtensorMap h[8];    // h buffer [256, H]: boxes of 64 columns x NB rows, NB = 16 (i + 1)
 };
 struct TcBuffers {
-  uint16_t* hbuf;  // ffn_tc_hbuf_elems(plan) bf16 values
+  uint16_t* hbuf;  // ffn_tc_hbuf_elems(plan) bf16 values: h of token b in row b
   float* yacc;     // [B_max * YACC_COPIES, D]
   int* ctrl;
   uint8_t* mask;   // [B_max, H]

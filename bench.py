@@ -342,16 +342,16 @@ def batched_extras(ffns, layers, x, stream, args, peak):
         us = 1e6 * tt / (args.steps * calls)
         # B = 2 gathers the union of the live sets (gate on the tensor cores, union rows of W3 and
         # W2^T on the CUDA cores): W1 + the union rows + x, y.  Larger batches of this shape stream
-        # every unit slice of W1, W3 and W2 plus x, y and h (bf16 pair, written once, read once): here
+        # every unit slice of W1, W3 and W2 plus x, y and h (bf16, written once, read once): here
         # the union-skip kernels would save less than 128 MB a call, below what pays on this GPU (they
         # run when forced through SFFN_TCG_MAX_BATCH: W1, the union rows of W3 and W2^T, x, y, the
-        # union's h pair and the union list).  union_gather_bytes is what a row-gathering design reads.
+        # union's h and the union list).  union_gather_bytes is what a row-gathering design reads.
         union_path = 2 <= B <= int(os.environ.get("SFFN_TCU_MAX_BATCH", "2"))
         skip_path = not union_path and 3 <= B <= int(os.environ.get("SFFN_TCG_MAX_BATCH", "0"))
         tc_path = B >= int(os.environ.get("SFFN_TC_MIN_BATCH", "2")) and not union_path and not skip_path
         union_bytes = 2 * H * D + 2 * 2 * mean_union * D + 2 * 2 * B * D
-        skip_bytes = union_bytes + 2 * 2 * 2 * B * mean_union + 2 * 4 * mean_union
-        bytes_call = ((3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H) if tc_path else
+        skip_bytes = union_bytes + 2 * 2 * B * mean_union + 2 * 4 * mean_union
+        bytes_call = ((3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * B * H) if tc_path else
                       skip_bytes if skip_path else union_bytes)
         yd = torch.empty_like(x)
 
@@ -419,9 +419,9 @@ def union_skip_extras(stream, args, peak, dev):
         us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
         u = sum(unions) / len(unions)
         if name == "union_skip":
-            nbytes = 2 * H * D + 2 * 2 * u * D + 2 * 2 * B * D + 2 * 2 * 2 * B * u + 2 * 4 * u
+            nbytes = 2 * H * D + 2 * 2 * u * D + 2 * 2 * B * D + 2 * 2 * B * u + 2 * 4 * u
         else:
-            nbytes = 3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * 2 * B * H
+            nbytes = 3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * B * H
         out[name] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": u,
                      "union_fraction": u / H, "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e3),
                      "frac_of_measured": nbytes / (us * 1e3) / peak, "gpu_launches_per_call": 2}
@@ -454,8 +454,8 @@ def lopa_batched_extras(ffns, x, stream, args, peak, D, Hp, r):
                 sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
         us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
         del g
-        # streamed: U, V and every slice of W3 and W2^T, plus x, y, the t pair and the h pair
-        streamed = 2 * r * (D + Hp) + 2 * 2 * Hp * D + 2 * 2 * B * D + 2 * 2 * B * r + 2 * 2 * 2 * B * Hp
+        # streamed: U, V and every slice of W3 and W2^T, plus x, y, the t pair and h
+        streamed = 2 * r * (D + Hp) + 2 * 2 * Hp * D + 2 * 2 * B * D + 2 * 2 * B * r + 2 * 2 * B * Hp
         union_bytes = 2 * r * (D + Hp) + 2 * 2 * mean_union * D + 2 * 2 * B * D
         out[f"B{B}"] = {"path": "tensor cores: t pair, gate-up (U t and W3 x) + down kernels",
                         "us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": mean_union,

@@ -483,8 +483,8 @@ def test_union_skip_every_unit_and_none(monkeypatch, shift):
 
 
 def test_union_skip_after_an_overflowing_call(monkeypatch):
-    """A call whose h overflows to inf (and h_lo = inf - inf to NaN) leaves those values in the h
-    buffer past the next call's union; the next calls must not pick them up (0 * NaN)."""
+    """A call whose h overflows to inf leaves inf in the h buffer past the next call's union; the
+    next calls must not pick it up (0 * inf = NaN)."""
     monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
     lw = syn.standard_layer(640, 2300, dtype="bf16", seed=65)
     x = syn.tokens(12, 640, dtype="bf16", seed=66)
