@@ -455,18 +455,19 @@ int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* 
 }
 
 namespace {
-// Batches of 3..16 tokens (bf16, standard gate) read only the union of the live sets when that pays:
-// the expected union u = 1 - (1 - rho)^B is at most a quarter of the units and the W3 and W2 bytes of
-// the other units come to at least 128 MB.  Below that the streaming kernels win on this GPU: they
-// stream every slice at close to the copy bandwidth, while the union's scattered rows arrive at a
-// fraction of it and the gate must finish before they can be requested.
+// Batches of 3..16 tokens (bf16) read only the union of the live sets when that pays: the expected
+// union u = 1 - (1 - rho)^B is at most a quarter of the units and the W3 and W2 bytes of the other units
+// come to at least 128 MB (standard gate) or 64 MB (low-rank gate, whose streaming form pays a t kernel
+// and whose union form streams only U before the union is known).  Below that the streaming kernels win
+// on this GPU: they stream every slice at close to the copy bandwidth, while the union's scattered rows
+// arrive at a fraction of it and the gate must finish before they can be requested.
 bool use_union_skip(const sffn_s* h, int B) {
-  if (h->r > 0 || B > TCG_MAX_BATCH) return false;
+  if (B > TCG_MAX_BATCH) return false;
   if (h->tcg_force >= 0) return B <= h->tcg_force;
   if (h->live_frac < 0.f || B > 16) return false;
   const double u = 1.0 - std::pow(1.0 - (double)h->live_frac, B);
   const double saved = (1.0 - u) * 2.0 * 2.0 * (double)h->H * (double)h->D;
-  return u <= 0.25 && saved >= 128e6;
+  return u <= 0.25 && saved >= (h->r > 0 ? 64e6 : 128e6);
 }
 }  // namespace
 
@@ -487,12 +488,24 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
   // batches on the tensor cores (the low-rank gate's RMSNorm needs all of t first: CUDA-core path)
   const bool tc_batch = !det && h->tc_ready && B >= h->tc_min_batch && !(lopa && (h->flags & FLAG_RMSNORM));
   const bool tcu = tc_batch && !lopa && B <= h->tcu_max_batch;
-  const bool tcg = tc_batch && !tcu && !lopa && B >= 3 && use_union_skip(h, B);
+  const bool tcg = tc_batch && !tcu && B >= 3 && use_union_skip(h, B);
   if (tcg) {
-    // small batch, union skip: gate kernel (W1, then the union's W3 rows), down kernel (the union's W2 columns)
-    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, nullptr, nullptr, nullptr};
+    // small batch, union skip: gate kernel (W1 or U t, then the union's W3 rows), down kernel (the union's W2
+    // columns); the low-rank gate's t pair first
+    TcBuffers buf{h->hbuf, h->yacc, h->ctrl, h->mask, h->counts, h->tickets, h->tpair, h->tacc,
+                  h->tickets + TC_TICKETS};
     TcgBuffers ub{h->ulist, h->tickets + 2 * TC_TICKETS, h->tickets + 2 * TC_TICKETS + 1};
     cudaError_t ce = cudaSuccess;
+    if (lopa) {
+      if (B <= h->tc_t_cuda_max) {
+        SFFN_CUDA(launch_lopa_t_pair(h->V, x, h->tpair, h->r, h->D, B, (B + 15) / 16 * 16, s));
+      } else {
+        if (int rc = launch_ffn_tc(h->tc, h->tcm, buf, x, y, h->D, h->H, B, h->act, h->flags, h->thr, kTimeoutNs,
+                                   h->max_smem, s, &ce, false, true))
+          return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
+        SFFN_CUDA(ce);
+      }
+    }
     if (int rc = launch_ffn_tcg(h->tc, h->tcm, buf, ub, h->W3, h->W2t, x, y, h->D, h->H, B, h->act, h->flags, h->thr,
                                 kTimeoutNs, h->max_smem, s, &ce))
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);

@@ -726,7 +726,7 @@ cudaError_t ffn_tc_prepare(size_t max_smem) {
 
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
-                  cudaError_t* cuda_err, bool tpair_ready) {
+                  cudaError_t* cuda_err, bool tpair_ready, bool t_only) {
   *cuda_err = cudaSuccess;
   const bool lopa = plan.r > 0;
   if (!plan.ok || B < 1 || B > 128 || (lopa && !buf.tpair)) return -1;
@@ -805,7 +805,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     }
     e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t * gt.ksplit), gb, smt, s, maps.v, maps.v,
                    mx, mx, gt);
-    if (e) {
+    if (e || t_only) {
       *cuda_err = e;
       return 0;
     }

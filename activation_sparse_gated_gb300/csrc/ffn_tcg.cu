@@ -61,6 +61,7 @@ constexpr size_t SMEM_BUDGET = 200 * 1024;
 
 struct GateArgs {
   int D, H, B, NB, NU, KC, C, NCG, NS, act, flags, Hs, nacc, apw;  // nacc MMA warps, apw accumulators each
+  int XR;  // rows of phase 1's B tiles: NB (x), or 2 NB (the low-rank gate's t pair, t_hi then t_lo)
   int NX;  // phase 2: tokens padded to 8
   float thr;
   uint32_t tmem_cols;
@@ -118,8 +119,8 @@ __host__ __device__ inline int g_segment(uint32_t area, int nu16, int NX) {
 // after the stages and slack: 2 NS + 2 NBUF + 1 mbarriers, then tslot,
 // abort flag, union count and base, per-token counts [NB], union flags [NU],
 // union list [NU], A(z) [NU][NB + 1]
-size_t g_smem_bytes(int C, int NU, int NB, int NS) {
-  return 1024 + (size_t)NS * g_stage_bytes(C, NU, NB) + g_slack_bytes(C, NU, NB) + 8 * (2 * NS + 2 * NBUF + 1) +
+size_t g_smem_bytes(int C, int NU, int NB, int XR, int NS) {
+  return 1024 + (size_t)NS * g_stage_bytes(C, NU, XR) + g_slack_bytes(C, NU, XR) + 8 * (2 * NS + 2 * NBUF + 1) +
          16 + 4 * (size_t)NB + 8 * (size_t)NU + 4 * (size_t)NU * (NB + 1) + 64;
 }
 __host__ __device__ constexpr uint32_t d_slot_bytes(int NB) { return 2u * UCH * 128u + (uint32_t)NB * 128u; }
@@ -175,15 +176,19 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 // 2 lays a ring of slots [nu8 rows of W3 | NB rows of x] over the same bytes.
 // TMEM: nacc * apw accumulators of NB columns (lanes = slice rows in phase 1, union
 // entries in phase 2).
+// LOPA: phase 1 is the low-rank gate z = U t: mW1 maps U [H, r] (K chunks over
+// r) and mX the t pair [2 NB, r]; two MMAs per K step, U t_hi and U t_lo, into
+// one accumulator.  Phases 2 and the down kernel are the standard gate's.
+template <bool LOPA>
 __global__ void __launch_bounds__(G_THREADS, 1)
     ffn_tcg_gate_kernel(const __grid_constant__ CUtensorMap mW1, const __grid_constant__ CUtensorMap mX,
                         const GateArgs p) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   const int NS = p.NS, NB = p.NB, C = p.C, NU = p.NU;
-  const uint32_t wreg = (uint32_t)NU * 128u, xreg = (uint32_t)NB * 128u;
-  const uint32_t st_bytes = g_stage_bytes(C, NU, NB);
-  const uint32_t ring_bytes = (uint32_t)NS * st_bytes + g_slack_bytes(C, NU, NB);
+  const uint32_t wreg = (uint32_t)NU * 128u, xreg = (uint32_t)p.XR * 128u;
+  const uint32_t st_bytes = g_stage_bytes(C, NU, p.XR);
+  const uint32_t ring_bytes = (uint32_t)NS * st_bytes + g_slack_bytes(C, NU, p.XR);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + ring_bytes);
   uint64_t* empty = full + NS;
   uint64_t* f2 = empty + NS;  // phase 2: segment buffer filled (bulk copies)
@@ -287,7 +292,10 @@ __global__ void __launch_bounds__(G_THREADS, 1)
           const uint64_t ac = a0 + ((c * wreg) >> 4), bc = b0 + ((c * xreg) >> 4);
           const int kc = q * C + c;
           const uint32_t da = tmem + (uint32_t)(mw + p.nacc * (kc % p.apw)) * NB;
-          for (int kk = mw; kk < 4; kk += p.nacc) tc_mma(da, ac + 2 * kk, bc + 2 * kk, idesc, kc >= p.apw);
+          for (int kk = mw; kk < 4; kk += p.nacc) {
+            tc_mma(da, ac + 2 * kk, bc + 2 * kk, idesc, kc >= p.apw);
+            if constexpr (LOPA) tc_mma(da, ac + 2 * kk, bc + (uint32_t)NB * 8u + 2 * kk, idesc, true);  // U t_lo
+          }
         }
         tc_commit(&empty[s]);
       }
@@ -323,7 +331,9 @@ __global__ void __launch_bounds__(G_THREADS, 1)
       const int u = u0 + r;
       bool any = false;
       for (int b = g; b < p.B; b += 4) {
-        const float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
+        float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
+        if (LOPA && valid && (p.flags & FLAG_TILED_G))  // (G x)_u = x_{u mod D}
+          z += __bfloat162float(__ushort_as_bfloat16(p.x[(size_t)b * D + u % D]));
         const float az = activation(p.act, z);
         const bool lv = valid && is_live(az, p.thr);
         const unsigned bal = __ballot_sync(0xffffffffu, lv);
@@ -714,7 +724,9 @@ uint32_t tmem_cols_pow2(int n) {
 }  // namespace
 
 cudaError_t ffn_tcg_prepare(size_t max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(ffn_tcg_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(ffn_tcg_gate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  if (!e) e = cudaFuncSetAttribute(ffn_tcg_gate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   if (!e) e = cudaFuncSetAttribute(ffn_tcg_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   return e;
 }
@@ -723,12 +735,17 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
                    const void* W2t, const void* x, void* y, int D, int H, int B, int act, int flags, float thr,
                    unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err) {
   *cuda_err = cudaSuccess;
-  if (!plan.ok || plan.r > 0 || B < 1 || B > TCG_MAX_BATCH || plan.NU > 128 || !ub.ulist || !ub.ucount ||
-      !ub.dticket)
+  const bool lopa = plan.r > 0;
+  if (!plan.ok || B < 1 || B > TCG_MAX_BATCH || plan.NU > 128 || !ub.ulist || !ub.ucount || !ub.dticket ||
+      (lopa && !buf.tpair))
     return -1;
   const int NB = (B + 15) / 16 * 16;
+  // phase 1's B operand: x [B, D], or the low-rank gate's t pair [2 NB, r] (written before this launch)
   CUtensorMap mx;
-  if (int rc = encode_2d(&mx, x, (uint64_t)B, (uint64_t)D, (uint64_t)D * 2, (uint32_t)NB)) return rc;
+  if (int rc = lopa ? encode_2d(&mx, buf.tpair, (uint64_t)(2 * NB), (uint64_t)plan.r, (uint64_t)plan.r * 2,
+                                (uint32_t)(2 * NB))
+                    : encode_2d(&mx, x, (uint64_t)B, (uint64_t)D, (uint64_t)D * 2, (uint32_t)NB))
+    return rc;
   const size_t budget = std::min(max_smem, SMEM_BUDGET);
   GateArgs g;
   g.D = D;
@@ -736,13 +753,14 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
   g.B = B;
   g.NB = NB;
   g.NU = plan.NU;
-  g.KC = plan.KC;
+  g.KC = lopa ? plan.KCZ : plan.KC;  // phase 1's 64-wide K chunks (over r or D)
+  g.XR = lopa ? 2 * NB : NB;
   g.C = 4;
-  while (g.C > 1 && g_smem_bytes(g.C, g.NU, NB, 2) > budget) g.C >>= 1;
-  g.NCG = (plan.KC + g.C - 1) / g.C;
+  while (g.C > 1 && g_smem_bytes(g.C, g.NU, NB, g.XR, 2) > budget) g.C >>= 1;
+  g.NCG = (g.KC + g.C - 1) / g.C;
   g.NS = 2;
   // phase 1 keeps up to NS_MAX stages; phase 2's ring spans all of them
-  while (g.NS < NS_MAX && g_smem_bytes(g.C, g.NU, NB, g.NS + 1) <= budget) ++g.NS;
+  while (g.NS < NS_MAX && g_smem_bytes(g.C, g.NU, NB, g.XR, g.NS + 1) <= budget) ++g.NS;
   g.act = act;
   g.flags = flags;
   g.thr = thr;
@@ -755,7 +773,7 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
   g.x = static_cast<const uint16_t*>(x);
   g.NX = (B + 7) / 8 * 8;
   {  // phase 2: NBUF segment buffers of the largest possible union (every unit of a slice) fit over the stages
-    const uint32_t area = (uint32_t)g.NS * g_stage_bytes(g.C, g.NU, NB) + g_slack_bytes(g.C, g.NU, NB);
+    const uint32_t area = (uint32_t)g.NS * g_stage_bytes(g.C, g.NU, g.XR) + g_slack_bytes(g.C, g.NU, g.XR);
     if (g_segment(area, (g.NU + 15) / 16 * 16, g.NX) == 0 || 8u * 16u * (uint32_t)(g.NX + 1) * 4u > area) {
       *cuda_err = cudaErrorInvalidConfiguration;
       return 0;
@@ -767,13 +785,16 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
   g.ulist = ub.ulist;
   g.ucount = ub.ucount;
   g.timeout_ns = timeout_ns;
-  const size_t smem1 = g_smem_bytes(g.C, g.NU, NB, g.NS);
+  const size_t smem1 = g_smem_bytes(g.C, g.NU, NB, g.XR, g.NS);
   // the epilogue's copy of Z ([128][NB + 1] fp32) lies over the stages
-  if (smem1 > max_smem || (size_t)g.NS * g_stage_bytes(g.C, g.NU, NB) < (size_t)128 * (NB + 1) * 4) {
+  if (smem1 > max_smem || (size_t)g.NS * g_stage_bytes(g.C, g.NU, g.XR) < (size_t)128 * (NB + 1) * 4) {
     *cuda_err = cudaErrorInvalidConfiguration;
     return 0;
   }
-  cudaError_t e = launch_pdl(ffn_tcg_gate_kernel, dim3(plan.ntiles), dim3(G_THREADS), smem1, s, maps.w1, mx, g);
+  cudaError_t e = lopa ? launch_pdl(ffn_tcg_gate_kernel<true>, dim3(plan.ntiles), dim3(G_THREADS), smem1, s, maps.w1,
+                                    mx, g)
+                       : launch_pdl(ffn_tcg_gate_kernel<false>, dim3(plan.ntiles), dim3(G_THREADS), smem1, s, maps.w1,
+                                    mx, g);
   if (e) {
     *cuda_err = e;
     return 0;

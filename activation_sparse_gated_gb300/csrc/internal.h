@@ -116,11 +116,12 @@ int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, co
 cudaError_t ffn_tc_prepare(size_t max_smem);
 // Whole forward (y and counts written; no finalize kernel).  Low-rank gate:
 // tpair_ready says the caller already wrote the t pair (launch_lopa_t_pair);
-// otherwise the t kernel runs on the tensor cores first.  Returns 0 and sets
+// otherwise the t kernel runs on the tensor cores first (t_only: and nothing
+// else -- the t pair for the union-skip kernels).  Returns 0 and sets
 // *cuda_err to the launch status, or a non-zero encode status.
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
                   int B, int act, int flags, float thr, unsigned long long timeout_ns, size_t max_smem, cudaStream_t s,
-                  cudaError_t* cuda_err, bool tpair_ready = false);
+                  cudaError_t* cuda_err, bool tpair_ready = false, bool t_only = false);
 // Low-rank batches of up to this many tokens take the CUDA-core t kernel
 // (measured per call on the low-rank workload: 31.5 against 31.6 us at B = 2;
 // at B = 4 the split tensor-core t kernel is faster, 31.9 against 33.9 us).

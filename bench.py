@@ -384,21 +384,22 @@ def batched_extras(ffns, layers, x, stream, args, peak):
     return out
 
 
-def union_skip_extras(stream, args, peak, dev):
-    """The union-skip kernels where they pay: the D = 4096 sweep shape (standard gate, H = 14336) at
-    95 % sparsity, B = 4 (the union is ~19 % of the units), four rotated weight sets (1.4 GB), against
-    the streaming kernels on the same weights; the live-fraction hint picks the path."""
+def union_skip_extras(stream, args, peak, dev, gate, name, s, B, n_sets):
+    """The union-skip kernels where they pay, against the streaming kernels on the same weights (the
+    live-fraction hint picks the path): `gate` layer of workload `name` with its bias rewritten for
+    sparsity s, B tokens per call over n_sets rotated weight sets."""
     import torch
     import activation_sparse_gated_gb300 as sffn
     from activation_sparse_gated_gb300 import synthetic as syn
-    B, s, n_sets = 4, 0.95, 4
-    w = syn.WORKLOADS[SWEEP_WORKLOAD]
-    D, H = w["D"], w["H"]
-    layers = syn.workload_layers(SWEEP_WORKLOAD, sets=n_sets, gate="standard", s=s)
-    x = syn.workload_tokens(SWEEP_WORKLOAD).to(dev)
+    w = syn.WORKLOADS[name]
+    D = w["D"]
+    layers = syn.workload_layers(name, sets=n_sets, gate=gate, s=s)
+    H, r = layers[0].H, layers[0].r
+    x = syn.workload_tokens(name).to(dev)
+    x = x[:min(x.shape[0], 1024)]
     calls = x.shape[0] // B
-    out = {"workload": f"{SWEEP_WORKLOAD} standard gate, s = {s}, B = {B}, {n_sets} rotated weight sets"}
-    for name, rho in (("union_skip", 1.0 - s), ("streaming", -1.0)):
+    out = {"workload": f"{name} {gate} gate, s = {s}, B = {B}, {n_sets} rotated weight sets"}
+    for path, rho in (("union_skip", 1.0 - s), ("streaming", -1.0)):
         ffns = build_ffns(layers, dev)
         for f in ffns:
             f.set_live_fraction_hint(rho)
@@ -410,21 +411,21 @@ def union_skip_extras(stream, args, peak, dev):
                 sffn.sffn_forward(f.h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
                 unions.append(int(f.active_mask(B).any(axis=0).sum()))
         stream.synchronize()
-        for f in ffns:  # active_mask leaves the estimate alone; keep the path fixed
-            f.set_live_fraction_hint(rho)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for t in range(calls):
                 sffn.sffn_forward(ffns[t % n_sets].h, x[t * B:(t + 1) * B], y[t * B:(t + 1) * B], B, stream)
         us = 1e6 * time_graph(g, stream, args.steps, args.warmup) / (args.steps * calls)
         u = sum(unions) / len(unions)
-        if name == "union_skip":
-            nbytes = 2 * H * D + 2 * 2 * u * D + 2 * 2 * B * D + 2 * 2 * B * u + 2 * 4 * u
+        gate_bytes = 2 * H * D if r == 0 else 2 * r * (D + H) + 2 * 2 * B * r  # W1, or V, U and the t pair
+        if path == "union_skip":
+            nbytes = gate_bytes + 2 * 2 * u * D + 2 * 2 * B * D + 2 * 2 * B * u + 2 * 4 * u
         else:
-            nbytes = 3 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * B * H
-        out[name] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": u,
+            nbytes = gate_bytes + 2 * 2 * H * D + 2 * 2 * B * D + 2 * 2 * B * H
+        out[path] = {"us_per_call": us, "tokens_per_s": B * 1e6 / us, "mean_union_units": u,
                      "union_fraction": u / H, "bytes_per_call": nbytes, "gbs": nbytes / (us * 1e3),
-                     "frac_of_measured": nbytes / (us * 1e3) / peak, "gpu_launches_per_call": 2}
+                     "frac_of_measured": nbytes / (us * 1e3) / peak,
+                     "gpu_launches_per_call": 2 if r == 0 else 3}
         del g, ffns
     out["speedup_union_skip_vs_streaming"] = out["streaming"]["us_per_call"] / out["union_skip"]["us_per_call"]
     return out
@@ -630,7 +631,8 @@ def run_gpu(args):
             v["dense_bf16_us_per_call"] = dus
             v["speedup_vs_dense_bf16"] = dus / v["us_per_call"]
         extras["lopa_batched"] = lopa_batched
-        extras["union_skip"] = union_skip_extras(stream, args, peak, dev)
+        extras["union_skip"] = union_skip_extras(stream, args, peak, dev, "standard", SWEEP_WORKLOAD, 0.95, 4, 4)
+        extras["union_skip_lopa"] = union_skip_extras(stream, args, peak, dev, "lopa", LOPA_WORKLOAD, 0.95, 4, 8)
 
     cpu = None
     if rank == 0 and not args.no_cpu:

@@ -154,14 +154,15 @@ int sffn_set_live_threshold(sffn_t h, float thr);
 
 /*
  * Expected live fraction rho per token, which picks the kernels of a batch of
- * 3 <= B <= 16 tokens (bf16 handles, standard gate).  A batch needs the W3 rows
- * and W2 columns of the union of its tokens' live sets, about 1 - (1 - rho)^B of
- * the units ("Model casting: compute the gate, then skip most of the FFN", on
- * batching).  The union-skip kernels read W1 in full and then only the union's
- * rows of W3 and W2^T; the streaming kernels read every slice of W3 and W2 and
- * let the gate zero the dead terms.  The forward takes the union-skip kernels
- * when the expected union is at most a quarter of the units and the W3 and W2
- * bytes of the other units come to at least 128 MB, else the streaming kernels:
+ * 3 <= B <= 16 tokens (bf16 handles; the low-rank gate without RMSNorm).  A
+ * batch needs the W3 rows and W2 columns of the union of its tokens' live
+ * sets, about 1 - (1 - rho)^B of the units ("Model casting: compute the gate, then skip most of the FFN", on
+ * batching).  The union-skip kernels read the gate (W1, or U after t = V x) in
+ * full and then only the union's rows of W3 and W2^T; the streaming kernels
+ * read every slice of W3 and W2 and let the gate zero the dead terms.  The
+ * forward takes the union-skip kernels when the expected union is at most a
+ * quarter of the units and the W3 and W2 bytes of the other units come to at
+ * least 128 MB (64 MB for the low-rank gate), else the streaming kernels:
  * on this GPU a gathered row arrives at a fraction of the streaming bandwidth,
  * and the rows can only be requested once the gate is known.  Both compute the
  * same y within rounding.  rho in [0, 1] (SFFN_ERR_ARG otherwise); a negative

@@ -513,6 +513,33 @@ def test_union_skip_workload_sizes(monkeypatch):
     check(lw, x, y, c, m)
 
 
+@pytest.mark.parametrize("B", [3, 4, 9, 16])
+@pytest.mark.parametrize("flags", [0, sffn.SFFN_GATE_TILED_G, sffn.SFFN_GATE_TILED_G | sffn.SFFN_DOUBLE_ACT])
+def test_union_skip_low_rank_gate(monkeypatch, B, flags):
+    """The low-rank gate through the union-skip kernels: t as a bf16 pair (the tensor-core t kernel),
+    z = U t_hi + U t_lo in the gate kernel's first phase, then the union's W3 and W2 rows, against the
+    oracle with the same options."""
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
+    lw = syn.lopa_layer(640, 2300, 64, dtype="bf16", seed=67)
+    x = syn.tokens(2 * B, 640, dtype="bf16", seed=68)
+    ffn = make_ffn_ex(lw, flags)
+    y, c, m = run_tokens(ffn, x, B=B)
+    yref, z, n = reference_ex(lw, x, flags)
+    check(lw, x, y, c, m, ref=(yref, z, n), flags=flags)
+
+
+def test_union_skip_low_rank_workload(monkeypatch):
+    """The low-rank workload (D = 2560, H' = 9787, r = 400) at B = 4 and 12 through the union-skip kernels."""
+    monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
+    name = "lopa-bf16-D2560-H9787-r400-B1"
+    lw = syn.workload_layers(name, sets=1)[0]
+    ffn = make_ffn(lw)
+    for B in (4, 12):
+        x = syn.workload_tokens(name, B)
+        y, c, m = run_tokens(ffn, x, B=B)
+        check(lw, x, y, c, m)
+
+
 def test_union_skip_chosen_from_the_live_fraction():
     """With no environment override, a handle at the D = 4096 sweep shape picks the kernels of a
     4-token batch from its live-fraction estimate: the hint, then the counts sffn_active_counts
