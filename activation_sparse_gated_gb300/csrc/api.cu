@@ -138,6 +138,7 @@ int sync_and_check(sffn_s* h) {
     SFFN_CUDA(cudaMemset(h->ctrl, 0, sizeof(int) * CTRL_INTS));
     SFFN_CUDA(cudaMemset(h->yacc, 0, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * h->D));
     if (h->tickets) SFFN_CUDA(cudaMemset(h->tickets, 0, sizeof(int) * kTicketInts));
+    if (h->tacc) SFFN_CUDA(cudaMemset(h->tacc, 0, sizeof(float) * 128 * h->r));  // the t kernel's partial sums
     if (err & DEV_ERR_CHECK)
       return fail(SFFN_ERR_DEVICE, "a device-side bounds or alignment check failed (error word 0x%x); outputs "
                   "of the affected forward are invalid", err);
