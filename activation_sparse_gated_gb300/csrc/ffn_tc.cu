@@ -106,6 +106,11 @@ struct TcDownArgs {
 __host__ __device__ constexpr uint32_t gate_stage_bytes(int C, int NU, int NB) {
   return (uint32_t)C * 128u * (uint32_t)(2 * NU + NB);
 }
+// The epilogue's copy of the accumulator, transposed: [2 NB columns][TC_ACC_LD]
+// fp32 (128 TMEM lanes, padded so that every column starts 16-byte aligned and
+// a warp's 16-byte reads of neighbouring columns fall in different banks).
+constexpr int TC_ACC_LD = 132;
+__host__ __device__ constexpr size_t tc_acc_copy_bytes(int NB) { return (size_t)2 * NB * TC_ACC_LD * 4; }
 __host__ __device__ constexpr uint32_t down_chunk_bytes(int NB) { return 2u * TC_UCH * 128u + (uint32_t)NB * 128u; }
 
 // Bytes an MMA may read past the last A region of the last stage: it reads
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // kernel's blocks then never take the columns an earlier one still needs.
   if (tid == 0) pdl_launch_dependents();
   const bool fused = !LOPA && 2 * p.NU <= 128;
-  const int ncol = fused ? NB : 2 * NB, ldc = ncol + 1;  // epilogue copy of the accumulator
+  const int ncol = fused ? NB : 2 * NB;  // accumulator columns the epilogue copies
   float* s_acc = reinterpret_cast<float*>(sm);
   int stage_ok = 1;
 
@@ -363,12 +368,12 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
     if (stage_ok) {
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-      float* row = s_acc + (size_t)(32 * warp + lane) * ldc;
+      float* col = s_acc + 32 * warp + lane;  // transposed: column c at s_acc[c * TC_ACC_LD]
       for (int c0 = 0; c0 < ncol; c0 += 16) {
         float v[16];
         tmem_ld_sum(tl + c0, ncol, p.nacc, v);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) row[c0 + jj] = v[jj];
+        for (int jj = 0; jj < 16; ++jj) col[(size_t)(c0 + jj) * TC_ACC_LD] = v[jj];
       }
     }
   }
@@ -386,9 +391,8 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       for (int i = tid; i < p.B * nq; i += 256) {
         const int b = i / nq, r = 4 * (i - b * nq), u = u0 + r;
         if (u < p.H) {
-          const float* sa = s_acc + (size_t)r * ldc + NB + b;
           atomicAdd(reinterpret_cast<float4*>(p.tacc + (size_t)b * p.H + u),
-                    make_float4(sa[0], sa[ldc], sa[2 * ldc], sa[3 * ldc]));
+                    *reinterpret_cast<const float4*>(s_acc + (size_t)(NB + b) * TC_ACC_LD + r));
         }
       }
     }
@@ -433,29 +437,60 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       if (tid == 0) p.tickets[tile] = 0;
     }
   } else if (__syncthreads_and(stage_ok) && warp < 8) {
-    for (int r0 = 0; r0 < p.NU; r0 += 64) {
-      const int r = r0 + (tid & 63), g = tid >> 6;
-      const bool valid = r < p.NU && u0 + r < p.H;
-      const int u = u0 + r;
-      for (int b = g; b < p.B; b += 4) {
-        float z = valid ? s_acc[(size_t)r * ldc + b] : 0.f;
-        if (LOPA && valid && (p.flags & FLAG_TILED_G))  // (G x)_u = x_{u mod D}
-          z += __bfloat162float(__ushort_as_bfloat16(p.x[(size_t)b * p.D + u % p.D]));
-        const float pv = !valid ? 0.f : fused ? s_acc[(size_t)(p.NU + r) * ldc + b] : s_acc[(size_t)r * ldc + NB + b];
-        const float az = activation(p.act, z);
-        const bool lv = valid && is_live(az, p.thr);
-        const unsigned bal = __ballot_sync(0xffffffffu, lv);
-        if (lane == 0 && bal) atomicAdd(&s_cnt[b], __popc(bal));
-        if (valid) {
-          if (p.mask) p.mask[(size_t)b * p.H + u] = lv ? 1 : 0;
-          const float up = (p.flags & FLAG_DOUBLE_ACT) ? activation(p.act, pv) : pv;
-          const float hv = lv ? az * up : 0.f;
-          p.hbuf[(size_t)b * p.Hs + u] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+    // item = (token b, units 4q..4q+3): one 16-byte load of each operand from the
+    // transposed copy, one 8-byte store of h, the four mask bytes as one word where
+    // aligned, one count update.  (A loop over single units, with a ballot and a
+    // shared atomic per unit and token, was latency-bound: 16 rounds at 64 tokens.)
+    const int NU = p.NU, B = p.B, H = p.H, Hs = p.Hs, D = p.D, act = p.act, flags = p.flags;
+    const float thr = p.thr;
+    uint8_t* const mask = p.mask;
+    uint16_t* const hbuf = p.hbuf;
+    const uint16_t* const xin = p.x;
+    const int nq = NU / 4, items = B * nq;
+    for (int i = tid; i < items; i += 256) {
+      const int b = i / nq, r = 4 * (i - b * nq), u = u0 + r;
+      const float4 z4 = *reinterpret_cast<const float4*>(s_acc + (size_t)b * TC_ACC_LD + r);
+      const float4 p4 = *reinterpret_cast<const float4*>(
+          fused ? s_acc + (size_t)b * TC_ACC_LD + NU + r : s_acc + (size_t)(NB + b) * TC_ACC_LD + r);
+      const float zv[4] = {z4.x, z4.y, z4.z, z4.w}, pv[4] = {p4.x, p4.y, p4.z, p4.w};
+      uint32_t hw[2] = {0u, 0u}, mw = 0u;
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool valid = u + j < H;
+        float z = zv[j];
+        if (LOPA && valid && (flags & FLAG_TILED_G))  // (G x)_u = x_{u mod D}
+          z += __bfloat162float(__ushort_as_bfloat16(xin[(size_t)b * D + (u + j) % D]));
+        const float az = activation(act, z);
+        const bool lv = valid && is_live(az, thr);
+        const float up = (flags & FLAG_DOUBLE_ACT) ? activation(act, pv[j]) : pv[j];
+        const float hv = lv ? az * up : 0.f;
+        hw[j >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hv)) << (16 * (j & 1));
+        mw |= (uint32_t)lv << (8 * j);
+        n += lv;
+      }
+      if (n) atomicAdd(&s_cnt[b], n);
+      uint16_t* hp = hbuf + (size_t)b * Hs + u;  // 8-byte aligned: Hs and u are multiples of 4
+      uint8_t* mp = mask ? mask + (size_t)b * H + u : nullptr;
+      if (u + 3 < H) {
+        *reinterpret_cast<uint2*>(hp) = make_uint2(hw[0], hw[1]);
+        if (mp && (reinterpret_cast<uintptr_t>(mp) & 3u) == 0) {
+          *reinterpret_cast<uint32_t*>(mp) = mw;
+        } else if (mp) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mp[j] = (uint8_t)(mw >> (8 * j));
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (u + j < H) {
+            hp[j] = (uint16_t)(hw[j >> 1] >> (16 * (j & 1)));
+            if (mp) mp[j] = (uint8_t)(mw >> (8 * j));
+          }
       }
     }
     named_barrier(1, 256);
-    if (tid < p.B && s_cnt[tid]) atomicAdd(p.ctrl + CTRL_COUNT + tid, s_cnt[tid]);
+    if (tid < B && s_cnt[tid]) atomicAdd(p.ctrl + CTRL_COUNT + tid, s_cnt[tid]);
   }
   tc_fence_before();
   __syncthreads();
@@ -587,19 +622,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     const int d = d0 + 32 * warp + lane;
     const int used = min(p.nacc, (c1 - c0) * (TC_UCH / 16));  // accumulators that received a K step
-    const bool ok = nst > 0 && __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
-    if (ok) {
+    const bool mma_ok = nst > 0 && __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
+    // the slice's sums, transposed through the (drained) stages: s_y[token][TC_ACC_LD], then one
+    // 16-byte atomic per (token, four y values) instead of one 4-byte atomic per value
+    float* s_y = reinterpret_cast<float*>(sm);
+    if (mma_ok) {
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
-      float* ya = p.yacc + d;
       for (int cc = 0; cc < NB; cc += 16) {
         float v[16];
         tmem_ld_sum(tl + cc, NB, used, v);
-        if (d < p.D) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * p.D, v[jj]);
-        }
+        for (int jj = 0; jj < 16; ++jj) s_y[(size_t)(cc + jj) * TC_ACC_LD + 32 * warp + lane] = v[jj];
+      }
+    }
+    if (named_barrier_and(1, 128, mma_ok)) {  // all four warps copied their rows
+      const int B = p.B, D = p.D;
+      for (int i = tid; i < B * (TC_DTILE / 4); i += 128) {
+        const int b = i / (TC_DTILE / 4), j = 4 * (i - b * (TC_DTILE / 4));
+        if (d0 + j < D)  // D is a multiple of 8: the whole quad is in range
+          atomicAdd(reinterpret_cast<float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j),
+                    *reinterpret_cast<const float4*>(s_y + (size_t)b * TC_ACC_LD + j));
       }
     }
     // the last block of this y slice rounds the sum into y and clears the accumulator
@@ -767,9 +810,9 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     {  // a K-split block has few chunk groups: no more stages than it fills or the epilogue's copy needs
       const int kc_blk = (plan.KC + ksplit - 1) / ksplit;
       const int groups = g.NCZ + (kc_blk + g.C - 1) / g.C;
-      const size_t acc_copy = (size_t)128 * (2 * NB + 1) * 4;
+      const size_t acc_copy = tc_acc_copy_bytes(NB);
       const int need = (int)((acc_copy + stage_bytes(g.C) - 1) / stage_bytes(g.C));
-      g.NS = std::min(g.NS, std::max(2, std::max(groups, need)));
+      g.NS = std::max(std::min(g.NS, std::max(2, groups)), need);
     }
     while (g.NS > 2 && smem_bytes(g.C, g.NS) > cap) --g.NS;
     g.act = act;
@@ -790,8 +833,8 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     g.hbuf = buf.hbuf;
     g.timeout_ns = timeout_ns;
     smem = smem_bytes(g.C, g.NS);
-    // the epilogue stages the accumulator [128][2 NB + 1] fp32 over the pipeline stages
-    return (size_t)g.NS * stage_bytes(g.C) >= (size_t)128 * (2 * NB + 1) * 4 && smem <= cap;
+    // the epilogue stages the transposed accumulator (tc_acc_copy_bytes) over the pipeline stages
+    return (size_t)g.NS * stage_bytes(g.C) >= tc_acc_copy_bytes(NB) && smem <= cap;
   };
   const dim3 gb(TC_GATE_THREADS);
   cudaError_t e = cudaSuccess;
