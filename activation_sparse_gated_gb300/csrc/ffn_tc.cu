@@ -125,14 +125,18 @@ size_t gate_smem_bytes(int C, int MT, int NU, int NB, int NS) {
   return 1024 + (size_t)NS * gate_stage_bytes(C, NU, NB) + gate_slack_bytes(C, MT, NU, NB) + 8 * (2 * NS + 2) + 8 +
          4 * NB + 64;
 }
-// Low-rank stages: A regions [C][NU x 128 B] (U or W3 rows), then B regions
-// [C][2 NB x 128 B] (t_hi and t_lo, or x in the first half).  An MMA reads MT
-// rows from an A region's start; past the last one lie the B regions.
+// Low-rank stages: A regions [C][NU x 128 B] (U or W3 rows), then max(C, 2) B
+// regions of [NB x 128 B].  A group of W3 chunks fills C A regions and C B
+// regions (x); a group of U chunks fills lopa_zchunks(C) A regions and two B
+// regions per chunk (t_hi, t_lo): the t pair's rows do not take stage space
+// from the 40-odd W3 groups that follow.  An MMA reads MT rows from an A
+// region's start; past the last one lie the B regions.
+__host__ __device__ constexpr int lopa_zchunks(int C) { return C >= 2 ? C / 2 : 1; }
 __host__ __device__ constexpr uint32_t lopa_stage_bytes(int C, int NU, int NB) {
-  return (uint32_t)C * 128u * (uint32_t)(NU + 2 * NB);
+  return 128u * (uint32_t)(C * NU + (C >= 2 ? C : 2) * NB);
 }
 __host__ __device__ inline uint32_t lopa_slack_bytes(int C, int MT, int NU, int NB) {
-  const int over = (MT - NU) * 128 - C * 2 * NB * 128;
+  const int over = (MT - NU) * 128 - (C >= 2 ? C : 2) * NB * 128;
   return over > 0 ? (uint32_t)(over + 1023) / 1024 * 1024 : 0u;
 }
 size_t lopa_smem_bytes(int C, int MT, int NU, int NB, int NS) {
@@ -222,10 +226,12 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       if (LOPA) tma_prefetch_map(&mT);
     }
     if constexpr (LOPA) {
-      // groups [0, NCZ): U and t chunks (K over r); then W3 and x chunks (K over D)
+      // groups [0, NCZ): U and t chunks (K over r, CZ per group); then W3 and x chunks (K over D)
+      const int CZ = lopa_zchunks(C);
       auto zgroup = [&](int q) { return q < p.NCZ; };
-      auto kbase = [&](int q) { return zgroup(q) ? q * C : kc0 + (q - p.NCZ) * C; };
-      auto nchunks = [&](int q) { return zgroup(q) ? min(C, p.KCZ - q * C) : min(C, kc1 - kbase(q)); };
+      auto kbase = [&](int q) { return zgroup(q) ? q * CZ : kc0 + (q - p.NCZ) * C; };
+      auto nchunks = [&](int q) { return zgroup(q) ? min(CZ, p.KCZ - q * CZ) : min(C, kc1 - kbase(q)); };
+      auto breg = [&](int q, int c) { return C * wreg + (uint32_t)c * (zgroup(q) ? 2u : 1u) * xreg; };
       auto tx = [&](int q) { return (uint32_t)nchunks(q) * (wreg + (zgroup(q) ? 2u : 1u) * xreg); };
       const int npre = min(NS, NCG);
       for (int q = 0; q < npre; ++q) {  // weights first, before the dependency wait
@@ -238,8 +244,8 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
       pdl_wait();  // t and x come from earlier kernels
       for (int q = 0; q < npre; ++q)
         if (lane < nchunks(q))
-          tma_tile_2d(sm + (size_t)q * st_bytes + C * wreg + lane * 2 * xreg, zgroup(q) ? &mT : &mX,
-                      (kbase(q) + lane) * 64, 0, &full[q]);
+          tma_tile_2d(sm + (size_t)q * st_bytes + breg(q, lane), zgroup(q) ? &mT : &mX, (kbase(q) + lane) * 64, 0,
+                      &full[q]);
       int issued = npre;
       for (int q = npre; q < NCG; ++q) {
         const int s = q % NS;
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           if ((lane & 1) == 0)
             tma_tile_2d(st + c * wreg, zgroup(q) ? &mW1 : &mW3, kb, u0, &full[s]);
           else
-            tma_tile_2d(st + C * wreg + c * 2 * xreg, zgroup(q) ? &mT : &mX, kb, 0, &full[s]);
+            tma_tile_2d(st + breg(q, c), zgroup(q) ? &mT : &mX, kb, 0, &full[s]);
         }
         issued = q + 1;
       }
@@ -318,9 +324,10 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
           const uint64_t a0 = smem_desc(sa, 16, 1024, SMEM_LAYOUT_SW128);
           const uint64_t b0 = smem_desc(sa + C * wreg, 16, 1024, SMEM_LAYOUT_SW128);
           const bool zq = q < p.NCZ;
-          const int nc = zq ? min(C, p.KCZ - q * C) : min(C, kc1 - (kc0 + (q - p.NCZ) * C));
+          const int CZ = lopa_zchunks(C);
+          const int nc = zq ? min(CZ, p.KCZ - q * CZ) : min(C, kc1 - (kc0 + (q - p.NCZ) * C));
           for (int c = 0; c < nc; ++c) {
-            const uint64_t ac = a0 + ((c * wreg) >> 4), bc = b0 + ((c * 2 * xreg) >> 4);
+            const uint64_t ac = a0 + ((c * wreg) >> 4), bc = b0 + ((c * (zq ? 2 : 1) * xreg) >> 4);
             for (int kk = mw; kk < 4; kk += p.nacc) {
               if (zq) {  // z += U t_hi + U t_lo
                 tc_mma(da, ac + 2 * kk, bc + 2 * kk, idesc, started);
@@ -620,7 +627,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       p.counts[tid] = __ldcg(p.ctrl + CTRL_COUNT + tid);
       __stcg(p.ctrl + CTRL_COUNT + tid, 0);
     }
-    const int d = d0 + 32 * warp + lane;
     const int used = min(p.nacc, (c1 - c0) * (TC_UCH / 16));  // accumulators that received a K step
     const bool mma_ok = nst > 0 && __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
     // the slice's sums, transposed through the (drained) stages: s_y[token][TC_ACC_LD], then one
@@ -651,21 +657,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
     named_barrier(1, 128);
     if (*s_last) {
+      // 16-byte items (token b, four y values), sixteen loads in flight per thread before any
+      // store: the whole slice of up to 64 tokens in one round trip.  This pass ends the
+      // kernel, and the next kernel's dependency wait, for the slowest slice.
       __threadfence();
-      if (d < p.D) {
-        float* ya = p.yacc + d;
-        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + d;
-        for (int b0 = 0; b0 < p.B; b0 += 16) {  // 16 loads in flight, then the stores
-          float v[16];
+      const int B = p.B, D = p.D, items = B * (TC_DTILE / 4);
+      uint16_t* const y = static_cast<uint16_t*>(p.y);
+      for (int i0 = 0; i0 < items; i0 += 16 * 128) {
+        float4 v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            v[j] = b0 + j < p.B ? __ldcg(ya + (size_t)(b0 + j) * YACC_COPIES * p.D) : 0.f;
+        for (int e = 0; e < 16; ++e) {
+          const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
+          v[e] = i < items && d0 + j < D
+                     ? __ldcg(reinterpret_cast<const float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (b0 + j < p.B) {
-              __stcg(ya + (size_t)(b0 + j) * YACC_COPIES * p.D, 0.f);
-              y[(size_t)(b0 + j) * p.D] = __float2bfloat16_rn(v[j]);
-            }
+        for (int e = 0; e < 16; ++e) {
+          const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
+          if (i < items && d0 + j < D) {
+            __stcg(reinterpret_cast<float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j),
+                   make_float4(0.f, 0.f, 0.f, 0.f));
+            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].x)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].y)) << 16);
+            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].z)) |
+                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].w)) << 16);
+            *reinterpret_cast<uint2*>(y + (size_t)b * D + d0 + j) = make_uint2(lo, hi);
+          }
         }
       }
       if (tid == 0) p.tickets[dt] = 0;
@@ -800,11 +818,13 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     g.NB = NB;
     g.NU = NU;
     g.KC = plan.KC;
-    // four K chunks per stage; two once x makes up a large part of a stage (measured)
-    g.C = plan.gate_chunks > 0 ? plan.gate_chunks : (NB >= 48 ? 2 : 4);
+    // four K chunks per stage; for the standard gate two once x makes up a large part of a
+    // stage (measured: at 64 tokens 32.0 us per call with two, the low-rank gate 43.3 with four
+    // against 49.6 with two)
+    g.C = plan.gate_chunks > 0 ? plan.gate_chunks : (!lopa && NB >= 48 ? 2 : 4);
     while (g.C > 1 && smem_bytes(g.C, 2) > std::min(cap, (size_t)TC_SMEM_BUDGET)) g.C >>= 1;
     g.KCZ = with_u ? plan.KCZ : 0;
-    g.NCZ = (g.KCZ + g.C - 1) / g.C;
+    g.NCZ = (g.KCZ + lopa_zchunks(g.C) - 1) / lopa_zchunks(g.C);  // KCZ = 0 for the standard gate
     g.NCG = g.NCZ + (plan.KC + g.C - 1) / g.C;
     g.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, budget / stage_bytes(g.C)));
     {  // a K-split block has few chunk groups: no more stages than it fills or the epilogue's copy needs
