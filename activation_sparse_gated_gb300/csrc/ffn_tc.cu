@@ -94,8 +94,10 @@ struct TcGateArgs {
 
 struct TcDownArgs {
   int D, B, NB, nch, ndt, nsplit, NS, nacc;
+  int cluster;  // 1: the nsplit blocks of a slice are a cluster (block = dt * nsplit + sp) and sum in
+                // distributed shared memory; 0: block = sp * ndt + dt, fp32 atomics and a last block
   uint32_t tmem_cols;
-  float* yacc;  // [B_max * YACC_COPIES, D]; this path uses copy 0, zero between calls
+  float* yacc;  // [B_max * YACC_COPIES, D]; the atomic form uses copy 0, zero between calls
   void* y;      // [B, D] bf16
   int* ctrl;
   int* counts;  // [B] published live counts
@@ -525,7 +527,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int dt = blockIdx.x % p.ndt, sp = blockIdx.x / p.ndt, d0 = dt * TC_DTILE;
+  const bool clus = p.cluster != 0;
+  const int dt = clus ? blockIdx.x / p.nsplit : blockIdx.x % p.ndt;
+  const int sp = clus ? blockIdx.x % p.nsplit : blockIdx.x / p.ndt, d0 = dt * TC_DTILE;  // sp = rank in the cluster
   const int c0 = (int)((long long)sp * p.nch / p.nsplit), c1 = (int)((long long)(sp + 1) * p.nch / p.nsplit);
   const int nst = (c1 - c0 + TC_DC - 1) / TC_DC;
   int* err = p.ctrl + CTRL_ERR;
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int jj = 0; jj < 16; ++jj) s_y[(size_t)(cc + jj) * TC_ACC_LD + 32 * warp + lane] = v[jj];
       }
     }
-    if (named_barrier_and(1, 128, mma_ok)) {  // all four warps copied their rows
+    if (named_barrier_and(1, 128, mma_ok) && !clus) {  // all four warps copied their rows
       const int B = p.B, D = p.D;
       for (int i = tid; i < B * (TC_DTILE / 4); i += 128) {
         const int b = i / (TC_DTILE / 4), j = 4 * (i - b * (TC_DTILE / 4));
@@ -652,42 +656,84 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
     // the last block of this y slice rounds the sum into y and clears the accumulator
-    __threadfence();
-    named_barrier(1, 128);
-    if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
-    named_barrier(1, 128);
-    if (*s_last) {
-      // 16-byte items (token b, four y values), sixteen loads in flight per thread before any
-      // store: the whole slice of up to 64 tokens in one round trip.  This pass ends the
-      // kernel, and the next kernel's dependency wait, for the slowest slice.
+    if (!clus) {
       __threadfence();
-      const int B = p.B, D = p.D, items = B * (TC_DTILE / 4);
-      uint16_t* const y = static_cast<uint16_t*>(p.y);
-      for (int i0 = 0; i0 < items; i0 += 16 * 128) {
-        float4 v[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
-          v[e] = i < items && d0 + j < D
-                     ? __ldcg(reinterpret_cast<const float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
-          if (i < items && d0 + j < D) {
-            __stcg(reinterpret_cast<float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j),
-                   make_float4(0.f, 0.f, 0.f, 0.f));
-            const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].x)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].y)) << 16);
-            const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].z)) |
-                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].w)) << 16);
-            *reinterpret_cast<uint2*>(y + (size_t)b * D + d0 + j) = make_uint2(lo, hi);
+      named_barrier(1, 128);
+      if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
+      named_barrier(1, 128);
+      if (*s_last) {
+        // 16-byte items (token b, four y values), sixteen loads in flight per thread before any
+        // store: the whole slice of up to 64 tokens in one round trip.  This pass ends the
+        // kernel, and the next kernel's dependency wait, for the slowest slice.
+        __threadfence();
+        const int B = p.B, D = p.D, items = B * (TC_DTILE / 4);
+        uint16_t* const y = static_cast<uint16_t*>(p.y);
+        for (int i0 = 0; i0 < items; i0 += 16 * 128) {
+          float4 v[16];
+  #pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
+            v[e] = i < items && d0 + j < D
+                       ? __ldcg(reinterpret_cast<const float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+  #pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = i0 + e * 128 + tid, b = i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
+            if (i < items && d0 + j < D) {
+              __stcg(reinterpret_cast<float4*>(p.yacc + (size_t)b * YACC_COPIES * D + d0 + j),
+                     make_float4(0.f, 0.f, 0.f, 0.f));
+              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].x)) |
+                                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].y)) << 16);
+              const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[e].z)) |
+                                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[e].w)) << 16);
+              *reinterpret_cast<uint2*>(y + (size_t)b * D + d0 + j) = make_uint2(lo, hi);
+            }
           }
         }
+        if (tid == 0) p.tickets[dt] = 0;
       }
-      if (tid == 0) p.tickets[dt] = 0;
     }
+  }
+  if (clus) {
+    // every block's partial tile s_y[token][TC_ACC_LD] is complete once the cluster barrier
+    // passes; block sp then sums the nsplit tiles for its share of the tokens, 16-byte items
+    // (token b, four y values) read from each block's shared memory, and rounds them into y.
+    // The second barrier keeps every tile in place until all blocks have read it.
+    __syncwarp();
+    cluster_sync_all();
+    const int B = p.B, D = p.D, ns = p.nsplit;
+    const int b0 = (int)((long long)sp * B / ns), b1 = (int)((long long)(sp + 1) * B / ns);
+    const int items = (b1 - b0) * (TC_DTILE / 4);
+    const uint32_t s_y = smem_u32(sm);
+    uint16_t* const y = static_cast<uint16_t*>(p.y);
+    for (int i = tid; i < items; i += TC_THREADS) {
+      const int b = b0 + i / (TC_DTILE / 4), j = 4 * (i % (TC_DTILE / 4));
+      const uint32_t off = s_y + (uint32_t)((b * TC_ACC_LD + j) * 4);
+      float4 v[8];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r0 = 0; r0 < ns; r0 += 8) {  // up to eight loads in flight
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r0 + r < ns) v[r] = ld_cluster_f4(cluster_map(off, (uint32_t)(r0 + r)));
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r0 + r < ns) {
+            acc.x += v[r].x;
+            acc.y += v[r].y;
+            acc.z += v[r].z;
+            acc.w += v[r].w;
+          }
+      }
+      if (d0 + j < D) {  // D is a multiple of 8: the whole quad is in range
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+        *reinterpret_cast<uint2*>(y + (size_t)b * D + d0 + j) = make_uint2(lo, hi);
+      }
+    }
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -783,6 +829,45 @@ cudaError_t ffn_tc_prepare(size_t max_smem) {
     if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   if (!e) e = cudaFuncSetAttribute(ffn_tc_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
   return e;
+}
+
+namespace {
+// pipeline stages of the down kernel for NB padded tokens
+int down_stages(const TcPlan& plan, int NB, size_t max_smem) {
+  int ns = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.down_smem_budget / (TC_DC * down_chunk_bytes(NB))));
+  while (ns > 2 && down_smem_bytes(NB, ns) > max_smem) --ns;
+  return ns;
+}
+}  // namespace
+
+cudaError_t ffn_tc_plan_cluster(TcPlan& plan, size_t max_smem) {
+  plan.down_cluster = 0;
+  if (!plan.ok || plan.ndt < 1) return cudaSuccess;
+  size_t smem = 0;  // the largest down-kernel footprint of any batch size
+  for (int NB = 16; NB <= 128; NB += 16) smem = std::max(smem, down_smem_bytes(NB, down_stages(plan, NB, max_smem)));
+  for (int cs = std::min(std::min(8, plan.nch), plan.num_sms / plan.ndt); cs >= 2; --cs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.ndt * cs);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_tc_down_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();  // this size is not possible here: try a smaller one
+      continue;
+    }
+    if (n >= plan.ndt) {  // every slice's cluster resident at once: one wave
+      plan.down_cluster = cs;
+      break;
+    }
+  }
+  return cudaSuccess;
 }
 
 int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const void* x, void* y, int D, int H,
@@ -893,9 +978,9 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   d.NB = NB;
   d.nch = plan.nch;
   d.ndt = plan.ndt;
-  d.nsplit = plan.nsplit;
-  d.NS = (int)std::max<size_t>(2, std::min<size_t>(TC_NS_MAX, plan.down_smem_budget / (TC_DC * down_chunk_bytes(NB))));
-  while (d.NS > 2 && down_smem_bytes(NB, d.NS) > max_smem) --d.NS;
+  d.cluster = plan.down_cluster > 0 ? 1 : 0;
+  d.nsplit = d.cluster ? plan.down_cluster : plan.nsplit;
+  d.NS = down_stages(plan, NB, max_smem);
   d.nacc = NB <= 64 ? 4 : 2;  // a power of two, nacc * NB <= 256
   d.tmem_cols = tmem_cols_for(d.nacc * NB);
   d.y = y;
@@ -909,8 +994,12 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     *cuda_err = cudaErrorInvalidConfiguration;
     return 0;
   }
-  *cuda_err = launch_pdl(ffn_tc_down_kernel, dim3(plan.ndt * plan.nsplit), dim3(TC_THREADS), smem2, s, maps.w2,
-                         maps.h[NB / 16 - 1], d);
+  if (d.cluster)
+    *cuda_err = launch_pdl_cluster(ffn_tc_down_kernel, dim3(plan.ndt * d.nsplit), dim3(TC_THREADS), smem2, s,
+                                   (unsigned)d.nsplit, maps.w2, maps.h[NB / 16 - 1], d);
+  else
+    *cuda_err = launch_pdl(ffn_tc_down_kernel, dim3(plan.ndt * d.nsplit), dim3(TC_THREADS), smem2, s, maps.w2,
+                           maps.h[NB / 16 - 1], d);
   return 0;
 }
 

@@ -84,6 +84,9 @@ struct TcPlan {
   size_t gate_smem_budget = 0, down_smem_budget = 0;  // pipeline-stage bytes per block
   int gate_chunks = 0;                                // 64-wide K chunks per gate-up stage (0: 4)
   int tcg_acc = 1;  // union-skip gate kernel: TMEM accumulators per MMA warp
+  // streaming down kernel: blocks of an output slice that form a cluster and sum their partial
+  // tiles through distributed shared memory (0: nsplit blocks adding into fp32 accumulators)
+  int down_cluster = 0;
 };
 struct TcMaps {
   CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
@@ -114,6 +117,9 @@ size_t ffn_tc_hbuf_elems(const TcPlan& p);
 int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, const void* W3, const void* W2t,
                    uint16_t* hbuf, int D, int H);
 cudaError_t ffn_tc_prepare(size_t max_smem);
+// Chooses TcPlan::down_cluster: the largest cluster of 2..8 blocks per output slice whose
+// clusters are all resident at once (cudaOccupancyMaxActiveClusters); 0 when none is.
+cudaError_t ffn_tc_plan_cluster(TcPlan& plan, size_t max_smem);
 // Whole forward (y and counts written; no finalize kernel).  Low-rank gate:
 // tpair_ready says the caller already wrote the t pair (launch_lopa_t_pair);
 // otherwise the t kernel runs on the tensor cores first (t_only: and nothing
@@ -208,6 +214,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// The same with thread-block clusters of cluster_x blocks along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 

@@ -399,6 +399,33 @@ def test_tc_batched_shapes(D, H, B):
     check(lw, x, y, c, m)
 
 
+@pytest.mark.parametrize("reduction", ["cluster", "atomics"])
+@pytest.mark.parametrize("D,H,B", [(520, 1500, 17), (256, 10000, 64), (128, 3000, 128), (1152, 4096, 48)])
+def test_tc_down_reductions(monkeypatch, reduction, D, H, B):
+    """The down kernel sums the partial tiles of an output slice either in a thread-block cluster
+    (distributed shared memory; taken where every slice's cluster fits at once) or with fp32
+    atomics and a last block; both forms against the oracle, ragged D and H included."""
+    if reduction == "atomics":
+        monkeypatch.setenv("SFFN_TC_DOWN_CLUSTER", "0")
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=57)
+    x = syn.tokens(B, D, dtype="bf16", seed=58)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("reduction", ["cluster", "atomics"])
+def test_tc_down_reductions_lowrank_full_size(monkeypatch, reduction):
+    if reduction == "atomics":
+        monkeypatch.setenv("SFFN_TC_DOWN_CLUSTER", "0")
+    name = "lopa-bf16-D2560-H9787-r400-B1"
+    lw = syn.workload_layers(name, sets=1, gate="lopa")[0]
+    x = syn.workload_tokens(name, 64)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=64)
+    check(lw, x, y, c, m)
+
+
 @pytest.mark.parametrize("D,H", [(512, 2048), (384, 1000), (520, 1500), (256, 10000), (64, 151), (16, 40)])
 def test_union_gather_shapes(D, H):
     """B = 2 takes the union-gather kernel: slices of 16 and 72 units, ragged H, D off a multiple of 64
