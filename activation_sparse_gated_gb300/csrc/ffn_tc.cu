@@ -82,6 +82,8 @@ struct TcGateArgs {
   const uint16_t* x;     // [B, D] bf16 bits (the tiled identity G of the low-rank gate)
   uint16_t* tout;        // t kernel: the t pair [2 NB, H] (H = r) instead of h, masks and counts
   int ksplit;            // blocks per slice, each over a range of the K chunks (the t kernel; else 1)
+  int tcluster;          // t kernel: the ksplit blocks of a slice are a cluster and sum in distributed
+                         // shared memory (1), or add into tacc with a ticket and a last block (0)
   float* tacc;           // t kernel: [B, H] fp32 partial sums, zero between calls
   int* tickets;          // t kernel: [slices] blocks done, zero between calls
   float thr;  // live iff |A(z)| > thr
@@ -389,7 +391,53 @@ __global__ void __launch_bounds__(TC_GATE_THREADS, 1)
   // ---- epilogue on warps 0..7: thread (unit r, token group g = tid / 64) takes
   // tokens g, g + 4, ... (units in rounds of 64); a warp shares each token, so
   // the counts are ballots
-  if (LOPA && p.tout) {
+  if (LOPA && p.tout && p.tcluster) {
+    // t kernel, cluster form: the slice's ksplit blocks (cluster ranks = splits) hold their partials
+    // of T = V X^T in the transposed copy (columns NB + b); after the cluster barrier, block k sums
+    // the partials of its share of the (token, four rows) items through distributed shared memory
+    // and stores them as bf16 pairs (zero for the padding tokens, so the gate's MMA columns stay
+    // finite); the second barrier keeps every copy in place until all blocks have read it.
+    __syncwarp();
+    cluster_sync_all();
+    const int ks = p.ksplit, nq = p.NU / 4, total = NB * nq;
+    const int i0 = (int)((long long)split * total / ks), i1 = (int)((long long)(split + 1) * total / ks);
+    const uint32_t base = smem_u32(s_acc);
+    for (int i = i0 + tid; i < i1; i += TC_GATE_THREADS) {
+      const int b = i / nq, r = 4 * (i - b * nq), u = u0 + r;
+      if (u >= p.H) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (b < p.B) {
+        const uint32_t off = base + (uint32_t)(((NB + b) * TC_ACC_LD + r) * 4);
+        float4 v[8];
+        for (int q0 = 0; q0 < ks; q0 += 8) {  // up to eight loads in flight
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q0 + q < ks) v[q] = ld_cluster_f4(cluster_map(off, (uint32_t)(q0 + q)));
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q0 + q < ks) {
+              acc.x += v[q].x;
+              acc.y += v[q].y;
+              acc.z += v[q].z;
+              acc.w += v[q].w;
+            }
+        }
+      }
+      const float tv[4] = {acc.x, acc.y, acc.z, acc.w};
+      uint16_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(tv[k]);
+        hi[k] = __bfloat16_as_ushort(h);
+        lo[k] = __bfloat16_as_ushort(__float2bfloat16_rn(tv[k] - __bfloat162float(h)));
+      }
+      *reinterpret_cast<uint2*>(p.tout + (size_t)b * p.H + u) =
+          make_uint2(hi[0] | ((uint32_t)hi[1] << 16), hi[2] | ((uint32_t)hi[3] << 16));
+      *reinterpret_cast<uint2*>(p.tout + (size_t)(NB + b) * p.H + u) =
+          make_uint2(lo[0] | ((uint32_t)lo[1] << 16), lo[2] | ((uint32_t)lo[3] << 16));
+    }
+    cluster_sync_all();
+  } else if (LOPA && p.tout) {
     // t kernel: this block's partial of T = V X^T (its rows of V, its range of
     // D) into the fp32 sums; the last block of the row tile stores the sums as
     // bf16 pairs (zero rows for the padding tokens, so the gate's MMA columns
@@ -867,6 +915,29 @@ cudaError_t ffn_tc_plan_cluster(TcPlan& plan, size_t max_smem) {
       break;
     }
   }
+  plan.t_cluster = 0;
+  for (int cs = std::min(8, plan.KC); plan.r > 0 && cs >= 2; --cs) {  // the low-rank t kernel's K splits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.ntiles_t * cs);
+    cfg.blockDim = dim3(TC_GATE_THREADS);
+    cfg.dynamicSmemBytes = max_smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_tc_gateup_kernel<128, true>, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      continue;
+    }
+    if (n >= plan.ntiles_t) {
+      plan.t_cluster = cs;
+      break;
+    }
+  }
   return cudaSuccess;
 }
 
@@ -927,6 +998,7 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
     g.x = static_cast<const uint16_t*>(x);
     g.tout = tout;
     g.ksplit = ksplit;
+    g.tcluster = 0;
     g.tacc = buf.tacc;
     g.tickets = buf.tickets_t;
     const int cols = !lopa && 2 * NU <= 128 ? NB : 2 * NB;  // one accumulator
@@ -946,13 +1018,19 @@ int launch_ffn_tc(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, 
   if (lopa && !tpair_ready) {
     TcGateArgs gt;
     size_t smt = 0;
-    const int ksplit = std::max(1, std::min(plan.ksplit_t, plan.t_split_tokens / NB));
+    const bool tclus = plan.t_cluster > 0;
+    const int ksplit = tclus ? plan.t_cluster : std::max(1, std::min(plan.ksplit_t, plan.t_split_tokens / NB));
     if (!gate_args(plan.NUt, plan.r, false, buf.tpair, ksplit, gt, smt)) {
       *cuda_err = cudaErrorInvalidConfiguration;
       return 0;
     }
-    e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t * gt.ksplit), gb, smt, s, maps.v, maps.v,
-                   mx, mx, gt);
+    gt.tcluster = tclus ? 1 : 0;
+    if (tclus)
+      e = launch_pdl_cluster(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t * gt.ksplit), gb, smt, s,
+                             (unsigned)gt.ksplit, maps.v, maps.v, mx, mx, gt);
+    else
+      e = launch_pdl(ffn_tc_gateup_kernel<128, true>, dim3(plan.ntiles_t * gt.ksplit), gb, smt, s, maps.v, maps.v,
+                     mx, mx, gt);
     if (e || t_only) {
       *cuda_err = e;
       return 0;

@@ -87,6 +87,9 @@ struct TcPlan {
   // streaming down kernel: blocks of an output slice that form a cluster and sum their partial
   // tiles through distributed shared memory (0: nsplit blocks adding into fp32 accumulators)
   int down_cluster = 0;
+  // low-rank t kernel: K splits per slice that form a cluster and sum in distributed shared memory
+  // (0: ksplit_t splits adding into fp32 sums with a ticket and a last block)
+  int t_cluster = 0;
 };
 struct TcMaps {
   CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
@@ -117,8 +120,9 @@ size_t ffn_tc_hbuf_elems(const TcPlan& p);
 int encode_tc_maps(TcMaps* m, const TcPlan& p, const void* W1, const void* V, const void* W3, const void* W2t,
                    uint16_t* hbuf, int D, int H);
 cudaError_t ffn_tc_prepare(size_t max_smem);
-// Chooses TcPlan::down_cluster: the largest cluster of 2..8 blocks per output slice whose
-// clusters are all resident at once (cudaOccupancyMaxActiveClusters); 0 when none is.
+// Chooses TcPlan::down_cluster (and, for a low-rank gate, TcPlan::t_cluster): the largest cluster
+// of 2..8 blocks per slice whose clusters are all resident at once (cudaOccupancyMaxActiveClusters);
+// 0 when none is.
 cudaError_t ffn_tc_plan_cluster(TcPlan& plan, size_t max_smem);
 // Whole forward (y and counts written; no finalize kernel).  Low-rank gate:
 // tpair_ready says the caller already wrote the t pair (launch_lopa_t_pair);

@@ -416,8 +416,10 @@ def test_tc_down_reductions(monkeypatch, reduction, D, H, B):
 
 @pytest.mark.parametrize("reduction", ["cluster", "atomics"])
 def test_tc_down_reductions_lowrank_full_size(monkeypatch, reduction):
+    """Both reductions of the down kernel and of the low-rank t kernel's K splits, at full size."""
     if reduction == "atomics":
         monkeypatch.setenv("SFFN_TC_DOWN_CLUSTER", "0")
+        monkeypatch.setenv("SFFN_TC_T_CLUSTER", "0")
     name = "lopa-bf16-D2560-H9787-r400-B1"
     lw = syn.workload_layers(name, sets=1, gate="lopa")[0]
     x = syn.workload_tokens(name, 64)
@@ -657,6 +659,20 @@ def test_batched_lopa_tensor_cores(D, H, r, B):
     cores above), U t_hi + U t_lo in one accumulator."""
     lw = syn.lopa_layer(D, H, r, dtype="bf16", seed=D + r)
     x = syn.tokens(B, D, dtype="bf16", seed=H)
+    ffn = make_ffn(lw)
+    y, c, m = run_tokens(ffn, x, B=B)
+    check(lw, x, y, c, m)
+
+
+@pytest.mark.parametrize("D,H,r,B", [(520, 1500, 40, 5), (512, 3000, 400, 33), (384, 1000, 8, 128),
+                                     (1024, 4000, 128, 12)])
+def test_lowrank_t_kernel_atomic_form(monkeypatch, D, H, r, B):
+    """The t kernel's K splits summed with fp32 atomics, a ticket and a last block (the form taken
+    where its clusters do not fit), against the oracle."""
+    monkeypatch.setenv("SFFN_TC_T_CLUSTER", "0")
+    monkeypatch.setenv("SFFN_TC_T_CUDA_MAX_B", "0")
+    lw = syn.lopa_layer(D, H, r, dtype="bf16", seed=D + r + 1)
+    x = syn.tokens(B, D, dtype="bf16", seed=H + 1)
     ffn = make_ffn(lw)
     y, c, m = run_tokens(ffn, x, B=B)
     check(lw, x, y, c, m)
