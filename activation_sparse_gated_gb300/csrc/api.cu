@@ -343,12 +343,14 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
         return bail(SFFN_ERR_CUDA, "cudaMemset", e);
       if ((e = ffn_tc_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
       if ((e = ffn_tc_plan_cluster(h->tc, h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaOccupancyMaxActiveClusters", e);
-      if (const char* env = std::getenv("SFFN_TC_DOWN_CLUSTER"))
-        if (std::atoi(env) == 0) h->tc.down_cluster = 0;
-      if (const char* env = std::getenv("SFFN_TC_T_CLUSTER"))
-        if (std::atoi(env) == 0) h->tc.t_cluster = 0;
       if ((e = ffn_tcu_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
       if ((e = ffn_tcg_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
+      if ((e = ffn_tcg_plan_cluster(h->tc, h->max_smem)))
+        return bail(SFFN_ERR_CUDA, "cudaOccupancyMaxActiveClusters", e);
+      if (const char* env = std::getenv("SFFN_TC_DOWN_CLUSTER"))
+        if (std::atoi(env) == 0) h->tc.down_cluster = h->tc.tcg_down_cluster = 0;
+      if (const char* env = std::getenv("SFFN_TC_T_CLUSTER"))
+        if (std::atoi(env) == 0) h->tc.t_cluster = 0;
       if (const char* env = std::getenv("SFFN_TCG_ACC")) h->tc.tcg_acc = std::max(1, std::min(4, std::atoi(env)));
       if (const char* env = std::getenv("SFFN_TCG_MAX_BATCH"))
         h->tcg_force = std::max(0, std::min(TCG_MAX_BATCH, std::atoi(env)));

@@ -57,6 +57,7 @@ constexpr int DT = 128;         // y values per down-kernel block (MMA M)
 constexpr int UCH = 64;         // union positions per down-kernel K chunk
 constexpr int NS_MAX = 8;
 constexpr int DRING_MAX = 16;   // down kernel: ring slots
+constexpr int Y_LD = 132;       // down kernel, cluster form: the partial tile [token][Y_LD] fp32
 constexpr size_t SMEM_BUDGET = 200 * 1024;
 
 struct GateArgs {
@@ -78,6 +79,8 @@ struct GateArgs {
 
 struct DownArgs {
   int D, H, B, NB, ndt, nsplit, RD, nacc, Hs, maxpos;
+  int cluster;           // 1: the nsplit blocks of a y slice are a cluster (block = dt * nsplit + sp) and
+                         // sum in distributed shared memory; 0: block = sp * ndt + dt, atomics, last block
   uint32_t tmem_cols;
   const uint16_t* W2t;   // [H, D] bf16 (gathered row segments)
   const uint16_t* hbuf;  // the gate kernel's h (the union's last chunk is read directly)
@@ -511,7 +514,9 @@ __global__ void __launch_bounds__(D_THREADS, 1)
   int* s_last = reinterpret_cast<int*>(tslot + 2);
   int* s_units = s_last + 2;  // [maxpos] the units of this block's union positions
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int dt = blockIdx.x % p.ndt, sp = blockIdx.x / p.ndt, d0 = dt * DT;
+  const bool clus = p.cluster != 0;
+  const int dt = clus ? blockIdx.x / p.nsplit : blockIdx.x % p.ndt;
+  const int sp = clus ? blockIdx.x % p.nsplit : blockIdx.x / p.ndt, d0 = dt * DT;  // sp = rank in the cluster
   const int D = p.D;
   int* err = p.ctrl + CTRL_ERR;
 
@@ -663,6 +668,9 @@ __global__ void __launch_bounds__(D_THREADS, 1)
     const int d = d0 + 32 * warp + lane;
     const int used = min(p.nacc, nch * (UCH / 16));  // accumulators that received a K step
     const bool okd = nch > 0 && __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, err, p.timeout_ns));
+    // cluster form: the partial tile goes to the drained ring token-major (zero for a block with no
+    // union chunk), for the reduction after the warp roles end
+    float* s_y = reinterpret_cast<float*>(sm) + 32 * warp + lane;
     if (okd) {
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
@@ -670,37 +678,83 @@ __global__ void __launch_bounds__(D_THREADS, 1)
       for (int cc = 0; cc < NB; cc += 16) {
         float v[16];
         tmem_ld_sum(tl + cc, NB, used, v);
-        if (d < D) {
+        if (clus) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) s_y[(size_t)(cc + jj) * Y_LD] = v[jj];
+        } else if (d < D) {
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj)
             if (cc + jj < p.B) atomicAdd(ya + (size_t)(cc + jj) * YACC_COPIES * D, v[jj]);
         }
       }
+    } else if (clus && nch == 0) {
+      for (int c = 0; c < NB; ++c) s_y[(size_t)c * Y_LD] = 0.f;
     }
     // the last block of this y slice rounds the sum into y and clears the accumulator
-    __threadfence();
-    named_barrier(1, 128);
-    if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
-    named_barrier(1, 128);
-    if (*s_last) {
+    if (!clus) {
       __threadfence();
-      if (d < D) {
-        float* ya = p.yacc + d;
-        __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + d;
-        for (int b0 = 0; b0 < p.B; b0 += 16) {  // 16 loads in flight, then the stores
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = b0 + j < p.B ? __ldcg(ya + (size_t)(b0 + j) * YACC_COPIES * D) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (b0 + j < p.B) {
-              __stcg(ya + (size_t)(b0 + j) * YACC_COPIES * D, 0.f);
-              y[(size_t)(b0 + j) * D] = __float2bfloat16_rn(v[j]);
-            }
+      named_barrier(1, 128);
+      if (tid == 0) *s_last = atomicAdd(p.tickets + dt, 1) == p.nsplit - 1;
+      named_barrier(1, 128);
+      if (*s_last) {
+        __threadfence();
+        if (d < D) {
+          float* ya = p.yacc + d;
+          __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.y) + d;
+          for (int b0 = 0; b0 < p.B; b0 += 16) {  // 16 loads in flight, then the stores
+            float v[16];
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = b0 + j < p.B ? __ldcg(ya + (size_t)(b0 + j) * YACC_COPIES * D) : 0.f;
+  #pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (b0 + j < p.B) {
+                __stcg(ya + (size_t)(b0 + j) * YACC_COPIES * D, 0.f);
+                y[(size_t)(b0 + j) * D] = __float2bfloat16_rn(v[j]);
+              }
+          }
         }
+        if (tid == 0) p.tickets[dt] = 0;
       }
-      if (tid == 0) p.tickets[dt] = 0;
     }
+  }
+  if (clus) {
+    // after the cluster barrier block sp sums the slice's nsplit tiles for its share of the tokens
+    // (16-byte items read through distributed shared memory) and rounds them into y; the second
+    // barrier keeps every tile in place until all blocks have read it
+    __syncwarp();
+    cluster_sync_all();
+    const int B = p.B, ns = p.nsplit;
+    const int b0 = (int)((long long)sp * B / ns), b1 = (int)((long long)(sp + 1) * B / ns);
+    const int items = (b1 - b0) * (DT / 4);
+    const uint32_t base = smem_u32(sm);
+    uint16_t* const yo = static_cast<uint16_t*>(p.y);
+    for (int i = tid; i < items; i += D_THREADS) {
+      const int b = b0 + i / (DT / 4), j = 4 * (i % (DT / 4));
+      const uint32_t off = base + (uint32_t)((b * Y_LD + j) * 4);
+      float4 v[8];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r0 = 0; r0 < ns; r0 += 8) {  // up to eight loads in flight
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r0 + r < ns) v[r] = ld_cluster_f4(cluster_map(off, (uint32_t)(r0 + r)));
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+          if (r0 + r < ns) {
+            acc.x += v[r].x;
+            acc.y += v[r].y;
+            acc.z += v[r].z;
+            acc.w += v[r].w;
+          }
+      }
+      if (d0 + j < D) {  // D is a multiple of 8: the whole quad is in range
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+        *reinterpret_cast<uint2*>(yo + (size_t)b * D + d0 + j) = make_uint2(lo, hi);
+      }
+    }
+    cluster_sync_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -722,6 +776,34 @@ uint32_t tmem_cols_pow2(int n) {
 }
 
 }  // namespace
+
+cudaError_t ffn_tcg_plan_cluster(TcPlan& plan, size_t max_smem) {
+  plan.tcg_down_cluster = 0;
+  if (!plan.ok || plan.ndt < 1) return cudaSuccess;
+  for (int cs = std::min(std::min(8, plan.nch), plan.num_sms / plan.ndt); cs >= 2; --cs) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.ndt * cs);
+    cfg.blockDim = dim3(D_THREADS);
+    cfg.dynamicSmemBytes = max_smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = (unsigned)cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_tcg_down_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      continue;
+    }
+    if (n >= plan.ndt) {
+      plan.tcg_down_cluster = cs;
+      break;
+    }
+  }
+  return cudaSuccess;
+}
 
 cudaError_t ffn_tcg_prepare(size_t max_smem) {
   cudaError_t e =
@@ -805,9 +887,10 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
   d.B = B;
   d.NB = NB;
   d.ndt = plan.ndt;
-  d.nsplit = plan.nsplit;
+  d.cluster = plan.tcg_down_cluster > 0 ? 1 : 0;
+  d.nsplit = d.cluster ? plan.tcg_down_cluster : plan.nsplit;
   d.Hs = plan.Hs;
-  d.maxpos = (plan.nch + plan.nsplit - 1) / plan.nsplit * UCH;  // the union has at most nch chunks
+  d.maxpos = (plan.nch + d.nsplit - 1) / d.nsplit * UCH;  // the union has at most nch chunks
   d.RD = 2;
   while (d.RD < DRING_MAX && d.RD * UCH < d.maxpos && d_smem_bytes(NB, d.RD + 1, d.maxpos) <= budget) ++d.RD;
   d.nacc = 8;  // a power of two, nacc * NB <= 256 TMEM columns (NB <= 32)
@@ -828,8 +911,12 @@ int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf,
     *cuda_err = cudaErrorInvalidConfiguration;
     return 0;
   }
-  *cuda_err = launch_pdl(ffn_tcg_down_kernel, dim3(plan.ndt * plan.nsplit), dim3(D_THREADS), smem2, s,
-                         maps.h[NB / 16 - 1], d);
+  if (d.cluster)
+    *cuda_err = launch_pdl_cluster(ffn_tcg_down_kernel, dim3(plan.ndt * d.nsplit), dim3(D_THREADS), smem2, s,
+                                   (unsigned)d.nsplit, maps.h[NB / 16 - 1], d);
+  else
+    *cuda_err = launch_pdl(ffn_tcg_down_kernel, dim3(plan.ndt * d.nsplit), dim3(D_THREADS), smem2, s,
+                           maps.h[NB / 16 - 1], d);
   return 0;
 }
 

@@ -90,6 +90,7 @@ struct TcPlan {
   // low-rank t kernel: K splits per slice that form a cluster and sum in distributed shared memory
   // (0: ksplit_t splits adding into fp32 sums with a ticket and a last block)
   int t_cluster = 0;
+  int tcg_down_cluster = 0;  // union-skip down kernel: blocks per output slice in a cluster (0: atomics)
 };
 struct TcMaps {
   CUtensorMap w1, w3;  // W1 [H, D] (or U [H, r]), W3 [H, D]: boxes of 64 columns x NU rows
@@ -159,6 +160,8 @@ struct TcgBuffers {
   int* dticket;  // [1] down blocks done, zero between calls
 };
 cudaError_t ffn_tcg_prepare(size_t max_smem);
+// Chooses TcPlan::tcg_down_cluster as ffn_tc_plan_cluster does for the streaming down kernel.
+cudaError_t ffn_tcg_plan_cluster(TcPlan& plan, size_t max_smem);
 int launch_ffn_tcg(const TcPlan& plan, const TcMaps& maps, const TcBuffers& buf, const TcgBuffers& ub, const void* W3,
                    const void* W2t, const void* x, void* y, int D, int H, int B, int act, int flags, float thr,
                    unsigned long long timeout_ns, size_t max_smem, cudaStream_t s, cudaError_t* cuda_err);

@@ -490,18 +490,26 @@ def test_union_skip_kernels(monkeypatch, B, act, thr, flags):
     (256, 20000, 12),   # slices of 128 units, more slices than SMs
     (1032, 777, 4),
 ])
-def test_union_skip_shapes(monkeypatch, D, H, B):
+@pytest.mark.parametrize("reduction", ["cluster", "atomics"])
+def test_union_skip_shapes(monkeypatch, D, H, B, reduction):
+    """Every shape with both reductions of the down kernel (a cluster summing in distributed shared
+    memory where the clusters fit; fp32 atomics and a last block)."""
     monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")  # read when a handle is created
+    if reduction == "atomics":
+        monkeypatch.setenv("SFFN_TC_DOWN_CLUSTER", "0")
     lw = syn.standard_layer(D, H, dtype="bf16", seed=D + 3 * H, shift=-0.8)
     x = syn.tokens(2 * B, D, dtype="bf16", seed=D + 1)
     y, c, m = run_tokens(make_ffn(lw), x, B=B)
     check(lw, x, y, c, m)
 
 
+@pytest.mark.parametrize("reduction", ["cluster", "atomics"])
 @pytest.mark.parametrize("shift", [+30.0, -30.0])
-def test_union_skip_every_unit_and_none(monkeypatch, shift):
+def test_union_skip_every_unit_and_none(monkeypatch, shift, reduction):
     """A union of all H units (its last chunk ragged) and an empty one (y == 0 exactly)."""
     monkeypatch.setenv("SFFN_TCG_MAX_BATCH", "16")
+    if reduction == "atomics":
+        monkeypatch.setenv("SFFN_TC_DOWN_CLUSTER", "0")
     lw = syn.standard_layer(512, 3001, dtype="bf16", seed=63, shift=shift)
     x = syn.tokens(8, 512, dtype="bf16", seed=64)
     y, c, m = run_tokens(make_ffn(lw), x, B=4)
