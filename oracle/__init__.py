@@ -57,6 +57,8 @@ def _bind(path):
     lib.oracle_num_threads.argtypes = []
     lib.oracle_quantize_rows.restype = ip
     lib.oracle_quantize_rows.argtypes = [ip, ip, vp, vp, vp]
+    lib.oracle_quantize_rows_q.restype = ip
+    lib.oracle_quantize_rows_q.argtypes = [ip, ip, ip, vp, vp, vp]
     lib.oracle_ffn_dense_q8.restype = ip
     lib.oracle_ffn_dense_q8.argtypes = [ip] * 5 + [ctypes.c_double] + [vp] * 10
     return lib
@@ -93,8 +95,8 @@ class Variant:
                      lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps,
                      thr=thr)
 
-    def quantize_rows(self, W):
-        return _quantize_rows(W, self._lib)
+    def quantize_rows(self, W, qmax=127):
+        return _quantize_rows(W, self._lib, qmax)
 
     def ffn_dense_q8(self, D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0):
         return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, self._lib)
@@ -178,20 +180,21 @@ def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNO
 
 # Weight-only int8 ("Model Casting and Low-Parameter Gating", appendix Table 17):
 # symmetric per-output-channel scales, codes decided in binary32 (see the C file).
-def _quantize_rows(W, lib=None):
+def _quantize_rows(W, lib=None, qmax=127):
     W = np.ascontiguousarray(W, dtype=np.float32)
     rows, cols = W.shape
     q = np.zeros((rows, cols), dtype=np.int8)
     s = np.zeros(rows, dtype=np.float32)
-    rc = (lib or _load()).oracle_quantize_rows(rows, cols, _ptr(W), _ptr(q), _ptr(s))
+    rc = (lib or _load()).oracle_quantize_rows_q(rows, cols, int(qmax), _ptr(W), _ptr(q), _ptr(s))
     if rc != 0:
-        raise RuntimeError(f"oracle_quantize_rows failed with code {rc}")
+        raise RuntimeError(f"oracle_quantize_rows_q failed with code {rc}")
     return q, s
 
 
-def quantize_rows(W):
-    """Per-row int8 codes and fp32 scales of a float32 matrix: (q[rows, cols] int8, s[rows] f32)."""
-    return _quantize_rows(W)
+def quantize_rows(W, qmax=127):
+    """Per-row codes in [-qmax, qmax] (127: int8 weights, 7: int4) and fp32 scales of a float32
+    matrix: (q[rows, cols] int8, s[rows] f32)."""
+    return _quantize_rows(W, qmax=qmax)
 
 
 def _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, lib=None):

@@ -56,7 +56,9 @@
  * round-half-to-even(w / s) clamped to [-127, 127], both decided in binary32
  * (the precision of the weights being quantised); an all-zero row has s = 0
  * and codes 0.  The forward is the definition above with every weight replaced
- * by its dequantised value q * s (exact in double); x is bf16.
+ * by its dequantised value q * s (exact in double); x is bf16.  Weight-only
+ * int4 takes the same convention with 7 in place of 127 (codes in [-7, 7]);
+ * the "_q8" forward serves it unchanged, its codes being small integers.
  *
  * Portable C99 + OpenMP; no SIMD intrinsics, no -ffast-math.
  */
@@ -336,9 +338,11 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
 
 /* ------------------------------------------------------------------------ int8 */
 
-/* Per-row symmetric int8 quantisation of W[rows, cols] (binary32 decisions). */
-int oracle_quantize_rows(int rows, int cols, const float* W, int8_t* q, float* s) {
-  if (rows < 0 || cols <= 0) return -1;
+/* Per-row symmetric quantisation of W[rows, cols] to codes in [-qmax, qmax]
+ * (binary32 decisions): qmax = 127 for int8 weights, 7 for int4. */
+int oracle_quantize_rows_q(int rows, int cols, int qmax, const float* W, int8_t* q, float* s) {
+  if (rows < 0 || cols <= 0 || qmax < 1 || qmax > 127) return -1;
+  const float qm = (float)qmax;
   for (int i = 0; i < rows; ++i) {
     const float* w = W + (size_t)i * cols;
     float amax = 0.0f;
@@ -346,19 +350,24 @@ int oracle_quantize_rows(int rows, int cols, const float* W, int8_t* q, float* s
       const float a = fabsf(w[j]);
       if (a > amax) amax = a;
     }
-    const float sc = amax / 127.0f;
+    const float sc = amax / qm;
     s[i] = sc;
     for (int j = 0; j < cols; ++j) {
       float v = 0.0f;
       if (sc > 0.0f) {
         v = rintf(w[j] / sc); /* default rounding mode: to nearest, ties to even */
-        if (v > 127.0f) v = 127.0f;
-        if (v < -127.0f) v = -127.0f;
+        if (v > qm) v = qm;
+        if (v < -qm) v = -qm;
       }
       q[(size_t)i * cols + j] = (int8_t)v;
     }
   }
   return 0;
+}
+
+/* Per-row symmetric int8 quantisation of W[rows, cols] (binary32 decisions). */
+int oracle_quantize_rows(int rows, int cols, const float* W, int8_t* q, float* s) {
+  return oracle_quantize_rows_q(rows, cols, 127, W, q, s);
 }
 
 /* row i of a quantised matrix, dequantised: q[i, j] * s[i] (exact in double) */

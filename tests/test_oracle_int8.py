@@ -99,3 +99,64 @@ def test_q8_rejects_low_rank_flags():
     x = bf16_bits(np.ones((1, 8), dtype=np.float32))
     with pytest.raises(RuntimeError):
         oracle.ffn_dense_q8(8, 4, RELU, oracle.FLAG_TILED_G, q, s, q, s, q.T.copy(), np.ones(8, np.float32), x)
+
+
+# Weight-only int4 ("Model Casting and Low-Parameter Gating", appendix Table 17, quantises the cast
+# models to int4 too): the same convention with 7 in place of 127, codes in [-7, 7].
+
+def test_quantize_int4_hand_worked():
+    W = np.array([[7.0, -3.5, 2.5, 0.5, -1.5, 0.0],       # s = 1: ties go to the even code
+                  [0.0, 0.0, 0.0, 0.0, 0.0, 0.0],         # all zero: s = 0, codes 0
+                  [-14.0, 3.0, 5.0, 1.0, 13.0, -9.0]],    # s = 2: 1.5 -> 2, 2.5 -> 2, 0.5 -> 0, 6.5 -> 6, -4.5 -> -4
+                 dtype=np.float32)
+    q, s = oracle.quantize_rows(W, qmax=7)
+    assert s.tolist() == [1.0, 0.0, 2.0]
+    assert q.tolist() == [[7, -4, 2, 0, -2, 0], [0] * 6, [-7, 2, 2, 0, 6, -4]]
+
+
+def test_quantize_int4_invariants():
+    rng = np.random.default_rng(4)
+    W = (rng.standard_normal((48, 256)) * rng.uniform(0.01, 10.0, size=(48, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows(W, qmax=7)
+    assert (np.abs(q.astype(np.int32)) <= 7).all()
+    j = np.abs(W).argmax(axis=1)
+    assert (np.abs(q[np.arange(48), j].astype(np.int32)) == 7).all()
+    err = np.abs(W.astype(np.float64) - q.astype(np.float64) * s[:, None].astype(np.float64))
+    assert (err <= s[:, None].astype(np.float64) * (0.5 + 1e-5)).all()
+    assert (q.astype(np.int32) * np.sign(W) >= 0).all()
+    # an int8 grid is 127 / 7 times finer: the int4 error bound is the looser one
+    q8, s8 = oracle.quantize_rows(W)
+    np.testing.assert_allclose(s, s8 * (127.0 / 7.0), rtol=1e-6)
+
+
+def test_quantize_rejects_a_code_range_outside_int8():
+    W = np.ones((2, 4), dtype=np.float32)
+    for qmax in (0, 128):
+        with pytest.raises(RuntimeError):
+            oracle.quantize_rows(W, qmax=qmax)
+
+
+@pytest.mark.parametrize("act", [RELU, SILU])
+def test_int4_codes_through_the_q8_forward_equal_the_float_oracle(act):
+    """int4 codes are small integers; with power-of-two scales q * s is exact, so the _q8 forward on
+    them must equal the pinned float32 oracle on the dequantised weights."""
+    D, H, B = 32, 70, 3
+    rng = np.random.default_rng(5)
+
+    def mat(rows, cols):
+        q = rng.integers(-7, 8, size=(rows, cols)).astype(np.int8)
+        q[np.arange(rows), rng.integers(0, cols, size=rows)] = rng.choice([-7, 7], size=rows)
+        s = np.ldexp(1.0, -rng.integers(1, 5, size=rows)).astype(np.float32)
+        return q, s, (q.astype(np.float32) * s[:, None]).astype(np.float32)
+
+    (q1, s1, W1), (q3, s3, W3), (q2, s2, W2) = mat(H, D), mat(H, D), mat(D, H)
+    for q, s, W in ((q1, s1, W1), (q3, s3, W3), (q2, s2, W2)):
+        qq, ss = oracle.quantize_rows(W, qmax=7)
+        assert np.array_equal(qq, q) and np.array_equal(ss, s)
+    xf = torch.from_numpy(rng.standard_normal((B, D)).astype(np.float32)).bfloat16().float().numpy()
+    thr = 0.05 if act == SILU else 0.0
+    y4, z4, n4 = oracle.ffn_dense_q8(D, H, act, 0, q1, s1, q3, s3, q2, s2, bf16_bits(xf), thr=thr)
+    yf, zf, nf = oracle.ffn_dense_ex(D, H, 0, act, F32, 0, W1, None, None, W3, W2, xf, thr=thr)
+    np.testing.assert_allclose(z4, zf, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(y4, yf, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(n4, nf)
