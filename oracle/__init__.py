@@ -59,8 +59,12 @@ def _bind(path):
     lib.oracle_quantize_rows.argtypes = [ip, ip, vp, vp, vp]
     lib.oracle_quantize_rows_q.restype = ip
     lib.oracle_quantize_rows_q.argtypes = [ip, ip, ip, vp, vp, vp]
+    lib.oracle_quantize_rows_g.restype = ip
+    lib.oracle_quantize_rows_g.argtypes = [ip, ip, ip, ip, vp, vp, vp]
     lib.oracle_ffn_dense_q8.restype = ip
     lib.oracle_ffn_dense_q8.argtypes = [ip] * 5 + [ctypes.c_double] + [vp] * 10
+    lib.oracle_ffn_dense_qg.restype = ip
+    lib.oracle_ffn_dense_qg.argtypes = [ip] * 5 + [ctypes.c_double, ip] + [vp] * 10
     return lib
 
 
@@ -95,11 +99,11 @@ class Variant:
                      lambda B: np.zeros((B, H), dtype=np.float64), lib=self._lib, flags=flags, eps=eps,
                      thr=thr)
 
-    def quantize_rows(self, W, qmax=127):
-        return _quantize_rows(W, self._lib, qmax)
+    def quantize_rows(self, W, qmax=127, group=None):
+        return _quantize_rows(W, self._lib, qmax, group)
 
-    def ffn_dense_q8(self, D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0):
-        return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, self._lib)
+    def ffn_dense_q8(self, D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, group=None):
+        return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, self._lib, group)
 
 
 def num_threads() -> int:
@@ -180,42 +184,61 @@ def ffn_gate_first_ex(D, H, r, act, dtype, flags, W1, U, V, W3, W2, x, eps=RMSNO
 
 # Weight-only int8 ("Model Casting and Low-Parameter Gating", appendix Table 17):
 # symmetric per-output-channel scales, codes decided in binary32 (see the C file).
-def _quantize_rows(W, lib=None, qmax=127):
+def _quantize_rows(W, lib=None, qmax=127, group=None):
     W = np.ascontiguousarray(W, dtype=np.float32)
     rows, cols = W.shape
     q = np.zeros((rows, cols), dtype=np.int8)
-    s = np.zeros(rows, dtype=np.float32)
-    rc = (lib or _load()).oracle_quantize_rows_q(rows, cols, int(qmax), _ptr(W), _ptr(q), _ptr(s))
+    if group is None:
+        s = np.zeros(rows, dtype=np.float32)
+        rc = (lib or _load()).oracle_quantize_rows_q(rows, cols, int(qmax), _ptr(W), _ptr(q), _ptr(s))
+    else:
+        s = np.zeros((rows, cols // group if group > 0 else 0), dtype=np.float32)
+        rc = (lib or _load()).oracle_quantize_rows_g(rows, cols, int(qmax), int(group), _ptr(W), _ptr(q),
+                                                     _ptr(s))
     if rc != 0:
-        raise RuntimeError(f"oracle_quantize_rows_q failed with code {rc}")
+        raise RuntimeError(f"oracle quantisation failed with code {rc}")
     return q, s
 
 
-def quantize_rows(W, qmax=127):
-    """Per-row codes in [-qmax, qmax] (127: int8 weights, 7: int4) and fp32 scales of a float32
-    matrix: (q[rows, cols] int8, s[rows] f32)."""
-    return _quantize_rows(W, qmax=qmax)
+def quantize_rows(W, qmax=127, group=None):
+    """Codes in [-qmax, qmax] (127: int8 weights, 7: int4) and fp32 scales of a float32 matrix:
+    (q[rows, cols] int8, s[rows] f32) with one scale per row, or s[rows, cols // group] with one
+    per group of `group` consecutive columns."""
+    return _quantize_rows(W, qmax=qmax, group=group)
 
 
-def _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, lib=None):
+def quantize_int4(W1, W3, W2):
+    """The int4 convention: W1, W3 [H, D] with a scale per group of INT4_GROUP columns, W2 [D, H]
+    with a scale per row.  Returns (q1, s1, q3, s3, q2, s2)."""
+    return (quantize_rows(W1, 7, INT4_GROUP) + quantize_rows(W3, 7, INT4_GROUP) + quantize_rows(W2, 7))
+
+
+INT4_GROUP = 64
+
+
+def _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, lib=None, group=None):
+    g = D if group is None else int(group)
+    if g < 1 or D % g:
+        raise RuntimeError(f"group {g} does not divide D={D}")
     i8 = lambda a, n: np.ascontiguousarray(a, dtype=np.int8).reshape(n)  # noqa: E731
     f32 = lambda a, n: np.ascontiguousarray(a, dtype=np.float32).reshape(n)  # noqa: E731
     q1, q3, q2 = i8(q1, H * D), i8(q3, H * D), i8(q2, D * H)
-    s1, s3, s2 = f32(s1, H), f32(s3, H), f32(s2, D)
+    s1, s3, s2 = f32(s1, H * (D // g)), f32(s3, H * (D // g)), f32(s2, D)
     x = _as_input(x, BF16)
     B = x.size // D
     y = np.zeros((B, D), dtype=np.float64)
     z = np.zeros((B, H), dtype=np.float64)
     n_live = np.zeros(B, dtype=np.int32)
-    rc = (lib or _load()).oracle_ffn_dense_q8(D, H, act, B, flags, float(thr), _ptr(q1), _ptr(s1), _ptr(q3),
+    rc = (lib or _load()).oracle_ffn_dense_qg(D, H, act, B, flags, float(thr), g, _ptr(q1), _ptr(s1), _ptr(q3),
                                               _ptr(s3), _ptr(q2), _ptr(s2), _ptr(x), _ptr(y), _ptr(z),
                                               _ptr(n_live))
     if rc != 0:
-        raise RuntimeError(f"oracle_ffn_dense_q8 failed with code {rc}")
+        raise RuntimeError(f"oracle_ffn_dense_qg failed with code {rc}")
     return y, z, n_live
 
 
-def ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0):
-    """Dense definition with int8 weights (q1, q3 [H, D], scales [H]; q2 [D, H], scales [D]) and
-    bf16 x (uint16 bits).  flags: 0 or FLAG_DOUBLE_ACT.  Returns (y, z, n_live)."""
-    return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr)
+def ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, group=None):
+    """Dense definition with quantised weights (q1, q3 [H, D] with scales [H], or [H, D // group]
+    with one per group of columns; q2 [D, H], scales [D]) and bf16 x (uint16 bits).  flags: 0 or
+    FLAG_DOUBLE_ACT.  Returns (y, z, n_live)."""
+    return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, group=group)

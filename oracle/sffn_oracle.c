@@ -57,8 +57,12 @@
  * (the precision of the weights being quantised); an all-zero row has s = 0
  * and codes 0.  The forward is the definition above with every weight replaced
  * by its dequantised value q * s (exact in double); x is bf16.  Weight-only
- * int4 takes the same convention with 7 in place of 127 (codes in [-7, 7]);
- * the "_q8" forward serves it unchanged, its codes being small integers.
+ * int4 takes 7 in place of 127 (codes in [-7, 7]), and for W1 and W3 one scale
+ * per group of 64 consecutive columns of a row instead of one per row: with a
+ * single int4 scale per row, one large entry (a gate bias carried as a weight
+ * column, say) sets a step that rounds every ordinary entry of the row to 0.
+ * W2 keeps one scale per output element.  The "_qg" entry points take the
+ * group; the "_q8" ones are group = D.
  *
  * Portable C99 + OpenMP; no SIMD intrinsics, no -ffast-math.
  */
@@ -338,31 +342,41 @@ int oracle_ffn_gate_first(int D, int H, int r, int act, int dtype, int B,
 
 /* ------------------------------------------------------------------------ int8 */
 
-/* Per-row symmetric quantisation of W[rows, cols] to codes in [-qmax, qmax]
- * (binary32 decisions): qmax = 127 for int8 weights, 7 for int4. */
-int oracle_quantize_rows_q(int rows, int cols, int qmax, const float* W, int8_t* q, float* s) {
-  if (rows < 0 || cols <= 0 || qmax < 1 || qmax > 127) return -1;
+/* Symmetric quantisation of W[rows, cols] to codes in [-qmax, qmax] with one
+ * scale per group of `group` consecutive columns of a row (group = cols: one
+ * per row), s[i * (cols / group) + g]; binary32 decisions.  qmax = 127 for int8
+ * weights, 7 for int4. */
+int oracle_quantize_rows_g(int rows, int cols, int qmax, int group, const float* W, int8_t* q, float* s) {
+  if (rows < 0 || cols <= 0 || qmax < 1 || qmax > 127 || group < 1 || cols % group) return -1;
   const float qm = (float)qmax;
+  const int ng = cols / group;
   for (int i = 0; i < rows; ++i) {
-    const float* w = W + (size_t)i * cols;
-    float amax = 0.0f;
-    for (int j = 0; j < cols; ++j) {
-      const float a = fabsf(w[j]);
-      if (a > amax) amax = a;
-    }
-    const float sc = amax / qm;
-    s[i] = sc;
-    for (int j = 0; j < cols; ++j) {
-      float v = 0.0f;
-      if (sc > 0.0f) {
-        v = rintf(w[j] / sc); /* default rounding mode: to nearest, ties to even */
-        if (v > qm) v = qm;
-        if (v < -qm) v = -qm;
+    for (int g = 0; g < ng; ++g) {
+      const float* w = W + (size_t)i * cols + (size_t)g * group;
+      float amax = 0.0f;
+      for (int j = 0; j < group; ++j) {
+        const float a = fabsf(w[j]);
+        if (a > amax) amax = a;
       }
-      q[(size_t)i * cols + j] = (int8_t)v;
+      const float sc = amax / qm;
+      s[(size_t)i * ng + g] = sc;
+      for (int j = 0; j < group; ++j) {
+        float v = 0.0f;
+        if (sc > 0.0f) {
+          v = rintf(w[j] / sc); /* default rounding mode: to nearest, ties to even */
+          if (v > qm) v = qm;
+          if (v < -qm) v = -qm;
+        }
+        q[(size_t)i * cols + (size_t)g * group + j] = (int8_t)v;
+      }
     }
   }
   return 0;
+}
+
+/* Per-row symmetric quantisation to codes in [-qmax, qmax] (one scale per row). */
+int oracle_quantize_rows_q(int rows, int cols, int qmax, const float* W, int8_t* q, float* s) {
+  return oracle_quantize_rows_g(rows, cols, qmax, cols, W, q, s);
 }
 
 /* Per-row symmetric int8 quantisation of W[rows, cols] (binary32 decisions). */
@@ -370,22 +384,29 @@ int oracle_quantize_rows(int rows, int cols, const float* W, int8_t* q, float* s
   return oracle_quantize_rows_q(rows, cols, 127, W, q, s);
 }
 
-/* row i of a quantised matrix, dequantised: q[i, j] * s[i] (exact in double) */
+/* row i of a quantised matrix, dequantised: q[i, j] * s[i, j / group] (exact in double) */
+static void dequant_row_g(const int8_t* q, const float* s, size_t i, int n, int group, double* out) {
+  const size_t ng = (size_t)(n / group);
+  for (int j = 0; j < n; ++j) out[j] = (double)q[i * (size_t)n + j] * (double)s[i * ng + (size_t)(j / group)];
+}
 static void dequant_row(const int8_t* q, const float* s, size_t i, int n, double* out) {
-  for (int j = 0; j < n; ++j) out[j] = (double)q[i * (size_t)n + j] * (double)s[i];
+  dequant_row_g(q, s, i, n, n, out);
 }
 
 /*
- * Dense definition with weight-only int8 weights: q1, q3 [H, D] with scales
- * s1, s3 [H]; q2 [D, H] with scales s2 [D]; x [B, D] bf16 bits.  flags may only
- * hold OR_FLAG_DOUBLE_ACT (the standard gate).  Outputs as oracle_ffn_dense_ex.
+ * Dense definition with weight-only quantised weights: q1, q3 [H, D] with one
+ * scale per group of `group` columns, s1, s3 [H, D / group] (group = D: one per
+ * row, the int8 form); q2 [D, H] with scales s2 [D]; x [B, D] bf16 bits.  flags
+ * may only hold OR_FLAG_DOUBLE_ACT (the standard gate).  Outputs as
+ * oracle_ffn_dense_ex.  oracle_ffn_dense_q8 is the form with group = D.
  */
-int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
+int oracle_ffn_dense_qg(int D, int H, int act, int B, int flags, double thr, int group,
                         const int8_t* q1, const float* s1, const int8_t* q3, const float* s3,
                         const int8_t* q2, const float* s2, const void* x,
                         double* y, double* z, int* n_live) {
   if (check_args(D, H, 0, act, OR_BF16, B, flags, 0.0, thr)) return -1;
   if (flags & ~OR_FLAG_DOUBLE_ACT) return -1;
+  if (group < 1 || D % group) return -1;
   double* xd = (double*)malloc(sizeof(double) * (size_t)D);
   double* zb = (double*)malloc(sizeof(double) * (size_t)H);
   double* g = (double*)malloc(sizeof(double) * (size_t)H);
@@ -408,9 +429,9 @@ int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
 #pragma omp for schedule(static)
       for (int i = 0; i < H; ++i) {
         if (!row) continue;
-        dequant_row(q1, s1, (size_t)i, D, row);
+        dequant_row_g(q1, s1, (size_t)i, D, group, row);
         zb[i] = dot(row, xd, D);
-        dequant_row(q3, s3, (size_t)i, D, row);
+        dequant_row_g(q3, s3, (size_t)i, D, group, row);
         const double u = dot(row, xd, D);
         g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);
       }
@@ -431,4 +452,11 @@ int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
   }
   free(xd); free(zb); free(g);
   return rc;
+}
+
+int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
+                        const int8_t* q1, const float* s1, const int8_t* q3, const float* s3,
+                        const int8_t* q2, const float* s2, const void* x,
+                        double* y, double* z, int* n_live) {
+  return oracle_ffn_dense_qg(D, H, act, B, flags, thr, D, q1, s1, q3, s3, q2, s2, x, y, z, n_live);
 }

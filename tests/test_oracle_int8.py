@@ -160,3 +160,84 @@ def test_int4_codes_through_the_q8_forward_equal_the_float_oracle(act):
     np.testing.assert_allclose(z4, zf, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(y4, yf, rtol=1e-12, atol=1e-12)
     assert np.array_equal(n4, nf)
+
+
+# int4 for W1 and W3 takes one scale per group of oracle.INT4_GROUP columns (see the C file: with one
+# scale per row, a single large entry rounds every ordinary entry of the row to 0).
+
+def test_quantize_grouped_hand_worked():
+    W = np.array([[7.0, 1.0, -3.5, 0.5, 14.0, 2.0, -5.0, 3.0],    # groups of 4: s = 1, then s = 2
+                  [0.0, 0.0, 0.0, 0.0, -0.5, 0.25, 0.0, 0.0]],   # an all-zero group: s = 0; s = 1/14
+                 dtype=np.float32)
+    q, s = oracle.quantize_rows(W, 7, group=4)
+    assert s.shape == (2, 2)
+    assert s[0].tolist() == [1.0, 2.0] and s[1, 0] == 0.0
+    assert s[1, 1] == np.float32(np.float32(0.5) / np.float32(7.0))
+    assert q[0].tolist() == [7, 1, -4, 0, 7, 1, -2, 2]            # -3.5 -> -4, 0.5 -> 0, -2.5 -> -2, 1.5 -> 2
+    # binary32: fl(0.5 / 7) lies above 0.5 / 7, so 0.25 / s = 3.4999998 and the code is 3, not 4
+    assert q[1].tolist() == [0, 0, 0, 0, -7, 3, 0, 0]
+
+
+def test_quantize_grouped_with_one_group_is_per_row():
+    rng = np.random.default_rng(6)
+    W = rng.standard_normal((9, 192)).astype(np.float32)
+    for qmax in (7, 127):
+        qg, sg = oracle.quantize_rows(W, qmax, group=192)
+        q, s = oracle.quantize_rows(W, qmax)
+        assert np.array_equal(qg, q) and np.array_equal(sg[:, 0], s)
+
+
+def test_grouped_int4_keeps_a_row_with_one_large_entry():
+    """A row of N(0, 1/D) entries with one entry of -1.28 (a gate bias carried as a column): one int4
+    scale per row rounds almost every other entry to 0; one per 64-column group keeps the other groups."""
+    rng = np.random.default_rng(7)
+    D = 512
+    W = (rng.standard_normal((4, D)) / np.sqrt(D)).astype(np.float32)
+    W[:, D - 1] = -1.28
+    q_row, _ = oracle.quantize_rows(W, 7)
+    assert (q_row[:, :D - 1] != 0).mean() < 0.06                  # a step of 1.28 / 7: ~2 sigma, ~95 % zeros
+    q_g, s_g = oracle.quantize_rows(W, 7, group=oracle.INT4_GROUP)
+    assert (q_g[:, :D - 64] != 0).mean() > 0.6
+    assert (np.abs(q_g[:, :D - 64]).max(axis=1) == 7).all()      # every other group uses the full range
+    err = np.abs(W.astype(np.float64) - q_g * np.repeat(s_g, oracle.INT4_GROUP, axis=1).astype(np.float64))
+    assert (err <= np.repeat(s_g, oracle.INT4_GROUP, axis=1) * (0.5 + 1e-5)).all()
+
+
+@pytest.mark.parametrize("act,flags", [(RELU, 0), (SILU, 0), (RELU, oracle.FLAG_DOUBLE_ACT)])
+def test_grouped_forward_equals_float_oracle_on_exact_weights(act, flags):
+    """Codes with power-of-two scales per 16-column group: q * s is exact, so the grouped forward must
+    equal the pinned float32 oracle on the dequantised weights."""
+    D, H, B, G = 64, 90, 3, 16
+    rng = np.random.default_rng(8)
+
+    def grouped(rows, cols, g):
+        q = rng.integers(-7, 8, size=(rows, cols)).astype(np.int8)
+        q.reshape(rows, cols // g, g)[:, :, 0] = rng.choice([-7, 7], size=(rows, cols // g))
+        s = np.ldexp(1.0, -rng.integers(1, 6, size=(rows, cols // g))).astype(np.float32)
+        return q, s, (q.astype(np.float32) * np.repeat(s, g, axis=1)).astype(np.float32)
+
+    (q1, s1, W1), (q3, s3, W3) = grouped(H, D, G), grouped(H, D, G)
+    q2, s2, W2 = grouped(D, H, H)
+    s2 = s2[:, 0]
+    for q, s, W in ((q1, s1, W1), (q3, s3, W3)):
+        qq, ss = oracle.quantize_rows(W, 7, group=G)
+        assert np.array_equal(qq, q) and np.array_equal(ss, s)
+    xf = torch.from_numpy(rng.standard_normal((B, D)).astype(np.float32)).bfloat16().float().numpy()
+    thr = 0.05 if act == SILU else 0.0
+    yg, zg, ng = oracle.ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, bf16_bits(xf), thr=thr, group=G)
+    yf, zf, nf = oracle.ffn_dense_ex(D, H, 0, act, F32, flags, W1, None, None, W3, W2, xf, thr=thr)
+    np.testing.assert_allclose(zg, zf, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(yg, yf, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(ng, nf)
+
+
+def test_grouped_forward_hand_worked():
+    """D = 4, groups of 2, H = 1: z = 0.5 (2 - 1) + 2 (3 + 1) = 8.5 for x = (1, 1, 1, 1)."""
+    q1 = np.array([[2, -1, 3, 1]], dtype=np.int8); s1 = np.array([[0.5, 2.0]], dtype=np.float32)
+    q3 = np.array([[1, 1, 0, 1]], dtype=np.int8); s3 = np.array([[1.0, 0.25]], dtype=np.float32)
+    q2 = np.array([[1], [2], [-1], [4]], dtype=np.int8); s2 = np.array([1.0, 0.5, 2.0, 0.125], dtype=np.float32)
+    x = bf16_bits(np.ones((1, 4), dtype=np.float32))
+    y, z, n = oracle.ffn_dense_q8(4, 1, RELU, 0, q1, s1, q3, s3, q2, s2, x, group=2)
+    # u = 1 (1 + 1) + 0.25 (0 + 1) = 2.25; h = 8.5 * 2.25 = 19.125
+    assert z.tolist() == [[8.5]] and n.tolist() == [1]
+    assert y.tolist() == [[19.125, 19.125, -38.25, 9.5625]]
