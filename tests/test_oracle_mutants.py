@@ -47,10 +47,15 @@ MUTANTS = {
     "q8_truncate": ("v = rintf(w[j] / sc);", "v = truncf(w[j] / sc);"),
     "q8_round_half_away": ("v = rintf(w[j] / sc);", "v = roundf(w[j] / sc);"),
     "q8_amax_signed": ("const float a = fabsf(w[j]);", "const float a = w[j];"),
-    "q8_one_scale": ("out[j] = (double)q[i * (size_t)n + j] * (double)s[i];",
-                     "out[j] = (double)q[i * (size_t)n + j] * (double)s[0];"),
+    "q8_one_scale": ("(double)s[i * ng + (size_t)(j / group)];", "(double)s[0];"),
     "q8_down_uses_gate_scales": ("dequant_row(q2, s2, (size_t)m, H, row);", "dequant_row(q2, s1, (size_t)m, H, row);"),
-    "q8_up_uses_gate_codes": ("dequant_row(q3, s3, (size_t)i, D, row);", "dequant_row(q1, s3, (size_t)i, D, row);"),
+    "q8_up_uses_gate_codes": ("dequant_row_g(q3, s3, (size_t)i, D, group, row);",
+                              "dequant_row_g(q1, s3, (size_t)i, D, group, row);"),
+    # int4 groups of columns
+    "group_scale_index_mod": ("(double)s[i * ng + (size_t)(j / group)];", "(double)s[i * ng + (size_t)(j % ng)];"),
+    "group_amax_of_first_group": ("const float* w = W + (size_t)i * cols + (size_t)g * group;",
+                                  "const float* w = W + (size_t)i * cols;"),
+    "group_scale_of_row": ("s[(size_t)i * ng + g] = sc;", "s[(size_t)i * ng] = sc;"),
 }
 
 
@@ -182,6 +187,14 @@ def _pins(mod):
     y8, _, n8 = mod.ffn_dense_q8(D, H, oracle.RELU, 0, q1, s1, q3, s3, q2, s2, _bf16_bits(xq))
     yf, _, nf = mod.ffn_dense(D, H, 0, oracle.RELU, oracle.F32, E1, None, None, E3, E2, xq)
     check("q8_exact_weights", np.allclose(y8, yf, rtol=1e-12, atol=1e-12) and np.array_equal(n8, nf))
+    # int4 groups (values derived in test_oracle_int8)
+    q, sc = mod.quantize_rows(f([[7.0, 1.0, -3.5, 0.5, 14.0, 2.0, -5.0, 3.0]]), 7, 4)
+    check("q4g_hand_codes", q.tolist() == [[7, 1, -4, 0, 7, 1, -2, 2]] and sc.tolist() == [[1.0, 2.0]])
+    yg, zg, ng = mod.ffn_dense_q8(4, 1, oracle.RELU, 0, np.array([[2, -1, 3, 1]], np.int8), f([[0.5, 2.0]]),
+                                  np.array([[1, 1, 0, 1]], np.int8), f([[1.0, 0.25]]),
+                                  np.array([[1], [2], [-1], [4]], np.int8), f([1.0, 0.5, 2.0, 0.125]),
+                                  _bf16_bits(f(np.ones((1, 4)))), 0.0, 2)
+    check("q4g_hand_forward", zg.tolist() == [[8.5]] and yg.tolist() == [[19.125, 19.125, -38.25, 9.5625]])
     return failed
 
 
