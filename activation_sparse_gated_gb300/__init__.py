@@ -20,7 +20,8 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsffn.so")
 
-SFFN_F32, SFFN_BF16, SFFN_I8W = 0, 1, 2
+SFFN_F32, SFFN_BF16, SFFN_I8W, SFFN_I4W = 0, 1, 2, 3
+INT4_GROUP = 64  # int4 W1, W3: columns per scale
 SFFN_ACT_RELU, SFFN_ACT_RSP, SFFN_ACT_SILU = 0, 1, 2
 SFFN_OK = 0
 SFFN_ERR_ARG, SFFN_ERR_ALIGN, SFFN_ERR_DTYPE, SFFN_ERR_CUDA = -1, -2, -3, -4
@@ -201,8 +202,9 @@ class SparseFFN:
     ``SparseFFN(D, H, r=0, act="relu", dtype="bf16", flags=0)`` (flags: the
     SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT options); ``set_weights(W1_or_U, V,
     W3, W2)`` with torch tensors in the layer's dtype (W2 as [D, H]);
-    ``forward(x, y=None)`` with x [B, D] on the handle's device.  dtype "int8": weight-only
-    int8 (bf16 weights given to ``set_weights`` are quantised on the device; x and y bf16).
+    ``forward(x, y=None)`` with x [B, D] on the handle's device.  dtype "int8" / "int4":
+    weight-only int8 / int4 (bf16 weights given to ``set_weights`` are quantised on the device;
+    x and y bf16).
     """
 
     def __init__(self, D: int, H: int, r: int = 0, act: str = "relu", dtype: str = "bf16", flags: int = 0):
@@ -210,7 +212,7 @@ class SparseFFN:
         self.dtype = dtype
         self.flags = flags
         self._act = {"relu": SFFN_ACT_RELU, "rsp": SFFN_ACT_RSP, "silu": SFFN_ACT_SILU}[act]
-        self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16, "int8": SFFN_I8W}[dtype]
+        self._dt = {"f32": SFFN_F32, "bf16": SFFN_BF16, "int8": SFFN_I8W, "int4": SFFN_I4W}[dtype]
         self.h = sffn_create_ex(D, H, r, self._act, self._dt, flags)
 
     def set_weights(self, W1_or_U, V, W3, W2, stream=None):
@@ -242,15 +244,18 @@ class SparseFFN:
         sffn_synchronize(self.h)
 
     def set_weights_int8(self, W1q, s1, W3q, s3, W2q, s2, stream=None):
-        """Codes and scales quantised elsewhere (int8 [H, D], [H, D], [D, H]; fp32 [H], [H], [D])."""
+        """Codes and scales quantised elsewhere (int8 [H, D], [H, D], [D, H]; fp32 [H], [H], [D]); on an
+        int4 handle one code per byte in [-7, 7] and s1, s3 [H, D // 64] (one per group of 64 columns)."""
         sffn_set_weights_int8(self.h, W1q, s1, W3q, s3, W2q, s2, stream)
 
     def int8_weights(self, device="cuda"):
-        """The handle's codes and scales as tensors: (W1q, s1, W3q, s3, W2q, s2), W2q as [D, H]."""
+        """The handle's codes (one per byte, also for int4) and scales as tensors: (W1q, s1, W3q, s3,
+        W2q, s2), W2q as [D, H]; s1, s3 [H], or [H, D // 64] on an int4 handle."""
         import torch
         D, H = self.D, self.H
-        out = (torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(H, device=device),
-               torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(H, device=device),
+        ss = (H,) if self.dtype != "int4" else (H, D // INT4_GROUP)
+        out = (torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(ss, device=device),
+               torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(ss, device=device),
                torch.empty(D, H, dtype=torch.int8, device=device), torch.empty(D, device=device))
         sffn_get_weights_int8(self.h, *out)
         return out

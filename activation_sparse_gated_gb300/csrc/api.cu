@@ -43,7 +43,8 @@ void sffn::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s",
 
 struct sffn_s {
   int D = 0, H = 0, r = 0, act = 0, dtype = 0, elt = 0;
-  int welt = 0;  // bytes of a stored weight element (1: int8 codes of SFFN_I8W)
+  int welt = 0;  // bytes of a stored weight element (1: the int8 / int4 code arrays of SFFN_I8W / SFFN_I4W)
+  int qbits = 0; // weight-only codes: 8 (SFFN_I8W), 4 (SFFN_I4W, two per byte), else 0
   int flags = 0;  // SFFN_GATE_TILED_G | SFFN_GATE_RMSNORM | SFFN_DOUBLE_ACT
   float thr = 0.f;  // live iff |A(z)| > thr (sffn_set_live_threshold)
   int device = 0, num_sms = 0;
@@ -176,6 +177,11 @@ const char* sffn_strerror(int code) {
   }
 }
 
+namespace {
+// scales per row of W1 and of W3 on a quantised handle: one (int8), one per 64 columns (int4)
+size_t qscale_per_row(const sffn_s* h) { return h->qbits == 4 ? (size_t)h->D / INT4_GROUP : 1; }
+}  // namespace
+
 sffn_t sffn_create(int D, int H, int r, int act, int dtype) { return sffn_create_ex(D, H, r, act, dtype, 0); }
 
 sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
@@ -192,12 +198,16 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     fail(SFFN_ERR_ARG, "the tiled identity and RMSNorm options belong to the low-rank gate (r > 0)");
     return nullptr;
   }
-  if (dtype != SFFN_F32 && dtype != SFFN_BF16 && dtype != SFFN_I8W) {
+  if (dtype != SFFN_F32 && dtype != SFFN_BF16 && dtype != SFFN_I8W && dtype != SFFN_I4W) {
     fail(SFFN_ERR_ARG, "dtype %d unknown", dtype);
     return nullptr;
   }
   if (dtype == SFFN_I8W && (r != 0 || D % 16 != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
     fail(SFFN_ERR_DTYPE, "int8 weights need the standard gate (r = 0), D %% 16 == 0 and no low-rank option");
+    return nullptr;
+  }
+  if (dtype == SFFN_I4W && (r != 0 || D % INT4_GROUP != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
+    fail(SFFN_ERR_DTYPE, "int4 weights need the standard gate (r = 0), D %% 64 == 0 and no low-rank option");
     return nullptr;
   }
   if ((flags & SFFN_DETERMINISTIC) && dtype != SFFN_BF16) {
@@ -217,7 +227,8 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
   if (!h) { fail(SFFN_ERR_NOMEM, "host allocation failed"); return nullptr; }
   h->D = D; h->H = H; h->r = r; h->act = act; h->dtype = dtype; h->flags = flags;
   h->elt = dtype == SFFN_F32 ? 4 : 2;
-  h->welt = dtype == SFFN_I8W ? 1 : h->elt;
+  h->qbits = dtype == SFFN_I8W ? 8 : dtype == SFFN_I4W ? 4 : 0;
+  h->welt = h->qbits ? 1 : h->elt;
 
   auto bail = [&](int code, const char* what, cudaError_t e) -> sffn_t {
     fail(code, "%s: %s", what, cudaGetErrorString(e));
@@ -236,14 +247,14 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
 
   const size_t welt = h->welt;
   const size_t gk = (size_t)gate_k(h);
-  const bool i8 = dtype == SFFN_I8W;
+  const bool i8 = h->qbits != 0;  // int8 or int4 codes with per-channel scales
   struct { void** p; size_t bytes; } allocs[] = {
       {&h->gate_w, (size_t)H * gk * welt},
       {&h->V, (size_t)std::max(r, 1) * D * welt},
       {&h->W3, (size_t)H * D * welt},
       {&h->W2t, (size_t)H * D * welt},
-      {(void**)&h->qs1, i8 ? sizeof(float) * H : 16},
-      {(void**)&h->qs3, i8 ? sizeof(float) * H : 16},
+      {(void**)&h->qs1, i8 ? sizeof(float) * H * qscale_per_row(h) : 16},
+      {(void**)&h->qs3, i8 ? sizeof(float) * H * qscale_per_row(h) : 16},
       {(void**)&h->qs2, i8 ? sizeof(float) * D : 16},
       {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * D},
       {(void**)&h->tbuf, sizeof(float) * SFFN_MAX_BATCH * std::max(r, 8)},
@@ -305,9 +316,9 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     }
     if ((e = ffn_batch_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     if (i8) {
-      h->i8_plan = plan_ffn_b1_i8(D, h->stream_rows_cap);
+      h->i8_plan = plan_ffn_b1_i8(D, h->stream_rows_cap, h->qbits);
       if (h->i8_plan.smem > h->max_smem) {
-        fail(SFFN_ERR_DTYPE, "shared-memory plan of the int8 kernel exceeds the device limit");
+        fail(SFFN_ERR_DTYPE, "shared-memory plan of the int8 / int4 kernel exceeds the device limit");
         char keep[sizeof g_msg];
         std::memcpy(keep, g_msg, sizeof keep);
         release(h);
@@ -371,23 +382,45 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
   if (!W1_or_U || !W3 || !W2 || (h->r > 0 && !V)) return fail(SFFN_ERR_ARG, "null weight pointer");
   if (int rc = check_device(h)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (h->dtype == SFFN_I8W) {
-    // bf16 weights in, per-output-channel int8 codes and scales out (W2's codes transposed)
+  if (h->qbits) {
+    // bf16 weights in, per-output-channel codes and scales out (W2's codes transposed); int4
+    // codes are decided one per byte, then packed two per byte
     const size_t D = h->D, H = h->H;
+    const bool i4 = h->qbits == 4;
+    const int qmax = i4 ? 7 : 127;
     void* stage = nullptr;
-    int8_t* q2 = nullptr;
+    int8_t *q2 = nullptr, *codes = nullptr;
+    int* perr = nullptr;
     SFFN_CUDA(cudaMalloc(&stage, D * H * 2));
     cudaError_t e = cudaMalloc(&q2, D * H);
+    if (!e && i4) e = cudaMalloc(&codes, D * H);
+    if (!e && i4) e = cudaMalloc(&perr, sizeof(int));
+    if (!e && i4) e = cudaMemsetAsync(perr, 0, sizeof(int), s);
+    auto store = [&](void* dst, const int8_t* src) {  // int4: pack the one-per-byte codes
+      return i4 ? launch_pack_int4(src, dst, H * D, perr, s) : cudaSuccess;
+    };
+    // W1 and W3: int8 one scale per row, int4 one per group of 64 columns
+    auto quant_rows = [&](int8_t* dst, float* sc) {
+      return i4 ? launch_quantize_groups4(stage, dst, sc, (int)H, (int)D, s)
+                : launch_quantize_rows(stage, dst, sc, (int)H, (int)D, s, qmax);
+    };
+    int8_t* c1 = i4 ? codes : static_cast<int8_t*>(h->gate_w);
     if (!e) e = cudaMemcpyAsync(stage, W1_or_U, H * D * 2, cudaMemcpyDefault, s);
-    if (!e) e = launch_quantize_rows(stage, static_cast<int8_t*>(h->gate_w), h->qs1, (int)H, (int)D, s);
+    if (!e) e = quant_rows(c1, h->qs1);
+    if (!e) e = store(h->gate_w, c1);
+    int8_t* c3 = i4 ? codes : static_cast<int8_t*>(h->W3);
     if (!e) e = cudaMemcpyAsync(stage, W3, H * D * 2, cudaMemcpyDefault, s);
-    if (!e) e = launch_quantize_rows(stage, static_cast<int8_t*>(h->W3), h->qs3, (int)H, (int)D, s);
+    if (!e) e = quant_rows(c3, h->qs3);
+    if (!e) e = store(h->W3, c3);
     if (!e) e = cudaMemcpyAsync(stage, W2, D * H * 2, cudaMemcpyDefault, s);
-    if (!e) e = launch_quantize_rows(stage, q2, h->qs2, (int)D, (int)H, s);
-    if (!e) e = launch_transpose(q2, h->W2t, (int)D, (int)H, 1, s);
+    if (!e) e = launch_quantize_rows(stage, q2, h->qs2, (int)D, (int)H, s, qmax);
+    if (!e) e = launch_transpose(q2, i4 ? static_cast<void*>(codes) : h->W2t, (int)D, (int)H, 1, s);
+    if (!e) e = store(h->W2t, codes);
     if (!e) e = cudaStreamSynchronize(s);
     cudaFree(stage);
     cudaFree(q2);
+    cudaFree(codes);
+    cudaFree(perr);
     if (e) return fail(SFFN_ERR_CUDA, "weight quantisation failed: %s", cudaGetErrorString(e));
     h->weights_set = true;
     return SFFN_OK;
@@ -415,23 +448,44 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
 int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const int8_t* W3q, const float* s3,
                           const int8_t* W2q, const float* s2, void* stream) {
   if (!h) return fail(SFFN_ERR_ARG, "null handle");
-  if (h->dtype != SFFN_I8W) return fail(SFFN_ERR_STATE, "the handle does not hold int8 weights");
+  if (!h->qbits) return fail(SFFN_ERR_STATE, "the handle does not hold int8 or int4 weights");
   if (!W1q || !s1 || !W3q || !s3 || !W2q || !s2) return fail(SFFN_ERR_ARG, "null weight pointer");
   if (int rc = check_device(h)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t D = h->D, H = h->H;
-  int8_t* q2 = nullptr;
+  const bool i4 = h->qbits == 4;
+  int8_t *q2 = nullptr, *codes = nullptr;
+  int* perr = nullptr;
   SFFN_CUDA(cudaMalloc(&q2, D * H));
-  cudaError_t e = cudaMemcpyAsync(h->gate_w, W1q, H * D, cudaMemcpyDefault, s);
-  if (!e) e = cudaMemcpyAsync(h->W3, W3q, H * D, cudaMemcpyDefault, s);
-  if (!e) e = cudaMemcpyAsync(h->qs1, s1, sizeof(float) * H, cudaMemcpyDefault, s);
-  if (!e) e = cudaMemcpyAsync(h->qs3, s3, sizeof(float) * H, cudaMemcpyDefault, s);
+  cudaError_t e = i4 ? cudaMalloc(&codes, D * H) : cudaSuccess;
+  if (!e && i4) e = cudaMalloc(&perr, sizeof(int));
+  if (!e && i4) e = cudaMemsetAsync(perr, 0, sizeof(int), s);
+  // int4: each array goes through `codes` and is packed two per byte, codes outside [-7, 7] flagged
+  auto put = [&](void* dst, const int8_t* src) {
+    if (!i4) return cudaMemcpyAsync(dst, src, H * D, cudaMemcpyDefault, s);
+    cudaError_t r = cudaMemcpyAsync(codes, src, H * D, cudaMemcpyDefault, s);
+    return r ? r : launch_pack_int4(codes, dst, H * D, perr, s);
+  };
+  const size_t nsc = H * qscale_per_row(h);
+  if (!e) e = put(h->gate_w, W1q);
+  if (!e) e = put(h->W3, W3q);
+  if (!e) e = cudaMemcpyAsync(h->qs1, s1, sizeof(float) * nsc, cudaMemcpyDefault, s);
+  if (!e) e = cudaMemcpyAsync(h->qs3, s3, sizeof(float) * nsc, cudaMemcpyDefault, s);
   if (!e) e = cudaMemcpyAsync(h->qs2, s2, sizeof(float) * D, cudaMemcpyDefault, s);
   if (!e) e = cudaMemcpyAsync(q2, W2q, D * H, cudaMemcpyDefault, s);
-  if (!e) e = launch_transpose(q2, h->W2t, (int)D, (int)H, 1, s);
+  if (!e) e = launch_transpose(q2, i4 ? static_cast<void*>(codes) : h->W2t, (int)D, (int)H, 1, s);
+  if (!e && i4) e = launch_pack_int4(codes, h->W2t, H * D, perr, s);
+  int bad = 0;
+  if (!e && i4) e = cudaMemcpyAsync(&bad, perr, sizeof(int), cudaMemcpyDeviceToHost, s);
   if (!e) e = cudaStreamSynchronize(s);
   cudaFree(q2);
-  if (e) return fail(SFFN_ERR_CUDA, "int8 weight upload failed: %s", cudaGetErrorString(e));
+  cudaFree(codes);
+  cudaFree(perr);
+  if (e) return fail(SFFN_ERR_CUDA, "int8 / int4 weight upload failed: %s", cudaGetErrorString(e));
+  if (bad) {
+    h->weights_set = false;
+    return fail(SFFN_ERR_ARG, "int4 codes must lie in [-7, 7]");
+  }
   h->weights_set = true;
   return SFFN_OK;
 }
@@ -439,25 +493,35 @@ int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const in
 int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* s3, int8_t* W2q, float* s2,
                           void* stream) {
   if (!h) return fail(SFFN_ERR_ARG, "null handle");
-  if (h->dtype != SFFN_I8W) return fail(SFFN_ERR_STATE, "the handle does not hold int8 weights");
+  if (!h->qbits) return fail(SFFN_ERR_STATE, "the handle does not hold int8 or int4 weights");
   if (!h->weights_set) return fail(SFFN_ERR_STATE, "no weights have been set");
   if (int rc = check_device(h)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t D = h->D, H = h->H;
+  const bool i4 = h->qbits == 4;
   cudaError_t e = cudaSuccess;
-  if (W1q) e = cudaMemcpyAsync(W1q, h->gate_w, H * D, cudaMemcpyDefault, s);
-  if (!e && W3q) e = cudaMemcpyAsync(W3q, h->W3, H * D, cudaMemcpyDefault, s);
-  if (!e && s1) e = cudaMemcpyAsync(s1, h->qs1, sizeof(float) * H, cudaMemcpyDefault, s);
-  if (!e && s3) e = cudaMemcpyAsync(s3, h->qs3, sizeof(float) * H, cudaMemcpyDefault, s);
+  int8_t *q2 = nullptr, *codes = nullptr;
+  if (i4) e = cudaMalloc(&codes, D * H);
+  // int4: unpacked to one code per byte on the way out
+  auto get = [&](int8_t* dst, const void* src) {
+    if (!i4) return cudaMemcpyAsync(dst, src, H * D, cudaMemcpyDefault, s);
+    cudaError_t r = launch_unpack_int4(src, codes, H * D, s);
+    return r ? r : cudaMemcpyAsync(dst, codes, H * D, cudaMemcpyDefault, s);
+  };
+  if (!e && W1q) e = get(W1q, h->gate_w);
+  if (!e && W3q) e = get(W3q, h->W3);
+  if (!e && s1) e = cudaMemcpyAsync(s1, h->qs1, sizeof(float) * H * qscale_per_row(h), cudaMemcpyDefault, s);
+  if (!e && s3) e = cudaMemcpyAsync(s3, h->qs3, sizeof(float) * H * qscale_per_row(h), cudaMemcpyDefault, s);
   if (!e && s2) e = cudaMemcpyAsync(s2, h->qs2, sizeof(float) * D, cudaMemcpyDefault, s);
-  int8_t* q2 = nullptr;
   if (!e && W2q) {
     e = cudaMalloc(&q2, D * H);
-    if (!e) e = launch_transpose(h->W2t, q2, (int)H, (int)D, 1, s);
+    if (!e && i4) e = launch_unpack_int4(h->W2t, codes, H * D, s);
+    if (!e) e = launch_transpose(i4 ? static_cast<const void*>(codes) : h->W2t, q2, (int)H, (int)D, 1, s);
     if (!e) e = cudaMemcpyAsync(W2q, q2, D * H, cudaMemcpyDefault, s);
   }
   if (!e) e = cudaStreamSynchronize(s);
   cudaFree(q2);
+  cudaFree(codes);
   if (e) return fail(SFFN_ERR_CUDA, "int8 weight download failed: %s", cudaGetErrorString(e));
   return SFFN_OK;
 }
@@ -538,8 +602,8 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       return fail(SFFN_ERR_CUDA, "tensor-map encoding of x failed (status %d)", rc);
     SFFN_CUDA(ce);
   }
-  if (h->dtype == SFFN_I8W) {
-    // weight-only int8: one streaming pass per token
+  if (h->qbits) {
+    // weight-only int8 / int4: one streaming pass per token
     for (int b = 0; b < B; ++b) {
       B1Params p;
       p.gate_w = h->gate_w;
@@ -564,13 +628,13 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       p.s1 = h->qs1;
       p.s3 = h->qs3;
       p.s2 = h->qs2;
-      SFFN_CUDA(launch_ffn_b1_i8(p, h->stream_grid, h->i8_plan.smem, s));
+      SFFN_CUDA(launch_ffn_b1_i8(p, h->stream_grid, h->i8_plan.smem, s, h->qbits));
       SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, 1, SFFN_BF16, s));
     }
   }
   if (lopa && !tc_batch) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
-  for (int b = 0; b < B && h->dtype != SFFN_I8W && !tc_batch;) {
+  for (int b = 0; b < B && !h->qbits && !tc_batch;) {
     const int nb = det ? 1 : std::min(8, B - b);
     B1Params p;
     p.gate_w = h->gate_w;

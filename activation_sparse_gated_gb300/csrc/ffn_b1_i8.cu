@@ -1,5 +1,6 @@
-// ffn_b1_i8.cu -- single-token gate-first sparse FFN with weight-only int8
-// weights (standard gate), streaming form; and the per-row quantiser.
+// ffn_b1_i8.cu -- single-token gate-first sparse FFN with weight-only int8 or
+// int4 weights (standard gate), streaming form; the per-row quantiser and the
+// int4 packing.
 //
 // "Model Casting and Low-Parameter Gating", appendix Table 17, quantises the
 // cast models weight-only to int8.  Convention of this library (the pages give
@@ -20,7 +21,19 @@
 // widened to fp32 exactly with a byte permute and a packed add (no int->float
 // conversion instruction): the biased byte q + 128 becomes the low mantissa
 // byte of 2^23.  q * x is exact in fp32 (7 x 8 significant bits); the sums
-// are fp32, two lanes per packed fp32x2 FMA.  There are no spin-waits in this file.
+// are fp32, two lanes per packed fp32x2 FMA.
+//
+// int4 (same appendix, 7 in place of 127, and for W1 and W3 one scale per group
+// of 64 consecutive columns instead of one per row -- with one int4 scale per
+// row a single large entry rounds the rest of the row to zero): a row holds
+// D / 2 bytes, byte b carrying codes 2b (low nibble) and 2b + 1 (high nibble) in
+// two's complement.  A piece's dot product is scaled by its group's scale before
+// it joins the lane's sum.  The kernel is the int8 one with 8-byte pieces of 16 codes in
+// place of 16-byte pieces of 16 codes, so every piece still pairs with the same
+// 16 values of x and the same 16 outputs: the lane and warp mappings, the staged
+// x layout and the gathers are shared.  A nibble is widened like a byte: its sign
+// bit flipped (code + 8), placed in the low mantissa bits of 2^23, 2^23 + 8
+// subtracted.  There are no spin-waits in this file.
 #include <algorithm>
 
 #include "common.cuh"
@@ -33,6 +46,7 @@ namespace {
 constexpr int QW = 12;        // warps per block (two blocks fit an SM)
 constexpr int QT = QW * 32;
 constexpr int QPIECE = 5;     // 16-byte chunks per lane per piece of a streamed gate row
+constexpr int G4 = 64;        // int4: columns per scale group of W1 and W3 (four pieces of 16 codes)
 
 __host__ __device__ constexpr size_t a16(size_t v) { return (v + 15) & ~size_t(15); }
 
@@ -43,6 +57,23 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
                : "l"(p));
   return v;
 }
+__device__ __forceinline__ uint2 ldg_stream(const uint2* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_piece(const uint4* p) { return lds16(p); }
+__device__ __forceinline__ uint2 lds_piece(const uint2* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+  return v;
+}
+
+// The piece of a code row that pairs with 16 values of x: 16 bytes of int8
+// codes or 8 bytes of int4 codes.
+template <int BITS> struct Piece;
+template <> struct Piece<8> { using type = uint4; };
+template <> struct Piece<4> { using type = uint2; };
 
 __device__ __forceinline__ void cpa16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
@@ -66,9 +97,34 @@ __device__ __forceinline__ void widen_i8x4(uint32_t word, float2& v01, float2& v
                           __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543u))), bias);
 }
 
+// 8 int4 codes (one 32-bit word, code j in bits 4j .. 4j + 3) -> 8 exact fp32
+// values, v[k] = (code 2k, code 2k + 1).
+__device__ __forceinline__ void widen_i4x8(uint32_t word, float2 (&v)[4]) {
+  const uint32_t w = word ^ 0x88888888u;
+  const float2 bias = make_float2(-8388616.f, -8388616.f);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    v[k] = fadd2(make_float2(__uint_as_float(((w >> (8 * k)) & 0xFu) | 0x4B000000u),
+                             __uint_as_float(((w >> (8 * k + 4)) & 0xFu) | 0x4B000000u)),
+                 bias);
+}
+
 // acc += code chunk c . x[16c, 16c + 16), two lanes of fp32 per FMA.  x is
 // staged as fp32 in the interleaved layout xq[k * ncw + c] = x[16c + 4k .. +4),
 // so lanes reading consecutive chunks read consecutive 16-byte words.
+__device__ __forceinline__ void dot_chunk(const uint2& w, const float4* xq, int ncw, int c, float2& acc) {
+  const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {  // word h: codes 8h .. 8h + 7, x quarters 2h and 2h + 1
+    float2 v[4];
+    widen_i4x8(words[h], v);
+    const float4 xa = lds_f4(xq + (2 * h) * ncw + c), xb = lds_f4(xq + (2 * h + 1) * ncw + c);
+    ffma2(acc, v[0], make_float2(xa.x, xa.y));
+    ffma2(acc, v[1], make_float2(xa.z, xa.w));
+    ffma2(acc, v[2], make_float2(xb.x, xb.y));
+    ffma2(acc, v[3], make_float2(xb.z, xb.w));
+  }
+}
 __device__ __forceinline__ void dot_chunk(const uint4& w, const float4* xq, int ncw, int c, float2& acc) {
   const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -81,19 +137,87 @@ __device__ __forceinline__ void dot_chunk(const uint4& w, const float4* xq, int 
   }
 }
 
-__device__ __forceinline__ void load_piece_i8(uint4 (&w)[QPIECE], const uint4* row, int pc, int lane, int ncw) {
+// y partial += h * (the 16 codes of piece wv), outputs yr[0..16)
+__device__ __forceinline__ void fold_piece(const uint4& wv, float h, float (&yr)[16]) {
+  const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+  const float2 hh = make_float2(h, h);
 #pragma unroll
-  for (int k = 0; k < QPIECE; ++k) {
-    const int c = pc * 32 * QPIECE + lane + 32 * k;
-    w[k] = (c < ncw) ? ldg_stream(row + c) : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < 4; ++k) {
+    float2 v01, v23;
+    widen_i8x4(words[k], v01, v23);
+    float2 a = make_float2(yr[4 * k], yr[4 * k + 1]), b = make_float2(yr[4 * k + 2], yr[4 * k + 3]);
+    ffma2(a, v01, hh);
+    ffma2(b, v23, hh);
+    yr[4 * k] = a.x;
+    yr[4 * k + 1] = a.y;
+    yr[4 * k + 2] = b.x;
+    yr[4 * k + 3] = b.y;
+  }
+}
+__device__ __forceinline__ void fold_piece(const uint2& wv, float h, float (&yr)[16]) {
+  const uint32_t words[2] = {wv.x, wv.y};
+  const float2 hh = make_float2(h, h);
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    float2 v[4];
+    widen_i4x8(words[w], v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float2 a = make_float2(yr[8 * w + 2 * k], yr[8 * w + 2 * k + 1]);
+      ffma2(a, v[k], hh);
+      yr[8 * w + 2 * k] = a.x;
+      yr[8 * w + 2 * k + 1] = a.y;
+    }
   }
 }
 
+__device__ __forceinline__ float lds_f32(const float* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
+// acc += piece c . x, scaled for int4 by the scale of the piece's group (gs: the row's
+// group scales in shared memory); int8 rows are scaled once, after the sum.
+template <int BITS, typename CT>
+__device__ __forceinline__ void dot_piece(const CT& w, const float4* xq, int ncw, int c, float2& acc,
+                                          const float* gs) {
+  if constexpr (BITS == 4) {
+    float2 part = make_float2(0.f, 0.f);
+    dot_chunk(w, xq, ncw, c, part);
+    const float sc = lds_f32(gs + (c >> 2));
+    ffma2(acc, part, make_float2(sc, sc));
+  } else {
+    dot_chunk(w, xq, ncw, c, acc);
+  }
+}
+
+template <typename CT>
+__device__ __forceinline__ CT zero_piece();
+template <>
+__device__ __forceinline__ uint4 zero_piece<uint4>() { return make_uint4(0, 0, 0, 0); }
+template <>
+__device__ __forceinline__ uint2 zero_piece<uint2>() { return make_uint2(0, 0); }
+
+template <typename CT>
+__device__ __forceinline__ void load_piece_i8(CT (&w)[QPIECE], const CT* row, int pc, int lane, int ncw) {
+#pragma unroll
+  for (int k = 0; k < QPIECE; ++k) {
+    const int c = pc * 32 * QPIECE + lane + 32 * k;
+    w[k] = (c < ncw) ? ldg_stream(row + c) : zero_piece<CT>();
+  }
+}
+
+template <int BITS>
 __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
+  using CT = typename Piece<BITS>::type;
   extern __shared__ __align__(16) uint8_t smem[];
   const int D = p.D;
   const int nch = D / 8;    // 16-byte bf16 chunks of x
-  const int ncw = D / 16;   // 16-byte code chunks of a weight row
+  const int ncw = D / 16;   // pieces of 16 codes in a weight row (16 bytes int8, 8 bytes int4)
+  const uint32_t row_bytes = (uint32_t)(D * BITS / 8);
+  const int rq = (int)(row_bytes / 16);  // 16-byte units of a row (D % 64 == 0 for int4)
+  const int ng = BITS == 4 ? D / G4 : 1;  // scales per row of W1 and of W3
   const int npg = (ncw + 32 * QPIECE - 1) / (32 * QPIECE);
   const int row0 = (int)(((long long)blockIdx.x * p.H) / gridDim.x);
   const int row1 = (int)(((long long)(blockIdx.x + 1) * p.H) / gridDim.x);
@@ -105,9 +229,9 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   sp += a16((size_t)D * 4);
   float* s2s = reinterpret_cast<float*>(sp);
   sp += a16((size_t)D * 4);
-  float* s1s = reinterpret_cast<float*>(sp);
-  float* s3s = s1s + cap;
-  sp += a16((size_t)cap * 8);
+  float* s1s = reinterpret_cast<float*>(sp);  // [cap][ng] scales of the block's W1 rows, then of its W3 rows
+  float* s3s = s1s + (size_t)cap * ng;
+  sp += a16((size_t)cap * ng * 8);
   int* l_unit = reinterpret_cast<int*>(sp);
   float* l_a = reinterpret_cast<float*>(l_unit + cap);
   float* l_h = l_a + cap;
@@ -115,11 +239,12 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   uint8_t* l_mask = reinterpret_cast<uint8_t*>(misc + 4);
   sp += a16((size_t)cap * 13 + 16);
   uint4* srows = reinterpret_cast<uint4*>(sp);
+  const CT* srow_p = reinterpret_cast<const CT*>(sp);  // the same area as rows of ncw pieces
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint4* G = static_cast<const uint4*>(p.gate_w);
-  const uint4* W3 = static_cast<const uint4*>(p.W3);
-  const uint4* W2t = static_cast<const uint4*>(p.W2t);
+  const CT* G = static_cast<const CT*>(p.gate_w);
+  const CT* W3 = static_cast<const CT*>(p.W3);
+  const CT* W2t = static_cast<const CT*>(p.W2t);
 
   if (tid == 0) {
     pdl_launch_dependents();
@@ -133,19 +258,19 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   const int R = min(p.pref_rows, nrows);
   const int nreg = max(0, min(QW, nrows - R));
   auto copy_rows = [&](int first, int n) {
-    const uint4* src = G + (size_t)(row0 + first) * ncw;
-    for (int i = tid; i < n * ncw; i += QT) cpa16(srows + i, src + i);
+    const uint4* src = reinterpret_cast<const uint4*>(G + (size_t)(row0 + first) * ncw);
+    for (int i = tid; i < n * rq; i += QT) cpa16(srows + i, src + i);
     cpa_commit();
   };
   for (int i = tid; i < D / 4; i += QT) cpa16(s2s + 4 * i, p.s2 + 4 * i);  // committed with the rows
-  for (int i = tid; i < row1 - row0; i += QT) {  // scales of the block's units (weights: before the wait)
-    s1s[i] = __ldg(p.s1 + row0 + i);
-    s3s[i] = __ldg(p.s3 + row0 + i);
+  for (int i = tid; i < (row1 - row0) * ng; i += QT) {  // scales of the block's units (weights: before the wait)
+    s1s[i] = __ldg(p.s1 + (size_t)row0 * ng + i);
+    s3s[i] = __ldg(p.s3 + (size_t)row0 * ng + i);
   }
   copy_rows(0, R);
   const int n_seq = warp < nreg ? npg : 0;
-  const uint4* my_row = G + (size_t)(row0 + R + warp) * ncw;
-  uint4 wa[QPIECE], wb[QPIECE];
+  const CT* my_row = G + (size_t)(row0 + R + warp) * ncw;
+  CT wa[QPIECE], wb[QPIECE];
   if (n_seq > 0) load_piece_i8(wa, my_row, 0, lane, ncw);
   if (n_seq > 1) load_piece_i8(wb, my_row, 1, lane, ncw);
   if (tid == 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.x), "r"((uint32_t)nch * 16u)
@@ -163,7 +288,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   __syncthreads();
 
   auto decide = [&](int q, float dotv) {  // dotv identical in every lane of the warp
-    const float z = s1s[q - row0] * dotv;
+    const float z = BITS == 4 ? dotv : s1s[q - row0] * dotv;  // int4: scaled per group already
     const float a = activation(p.act, z);
     const bool live = is_live(a, p.thr);
     if (lane == 0) {
@@ -175,15 +300,16 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
       }
     }
     if (live) {
-      pf_l2(W3 + (size_t)q * ncw, (uint32_t)D, lane, 32);
-      pf_l2(W2t + (size_t)q * ncw, (uint32_t)D, lane, 32);
+      pf_l2(W3 + (size_t)q * ncw, row_bytes, lane, 32);
+      pf_l2(W2t + (size_t)q * ncw, row_bytes, lane, 32);
     }
   };
   auto shared_rows = [&](int first, int n) {
     for (int i = warp; i < n; i += QW) {
-      const uint4* r = srows + (size_t)i * ncw;
+      const CT* r = srow_p + (size_t)i * ncw;
+      const float* gs = s1s + (size_t)(first + i) * ng;
       float2 acc = make_float2(0.f, 0.f);
-      for (int c = lane; c < ncw; c += 32) dot_chunk(lds16(r + c), xq, ncw, c, acc);
+      for (int c = lane; c < ncw; c += 32) dot_piece<BITS>(lds_piece(r + c), xq, ncw, c, acc, gs);
       decide(row0 + first + i, warp_sum(acc.x + acc.y));
     }
   };
@@ -194,11 +320,12 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   if (nb1 > 0) copy_rows(next, nb1);
 
   float2 acc = make_float2(0.f, 0.f);
-  auto consume = [&](const uint4(&w)[QPIECE], int pc) {
+  const float* my_gs = s1s + (size_t)(R + warp) * ng;
+  auto consume = [&](const CT(&w)[QPIECE], int pc) {
 #pragma unroll
     for (int k = 0; k < QPIECE; ++k) {
       const int c = pc * 32 * QPIECE + lane + 32 * k;
-      if (c < ncw) dot_chunk(w[k], xq, ncw, c, acc);
+      if (c < ncw) dot_piece<BITS>(w[k], xq, ncw, c, acc, my_gs);
     }
     if (pc == npg - 1) {
       const float d = warp_sum(acc.x + acc.y);
@@ -233,46 +360,32 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   const int cs0 = warp * per;
   const int cs_n = min(per, ncw - cs0);
   const bool owns = lane < cs_n;
-  const uint4* col = W2t + cs0 + lane;
+  const CT* col = W2t + cs0 + lane;
   const int RB = p.gather_rows;
   const bool dbl = (p.flags & FLAG_DOUBLE_ACT) != 0;
   float yr[16];
 #pragma unroll
   for (int v = 0; v < 16; ++v) yr[v] = 0.f;
-  auto fold = [&](const uint4& wv, float h) {
-    const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-    const float2 hh = make_float2(h, h);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      float2 v01, v23;
-      widen_i8x4(words[k], v01, v23);
-      float2 a = make_float2(yr[4 * k], yr[4 * k + 1]), b = make_float2(yr[4 * k + 2], yr[4 * k + 3]);
-      ffma2(a, v01, hh);
-      ffma2(b, v23, hh);
-      yr[4 * k] = a.x;
-      yr[4 * k + 1] = a.y;
-      yr[4 * k + 2] = b.x;
-      yr[4 * k + 3] = b.y;
-    }
-  };
-  uint4 r8[8];
+  auto fold = [&](const CT& wv, float h) { fold_piece(wv, h, yr); };
+  CT r8[8];
   for (int b0 = 0; b0 < n_live; b0 += RB) {
     const int nb = min(RB, n_live - b0);
-    for (int i = tid; i < nb * ncw; i += QT) {
-      const int u = i / ncw, c = i - u * ncw;
-      cpa16(srows + i, W3 + (size_t)l_unit[b0 + u] * ncw + c);
+    for (int i = tid; i < nb * rq; i += QT) {
+      const int u = i / rq, c = i - u * rq;
+      cpa16(srows + i, reinterpret_cast<const uint4*>(W3 + (size_t)l_unit[b0 + u] * ncw) + c);
     }
     cpa_commit();
 #pragma unroll
     for (int m = 0; m < 8; ++m)
-      r8[m] = (owns && m < nb) ? ldg_stream(col + (size_t)l_unit[b0 + m] * ncw) : make_uint4(0, 0, 0, 0);
+      r8[m] = (owns && m < nb) ? ldg_stream(col + (size_t)l_unit[b0 + m] * ncw) : zero_piece<CT>();
     cpa_wait();
     __syncthreads();
     for (int u = warp; u < nb; u += QW) {
-      const uint4* r = srows + (size_t)u * ncw;
+      const CT* r = srow_p + (size_t)u * ncw;
+      const int ur = l_unit[b0 + u] - row0;
       float2 acc2 = make_float2(0.f, 0.f);
-      for (int c = lane; c < ncw; c += 32) dot_chunk(lds16(r + c), xq, ncw, c, acc2);
-      const float uval = s3s[l_unit[b0 + u] - row0] * warp_sum(acc2.x + acc2.y);
+      for (int c = lane; c < ncw; c += 32) dot_piece<BITS>(lds_piece(r + c), xq, ncw, c, acc2, s3s + (size_t)ur * ng);
+      const float uval = BITS == 4 ? warp_sum(acc2.x + acc2.y) : s3s[ur] * warp_sum(acc2.x + acc2.y);
       if (lane == 0) l_h[b0 + u] = l_a[b0 + u] * (dbl ? activation(p.act, uval) : uval);
     }
     __syncthreads();
@@ -283,7 +396,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
       for (int j = 8; j < nb; j += 4) {
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-          r8[m] = j + m < nb ? ldg_stream(col + (size_t)l_unit[b0 + j + m] * ncw) : make_uint4(0, 0, 0, 0);
+          r8[m] = j + m < nb ? ldg_stream(col + (size_t)l_unit[b0 + j + m] * ncw) : zero_piece<CT>();
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           if (j + m < nb) fold(r8[m], l_h[b0 + j + m]);
@@ -308,7 +421,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
     for (int j = 0; j < n_live; j += 4) {
 #pragma unroll
       for (int m = 0; m < 4; ++m)
-        r8[m] = j + m < n_live ? ldg_stream(col + 32 + (size_t)l_unit[j + m] * ncw) : make_uint4(0, 0, 0, 0);
+        r8[m] = j + m < n_live ? ldg_stream(col + 32 + (size_t)l_unit[j + m] * ncw) : zero_piece<CT>();
 #pragma unroll
       for (int m = 0; m < 4; ++m)
         if (j + m < n_live) fold(r8[m], l_h[j + m]);
@@ -320,9 +433,10 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
     for (int i = tid; i < nrows; i += QT) p.mask[row0 + i] = l_mask[i];
 }
 
-// One block per row of a bf16 matrix: s = max|w| / 127, codes = round-half-even(w / s)
-// clamped to [-127, 127] (binary32 division, correctly rounded); s = 0 and codes 0 for
-// an all-zero row.
+// One block per row of a bf16 matrix: s = max|w| / QMAX, codes = round-half-even(w / s)
+// clamped to [-QMAX, QMAX] (binary32 division, correctly rounded); s = 0 and codes 0 for
+// an all-zero row.  QMAX = 127 (int8) or 7 (int4, one code per byte before packing).
+template <int QMAX>
 __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __restrict__ src,
                                                             int8_t* __restrict__ dst, float* __restrict__ scale,
                                                             int cols) {
@@ -338,26 +452,78 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
   amax = red[0];
 #pragma unroll
   for (int k = 1; k < 8; ++k) amax = fmaxf(amax, red[k]);
-  const float s = __fdiv_rn(amax, 127.f);
+  const float s = __fdiv_rn(amax, (float)QMAX);
   if (threadIdx.x == 0) scale[blockIdx.x] = s;
   for (int j = threadIdx.x; j < cols; j += 256) {
     int v = 0;
     if (s > 0.f) {
       v = __float2int_rn(__fdiv_rn(__uint_as_float((uint32_t)w[j] << 16), s));
-      v = max(-127, min(127, v));
+      v = max(-QMAX, min(QMAX, v));
     }
     q[j] = (int8_t)v;
   }
 }
 
+// One block per row of a bf16 matrix, one scale per group of G4 columns (int4 W1, W3):
+// s[row * (cols / G4) + g] = max|w over the group| / 7, codes as quantize_rows_kernel<7>.
+// A warp takes a group, two columns per lane.
+__global__ void __launch_bounds__(256) quantize_groups4_kernel(const uint16_t* __restrict__ src,
+                                                               int8_t* __restrict__ dst, float* __restrict__ scale,
+                                                               int cols) {
+  const int lane = threadIdx.x & 31, ng = cols / G4;
+  const uint16_t* w = src + (size_t)blockIdx.x * cols;
+  int8_t* q = dst + (size_t)blockIdx.x * cols;
+  for (int g = threadIdx.x >> 5; g < ng; g += 8) {
+    const float a = __uint_as_float((uint32_t)w[g * G4 + lane] << 16);
+    const float b = __uint_as_float((uint32_t)w[g * G4 + 32 + lane] << 16);
+    float amax = fmaxf(fabsf(a), fabsf(b));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = __fdiv_rn(amax, 7.f);
+    if (lane == 0) scale[(size_t)blockIdx.x * ng + g] = s;
+    int va = 0, vb = 0;
+    if (s > 0.f) {
+      va = max(-7, min(7, __float2int_rn(__fdiv_rn(a, s))));
+      vb = max(-7, min(7, __float2int_rn(__fdiv_rn(b, s))));
+    }
+    q[g * G4 + lane] = (int8_t)va;
+    q[g * G4 + 32 + lane] = (int8_t)vb;
+  }
+}
+
+// int4 codes, one per byte in [-7, 7] -> two per byte (code 2i in the low nibble); a code
+// outside that range sets DEV_ERR_CHECK in *err and packs as 0.
+__global__ void pack_int4_kernel(const int8_t* __restrict__ codes, uint8_t* __restrict__ out, size_t n_bytes,
+                                 int* err) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_bytes; i += (size_t)gridDim.x * blockDim.x) {
+    int lo = codes[2 * i], hi = codes[2 * i + 1];
+    if (lo < -7 || lo > 7 || hi < -7 || hi > 7) {
+      atomicOr(err, DEV_ERR_CHECK);
+      lo = (lo < -7 || lo > 7) ? 0 : lo;
+      hi = (hi < -7 || hi > 7) ? 0 : hi;
+    }
+    out[i] = (uint8_t)((lo & 0xF) | ((hi & 0xF) << 4));
+  }
+}
+
+// two int4 codes per byte -> one code per byte (sign-extended)
+__global__ void unpack_int4_kernel(const uint8_t* __restrict__ in, int8_t* __restrict__ codes, size_t n_bytes) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_bytes; i += (size_t)gridDim.x * blockDim.x) {
+    const int b = in[i];
+    codes[2 * i] = (int8_t)(((b & 0xF) ^ 8) - 8);
+    codes[2 * i + 1] = (int8_t)(((b >> 4) ^ 8) - 8);
+  }
+}
+
 }  // namespace
 
-StreamPlan plan_ffn_b1_i8(int D, int rows_cap) {
+StreamPlan plan_ffn_b1_i8(int D, int rows_cap, int bits) {
   StreamPlan pl;
-  const size_t row = (size_t)D;  // bytes of a code row
+  const size_t row = (size_t)D * bits / 8;  // bytes of a code row
+  const size_t ng = bits == 4 ? (size_t)(D / G4) : 1;  // W1 and W3 scales per row
   // two blocks per SM (the next call's blocks prefetch while this call runs):
   // at most 110 KB per block, of which the gate-row area takes what is left
-  const size_t fixed = 2 * a16((size_t)D * 4) + a16((size_t)rows_cap * 8) + a16((size_t)rows_cap * 13 + 16);
+  const size_t fixed = 2 * a16((size_t)D * 4) + a16((size_t)rows_cap * ng * 8) + a16((size_t)rows_cap * 13 + 16);
   const size_t budget = 110u * 1024u;
   const size_t free_area = budget > fixed ? budget - fixed : 0;
   pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, std::max<size_t>(1, free_area / row));
@@ -368,19 +534,49 @@ StreamPlan plan_ffn_b1_i8(int D, int rows_cap) {
 }
 
 cudaError_t ffn_b1_i8_prepare(size_t max_smem) {
-  cudaError_t e = cudaFuncSetAttribute(ffn_b1_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(ffn_b1_i8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  cudaError_t e = cudaSuccess;
+  for (auto k : {ffn_b1_i8_kernel<8>, ffn_b1_i8_kernel<4>}) {
+    if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+    if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
   return e;
 }
 
-cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s) {
-  return launch_pdl(ffn_b1_i8_kernel, dim3(grid), dim3(QT), smem, s, p);
+cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s, int bits) {
+  return bits == 4 ? launch_pdl(ffn_b1_i8_kernel<4>, dim3(grid), dim3(QT), smem, s, p)
+                   : launch_pdl(ffn_b1_i8_kernel<8>, dim3(grid), dim3(QT), smem, s, p);
 }
 
-cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols,
-                                 cudaStream_t s) {
+cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols, cudaStream_t s,
+                                 int qmax) {
   if (rows <= 0) return cudaSuccess;
-  quantize_rows_kernel<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(src_bf16), dst, scale, cols);
+  if (qmax == 7)
+    quantize_rows_kernel<7><<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(src_bf16), dst, scale, cols);
+  else
+    quantize_rows_kernel<127><<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(src_bf16), dst, scale, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_groups4(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols,
+                                    cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  quantize_groups4_kernel<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(src_bf16), dst, scale, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_int4(const int8_t* codes, void* packed, size_t n_codes, int* err, cudaStream_t s) {
+  if (n_codes == 0) return cudaSuccess;
+  const size_t n = n_codes / 2;
+  const int grid = (int)std::min<size_t>(4096, (n + 255) / 256);
+  pack_int4_kernel<<<grid, 256, 0, s>>>(codes, static_cast<uint8_t*>(packed), n, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_int4(const void* packed, int8_t* codes, size_t n_codes, cudaStream_t s) {
+  if (n_codes == 0) return cudaSuccess;
+  const size_t n = n_codes / 2;
+  const int grid = (int)std::min<size_t>(4096, (n + 255) / 256);
+  unpack_int4_kernel<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(packed), codes, n);
   return cudaGetLastError();
 }
 

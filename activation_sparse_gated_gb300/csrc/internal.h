@@ -176,15 +176,26 @@ cudaError_t launch_finalize_ordered(const float* ypart, int nblocks, void* y, in
 cudaError_t launch_finalize(float* yacc, void* y, int* ctrl, int* counts, int count_slot, int D, int nb,
                             int dtype, cudaStream_t s);
 
-// Weight-only int8, standard gate, one token per launch (ffn_b1_i8.cu): codes
-// W1q, W3q, W2tq [H, D] in gate_w, W3, W2t; scales s1, s3 [H], s2 [D] in the
-// params (each block scales its partial y by s2 before adding it up).
-StreamPlan plan_ffn_b1_i8(int D, int rows_cap);
+// Weight-only int8 or int4 (bits), standard gate, one token per launch (ffn_b1_i8.cu):
+// codes W1q, W3q, W2tq [H, D] in gate_w, W3, W2t (int4: two per byte, D / 2 bytes a
+// row, code 2b in the low nibble of byte b); scales s1, s3 [H] (int4: [H, D / 64], one
+// per group of 64 columns), s2 [D] in the params (each block scales its partial y by
+// s2 before adding it up).
+StreamPlan plan_ffn_b1_i8(int D, int rows_cap, int bits);
 cudaError_t ffn_b1_i8_prepare(size_t max_smem);
-cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s);
-// Per-row symmetric int8 quantisation of a bf16 matrix [rows, cols].
-cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols,
-                                 cudaStream_t s);
+cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s, int bits);
+// Per-row symmetric quantisation of a bf16 matrix [rows, cols] to one code per byte in
+// [-qmax, qmax] (127: int8, 7: int4 before packing).
+cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols, cudaStream_t s,
+                                 int qmax);
+// int4 W1, W3: one scale per group of 64 columns, scale[row * (cols / 64) + g], codes one per byte.
+cudaError_t launch_quantize_groups4(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols,
+                                    cudaStream_t s);
+constexpr int INT4_GROUP = 64;
+// int4 codes one per byte -> two per byte (n_codes even); a code outside [-7, 7] sets
+// DEV_ERR_CHECK in *err.  And back, sign-extended.
+cudaError_t launch_pack_int4(const int8_t* codes, void* packed, size_t n_codes, int* err, cudaStream_t s);
+cudaError_t launch_unpack_int4(const void* packed, int8_t* codes, size_t n_codes, cudaStream_t s);
 
 // t[b, :] = V x[b, :] in fp32 for the low-rank gate (one warp per row of V).
 cudaError_t launch_lopa_t(const void* V, const void* x, float* t, int r, int D, int B, int dtype,

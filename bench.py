@@ -15,7 +15,7 @@ peak and of the nominal 8 TB/s, the same figures for the dense bf16 FFN
 (cuBLAS through torch), and for the variants: the low-rank gate layer
 (D=2560, H'=9787, r=400, 32 rotated sets) alone and in the full form (tiled
 identity G, RMSNorm, double activation), the smooth SiLU gate with a live
-threshold, weight-only int8 weights, batches of 2 tokens (union gathers) and
+threshold, weight-only int8 and int4 weights, batches of 2 tokens (union gathers) and
 of 4 / 16 / 64 tokens on the tensor cores for both gates; an end-to-end figure
 with host buffers, SM clocks sampled during the timed region, and the fp64 CPU
 oracle timed on a bounded sample of the same workload.
@@ -625,6 +625,23 @@ def run_gpu(args):
                                   "frac_of_measured": qbytes * args.steps / (qt * 1e9) / peak,
                                   "speedup_vs_dense_bf16": us_dense / qus, "gpu_launches_per_call": 2}
         del qffns, qg
+        # weight-only int4 (codes in [-7, 7], two per byte), same layers
+        q4ffns = build_ffns(layers, dev, dtype="int4")
+        q4counts = live_counts(q4ffns, x, stream)
+        q4bytes = sum(H * D // 2 + 4 * H * (D // 64) + k * D + 4 * k * (D // 64) + 2 * elt * D + 4 * D
+                      for k in q4counts)
+        q4g = capture_step(q4ffns, x, y, stream)
+        q4t = time_graph(q4g, stream, args.steps, args.warmup)
+        q4us = 1e6 * q4t / (args.steps * n_tok)
+        extras["int4_weights"] = {"workload": WORKLOAD + ", weight-only int4 (codes in [-7, 7], two per byte; "
+                                  "fp32 scales per 64-column group of W1 and W3, per output channel of W2), "
+                                  "bf16 x and y", "weight_sets": n_sets,
+                                  "us_per_call": q4us, "tokens_per_s": 1e6 / q4us,
+                                  "mean_live": sum(q4counts) / len(q4counts),
+                                  "gbs": q4bytes * args.steps / (q4t * 1e9),
+                                  "frac_of_measured": q4bytes * args.steps / (q4t * 1e9) / peak,
+                                  "speedup_vs_dense_bf16": us_dense / q4us, "gpu_launches_per_call": 2}
+        del q4ffns, q4g
         extras["batched"] = batched_extras(ffns, layers, x, stream, args, peak)
         for k, v in lopa_batched.items():  # against the dense standard layer at the same batch (iso-parameter)
             dus = extras["batched"][k]["dense_bf16_us_per_call"]
@@ -838,7 +855,7 @@ def run_profile_case(args):
     import activation_sparse_gated_gb300 as sffn
     name, gate = PROFILE_CASES[args.profile_case]
     lw = syn.workload_layers(name, sets=1, gate=gate, **({} if args.sparsity is None else {"s": args.sparsity}))[0]
-    dtype = {"int8": "int8", "bf16": "bf16", "f32": "f32"}.get(args.dtype or "", lw.dtype)
+    dtype = {"int8": "int8", "int4": "int4", "bf16": "bf16", "f32": "f32"}.get(args.dtype or "", lw.dtype)
     ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, "relu", dtype)
     w = {k: (None if t is None else t.cuda()) for k, t in lw.tensors().items()}
     ffn.set_weights(w["W1"] if lw.r == 0 else w["U"], w["V"], w["W3"], w["W2"])
@@ -872,8 +889,8 @@ def main():
                     help="--profile-case: rewrite the gate's bias for this sparsity (default: the workload's)")
     ap.add_argument("--live-fraction", type=float, default=None,
                     help="--profile-case: the handle's live-fraction hint (picks the kernels of 3..16-token batches)")
-    ap.add_argument("--dtype", choices=["bf16", "f32", "int8"], default=None,
-                    help="--profile-case: handle dtype (default: the workload's; int8 quantises on the device)")
+    ap.add_argument("--dtype", choices=["bf16", "f32", "int8", "int4"], default=None,
+                    help="--profile-case: handle dtype (default: the workload's; int8 / int4 quantise on the device)")
     ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
                     help="(internal) time the oracle on this process's OpenMP threads for SECONDS, print JSON")
     args = ap.parse_args()

@@ -49,8 +49,10 @@ typedef struct sffn_s* sffn_t;
 
 /* element type of W1/U, V, W3, W2, x and y.  SFFN_I8W: weight-only int8 --
    W1, W3 and W2 are held as int8 codes with one fp32 scale per output channel,
-   x and y are bf16 (standard gate only; see sffn_set_weights_int8) */
-enum { SFFN_F32 = 0, SFFN_BF16 = 1, SFFN_I8W = 2 };
+   x and y are bf16 (standard gate only; see sffn_set_weights_int8).  SFFN_I4W:
+   the same with int4 codes in [-7, 7], held two per byte, and one scale per
+   group of 64 columns for W1 and W3 */
+enum { SFFN_F32 = 0, SFFN_BF16 = 1, SFFN_I8W = 2, SFFN_I4W = 3 };
 
 /* activation A: ReLU, or R-S+ (z * sigmoid(z) for z >= 0, 0 for z < 0;
    "Model casting: make sparsity a target") */
@@ -85,8 +87,9 @@ enum {
  *          with rank r, r % 8 == 0, r <= D
  *   act    SFFN_ACT_RELU, SFFN_ACT_RSP, or SFFN_ACT_SILU (z sigmoid(z) for every
  *          z: the smooth gate, never exactly zero; see sffn_set_live_threshold)
- *   dtype  SFFN_F32, SFFN_BF16, or SFFN_I8W (int8 weights, bf16 x and y;
- *          needs r == 0 and D % 16 == 0; flags may only hold SFFN_DOUBLE_ACT)
+ *   dtype  SFFN_F32, SFFN_BF16, SFFN_I8W (int8 weights, bf16 x and y; needs
+ *          r == 0 and D % 16 == 0; flags may only hold SFFN_DOUBLE_ACT), or
+ *          SFFN_I4W (int4 weights, the same with D % 64 == 0)
  * Returns NULL on error (see sffn_last_error()).  Allocates device memory:
  * 3*H*D (+ r*D + H*r) elements of weights plus O(B_max * (D + r + H)) bytes of
  * accumulators.
@@ -189,25 +192,34 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
                      const void* W2, void* stream);
 
 /*
- * Weight-only int8 handles (dtype SFFN_I8W).  "Model Casting and Low-Parameter
- * Gating", appendix Table 17, quantises cast models weight-only to int8 and
- * gives no scale convention; this library uses symmetric per-output-channel
- * scales: one fp32 scale per row of W1 and of W3 (per unit) and per row of W2
- * (per output element), s = max|w| / 127, code = round-half-to-even(w / s)
- * clamped to [-127, 127], both computed in binary32 (s = 0 and codes 0 for an
- * all-zero row).  The forward uses the dequantised weights q * s:
+ * Weight-only int8 and int4 handles (dtypes SFFN_I8W, SFFN_I4W).  "Model
+ * Casting and Low-Parameter Gating", appendix Table 17, quantises cast models
+ * weight-only to int8 and to int4 and gives no scale convention; this library
+ * uses symmetric per-output-channel scales: one fp32 scale per row of W1 and of
+ * W3 (per unit) and per row of W2 (per output element), s = max|w| / Q, code =
+ * round-half-to-even(w / s) clamped to [-Q, Q], both computed in binary32 (s = 0
+ * and codes 0 for an all-zero row); Q = 127 for int8, 7 for int4.  int4 W1 and
+ * W3 take one scale per group of 64 consecutive columns of a row instead (the
+ * max over the group): with one int4 scale per row a single large entry, such
+ * as a gate bias carried as a weight column, rounds the rest of the row to 0.
+ * The forward uses the dequantised weights q * s:
  *     z_i = s1_i (q1[i, :] . x),   u_i = s3_i (q3[i, :] . x),
  *     y_m = s2_m sum_{i live} q2[m, i] A(z_i) u_i
- * with fp32 sums and y rounded once to bf16.
+ * (int4: z_i = sum_g s1_{i,g} (q1[i, 64g .. 64g + 63] . x[64g .. 64g + 63]),
+ * likewise u_i) with fp32 sums and y rounded once to bf16.
  *
  * On such a handle sffn_set_weights takes bf16 W1[H, D], W3[H, D], W2[D, H]
  * (V ignored) and quantises them on the device.  sffn_set_weights_int8 loads
  * codes and scales quantised elsewhere (a quantisation-aware-trained layer):
  *   W1q, W3q [H, D] int8 with s1, s3 [H] fp32;  W2q [D, H] int8 with s2 [D] fp32
- * (host or device pointers, any alignment).  sffn_get_weights_int8 copies the
- * handle's codes and scales out in the same layout (any pointer may be NULL to
- * skip that array).  Both return after `stream` has finished the copies, and
- * return SFFN_ERR_STATE on a handle of another dtype.
+ * (host or device pointers, any alignment).  On an SFFN_I4W handle the code
+ * arrays hold one int4 code per byte, each in [-7, 7] (the library packs them
+ * two per byte; a code outside that range gives SFFN_ERR_ARG and leaves the
+ * handle without weights), and s1, s3 are [H, D / 64] (scale of row i, columns
+ * 64 g .. 64 g + 63 at i * D / 64 + g).  sffn_get_weights_int8 copies the handle's codes (one per
+ * byte) and scales out in the same layout (any pointer may be NULL to skip that
+ * array).  Both return after `stream` has finished the copies, and return
+ * SFFN_ERR_STATE on a handle of another dtype.
  */
 int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const int8_t* W3q, const float* s3,
                           const int8_t* W2q, const float* s2, void* stream);

@@ -42,7 +42,7 @@ def test_constants_match_header():
     for name in ("SFFN_F32", "SFFN_BF16", "SFFN_ACT_RELU", "SFFN_ACT_RSP", "SFFN_OK", "SFFN_ERR_ARG",
                  "SFFN_ERR_ALIGN", "SFFN_ERR_DTYPE", "SFFN_ERR_CUDA", "SFFN_ERR_TIMEOUT",
                  "SFFN_ERR_STATE", "SFFN_ERR_NOMEM", "SFFN_ERR_DEVICE", "SFFN_GATE_TILED_G", "SFFN_GATE_RMSNORM",
-                 "SFFN_DOUBLE_ACT", "SFFN_DETERMINISTIC", "SFFN_ACT_SILU", "SFFN_I8W"):
+                 "SFFN_DOUBLE_ACT", "SFFN_DETERMINISTIC", "SFFN_ACT_SILU", "SFFN_I8W", "SFFN_I4W"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m and int(m.group(1)) == getattr(sffn, name), name
     assert int(re.search(r"#define SFFN_MAX_BATCH (\d+)", text).group(1)) == sffn.SFFN_MAX_BATCH
@@ -100,12 +100,12 @@ def test_create_ex_rejects_bad_options_before_touching_the_device(lib, r, flags)
     assert "flags" in sffn.sffn_last_error() or "low-rank" in sffn.sffn_last_error()
 
 
-@pytest.mark.parametrize("dtype", [sffn.SFFN_F32, sffn.SFFN_I8W])
+@pytest.mark.parametrize("dtype", [sffn.SFFN_F32, sffn.SFFN_I8W, sffn.SFFN_I4W])
 def test_deterministic_option_is_bf16_only_checked_on_host(lib, dtype):
     h = lib.sffn_create_ex(512, 1024, 0, sffn.SFFN_ACT_RELU, dtype, sffn.SFFN_DETERMINISTIC)
     assert not h
     msg = sffn.sffn_last_error()
-    assert "deterministic" in msg or (dtype == sffn.SFFN_I8W and "int8" in msg), msg
+    assert "deterministic" in msg or (dtype in (sffn.SFFN_I8W, sffn.SFFN_I4W) and "int" in msg), msg
 
 
 def test_live_threshold_rejects_bad_values_on_host(lib):
@@ -116,3 +116,12 @@ def test_live_threshold_rejects_bad_values_on_host(lib):
 def test_live_fraction_hint_rejects_a_null_handle_on_host(lib):
     import ctypes
     assert lib.sffn_set_live_fraction_hint(None, ctypes.c_float(0.1)) == sffn.SFFN_ERR_ARG
+
+
+@pytest.mark.parametrize("args", [(96, 64, 0, 0), (64, 64, 8, 0), (64, 64, 0, 8)])
+def test_int4_handle_shape_rules_checked_on_host(lib, args):
+    """int4 weights: standard gate only, D a multiple of 64 (the scale groups), no low-rank option."""
+    D, H, r, flags = args
+    h = lib.sffn_create_ex(D, H, r, sffn.SFFN_ACT_RELU, sffn.SFFN_I4W, flags)
+    assert not h
+    assert "int4" in sffn.sffn_last_error()

@@ -1,4 +1,4 @@
-"""GPU parity of the weight-only int8 path (dtype SFFN_I8W) against the oracle.
+"""GPU parity of the weight-only int8 and int4 paths (dtypes SFFN_I8W, SFFN_I4W) against the oracle.
 
 * The device quantiser must give the oracle's codes and scales bit for bit
   (an integer result decided in binary32 on both sides).
@@ -6,6 +6,8 @@
   q * s, fp64) within the bf16 output bar, with the live set identical outside
   the 1e-2 band, for every activation, the live threshold, the double
   activation and batches (one streaming pass per token).
+* int4 is the same convention with codes in [-7, 7] (held two per byte on the
+  device); every forward case runs for both.
 """
 import numpy as np
 import pytest
@@ -21,6 +23,8 @@ TOL = 2e-2
 BAND = 1e-2
 K_ELEM = 1.0  # element-wise bar: max |y - y*| <= K_ELEM * TOL * rms(y*) (derivation in test_gpu_parity.py)
 ACTS = {"relu": oracle.RELU, "rsp": oracle.RSP, "silu": oracle.SILU}
+QMAX = {"int8": 127, "int4": 7}
+DTYPES = ["int8", "int4"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,13 +42,15 @@ def floats(lw):
     return [t[k].float().numpy() for k in ("W1", "W3", "W2")]
 
 
-def oracle_codes(lw):
+def oracle_codes(lw, dtype="int8"):
     W1, W3, W2 = floats(lw)
+    if dtype == "int4":  # W1, W3 one scale per group of 64 columns, W2 one per row
+        return oracle.quantize_int4(W1, W3, W2)
     return oracle.quantize_rows(W1) + oracle.quantize_rows(W3) + oracle.quantize_rows(W2)
 
 
-def make_int8(lw, act="relu", flags=0, thr=0.0):
-    ffn = sffn.SparseFFN(lw.D, lw.H, 0, act, "int8", flags=flags)
+def make_int8(lw, act="relu", flags=0, thr=0.0, dtype="int8"):
+    ffn = sffn.SparseFFN(lw.D, lw.H, 0, act, dtype, flags=flags)
     t = lw.tensors()
     ffn.set_weights(t["W1"].cuda(), None, t["W3"].cuda(), t["W2"].cuda())
     if thr:
@@ -89,12 +95,14 @@ def act_abs(act, z):
     return zp if act == "relu" else np.where(z > 0, z / (1.0 + np.exp(-z)), 0.0)
 
 
-def check(lw, x, y, counts, masks, act="relu", flags=0, thr=0.0, codes=None):
-    q1, s1, q3, s3, q2, s2 = codes if codes is not None else oracle_codes(lw)
+def check(lw, x, y, counts, masks, act="relu", flags=0, thr=0.0, codes=None, dtype="int8"):
+    q1, s1, q3, s3, q2, s2 = codes if codes is not None else oracle_codes(lw, dtype)
+    group = oracle.INT4_GROUP if dtype == "int4" else None
     yref, z, n = oracle.ffn_dense_q8(lw.D, lw.H, ACTS[act], flags, q1, s1, q3, s3, q2, s2,
-                                     syn.oracle_view(x), thr=thr)
+                                     syn.oracle_view(x), thr=thr, group=group)
     A = act_abs(act, z)
-    W3 = q3.astype(np.float64) * np.asarray(s3, np.float64)[:, None]
+    s3v = np.asarray(s3, np.float64)
+    W3 = q3.astype(np.float64) * (np.repeat(s3v, group, axis=1) if group else s3v[:, None])
     W2 = q2.astype(np.float64) * np.asarray(s2, np.float64)[:, None]
     xv = x.double().numpy()
     for b in range(x.shape[0]):
@@ -149,72 +157,80 @@ def test_device_quantiser_is_bitexact(D, H):
     assert got[0][2, :6].tolist() == [127, 0, 2, -2, 64, -64] and got[1][2] == 2.0
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("act,flags,thr", [("relu", 0, 0.0), ("rsp", 0, 0.0), ("relu", sffn.SFFN_DOUBLE_ACT, 0.0),
                                            ("silu", 0, 0.3), ("relu", 0, 0.05)])
 @pytest.mark.parametrize("B", [1, 3])
-def test_forward_matches_oracle(act, flags, thr, B):
+def test_forward_matches_oracle(act, flags, thr, B, dtype):
     kw = {"shift": 0.0} if act == "silu" else {}
     lw = syn.standard_layer(512, 1500, dtype="bf16", seed=82, **kw)
     x = syn.tokens(2 * B, 512, dtype="bf16", seed=83)
-    ffn = make_int8(lw, act, flags, thr)
+    ffn = make_int8(lw, act, flags, thr, dtype)
     y, c, m = run(ffn, x, B=B)
-    check(lw, x, y, c, m, act, flags, thr)
+    check(lw, x, y, c, m, act, flags, thr, dtype=dtype)
 
 
-def test_full_size_workload():
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_full_size_workload(dtype):
     name = "std-bf16-D2560-H7168-B1"
     lw = syn.workload_layers(name, sets=1)[0]
     x = syn.workload_tokens(name, 6)
-    ffn = make_int8(lw)
+    ffn = make_int8(lw, dtype=dtype)
     y, c, m = run(ffn, x)
-    _, _, n = check(lw, x, y, c, m)
+    _, _, n = check(lw, x, y, c, m, dtype=dtype)
     assert 0.02 < n.mean() / lw.H < 0.3
 
 
-def test_d4096_shape():
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_d4096_shape(dtype):
     lw = syn.workload_layers("sweep-bf16-D4096-H14336", sets=1, s=0.75)[0]
     x = syn.workload_tokens("sweep-bf16-D4096-H14336", 2)
-    ffn = make_int8(lw)
+    ffn = make_int8(lw, dtype=dtype)
     y, c, m = run(ffn, x)
-    check(lw, x, y, c, m)
+    check(lw, x, y, c, m, dtype=dtype)
 
 
-@pytest.mark.parametrize("D,H", [(16, 1), (16, 37), (64, 151), (64, 153), (48, 300)])
-def test_ragged_shapes(D, H):
+@pytest.mark.parametrize("dtype,D,H", [("int8", 16, 1), ("int8", 16, 37), ("int8", 64, 151), ("int8", 64, 153),
+                                       ("int8", 48, 300), ("int4", 64, 1), ("int4", 64, 37), ("int4", 64, 151),
+                                       ("int4", 192, 300), ("int4", 4096, 40)])
+def test_ragged_shapes(dtype, D, H):
     lw = syn.standard_layer(D, H, dtype="bf16", seed=84)
     x = syn.tokens(3, D, dtype="bf16", seed=85)
-    ffn = make_int8(lw)
+    ffn = make_int8(lw, dtype=dtype)
     y, c, m = run(ffn, x)
-    check(lw, x, y, c, m)
+    check(lw, x, y, c, m, dtype=dtype)
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("shift", [+20.0, -20.0])
-def test_all_live_and_none_live(shift):
+def test_all_live_and_none_live(shift, dtype):
     lw = syn.standard_layer(256, 700, dtype="bf16", seed=86, shift=shift)
     x = syn.tokens(2, 256, dtype="bf16", seed=87)
-    ffn = make_int8(lw)
+    ffn = make_int8(lw, dtype=dtype)
     y, c, m = run(ffn, x)
-    check(lw, x, y, c, m)
+    check(lw, x, y, c, m, dtype=dtype)
     if shift < 0:
         assert (c == 0).all() and (y == 0).all()
     else:
         assert (c == lw.H).all()
 
 
-def test_external_codes_and_round_trip():
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_external_codes_and_round_trip(dtype):
     """Codes and scales quantised by the oracle, loaded with sffn_set_weights_int8, give the
-    same layer as the device quantiser, and read back unchanged."""
+    same layer as the device quantiser, and read back unchanged (int4: packed two per byte on
+    the device and unpacked on the way out)."""
     lw = syn.standard_layer(384, 1200, dtype="bf16", seed=88)
     x = syn.tokens(4, 384, dtype="bf16", seed=89)
-    codes = oracle_codes(lw)
-    ext = sffn.SparseFFN(384, 1200, 0, "relu", "int8")
+    codes = oracle_codes(lw, dtype)
+    ext = sffn.SparseFFN(384, 1200, 0, "relu", dtype)
     ext.set_weights_int8(*[torch.from_numpy(a).cuda() for a in codes])
     back = [a.cpu().numpy() for a in ext.int8_weights()]
     for g, w in zip(back, codes):
         assert np.array_equal(g, w)
     y1, c1, m1 = run(ext, x)
-    y2, c2, m2 = run(make_int8(lw), x)
-    check(lw, x, y1, c1, m1, codes=codes)
+    y2, c2, m2 = run(make_int8(lw, dtype=dtype), x)
+    check(lw, x, y1, c1, m1, codes=codes, dtype=dtype)
     assert np.array_equal(m1, m2) and np.array_equal(c1, c2)
     np.testing.assert_allclose(y1, y2, rtol=1e-2, atol=1e-6)
 
@@ -230,4 +246,54 @@ def test_int8_argument_errors():
     with pytest.raises(sffn.SffnError) as e:
         bf.set_weights_int8(q, s, q, s, torch.zeros(256, 512, dtype=torch.int8, device="cuda"),
                             torch.ones(256, device="cuda"))
+    assert e.value.code == sffn.SFFN_ERR_STATE
+
+
+def crafted_rows_int4(W):
+    """The int4 hand-worked rows of the oracle pins (ties, an all-zero row, a scale of 2)."""
+    W = W.copy()
+    W[0, :6] = [7.0, -3.5, 2.5, 0.5, -1.5, 0.0]
+    W[0, 6:] = 0.0
+    W[1, :] = 0.0
+    W[2, :6] = [-14.0, 3.0, 5.0, 1.0, 13.0, -9.0]
+    W[2, 6:] = 0.0
+    return W
+
+
+@pytest.mark.parametrize("D,H", [(512, 1500), (2560, 7168)])
+def test_device_quantiser_is_bitexact_int4(D, H):
+    lw = syn.standard_layer(D, H, dtype="bf16", seed=91)
+    t = lw.tensors()
+    W1 = crafted_rows_int4(t["W1"].float().numpy())
+    W1b = torch.from_numpy(W1).bfloat16()
+    assert np.array_equal(W1b.float().numpy(), W1)
+    ffn = sffn.SparseFFN(D, H, 0, "relu", "int4")
+    ffn.set_weights(W1b.cuda(), None, t["W3"].cuda(), t["W2"].cuda())
+    got = [a.cpu().numpy() for a in ffn.int8_weights()]
+    want = oracle.quantize_int4(W1, t["W3"].float().numpy(), t["W2"].float().numpy())
+    for g, w, name in zip(got, want, ("W1q", "s1", "W3q", "s3", "W2q", "s2")):
+        assert g.shape == w.shape, name
+        assert np.array_equal(g.view(np.uint8) if g.dtype == np.int8 else g.view(np.uint32),
+                              w.view(np.uint8) if w.dtype == np.int8 else w.view(np.uint32)), name
+    # the crafted rows fill the first group of 64 columns (the rest of it zero)
+    assert got[0][0, :6].tolist() == [7, -4, 2, 0, -2, 0] and got[1][0, 0] == 1.0
+    assert (got[0][1] == 0).all() and (got[1][1] == 0.0).all()
+    assert got[0][2, :6].tolist() == [-7, 2, 2, 0, 6, -4] and got[1][2, 0] == 2.0
+
+
+def test_int4_argument_errors():
+    with pytest.raises(sffn.SffnError):
+        sffn.SparseFFN(256, 512, 32, "relu", "int4")          # low-rank gate
+    with pytest.raises(sffn.SffnError):
+        sffn.SparseFFN(96, 512, 0, "relu", "int4")            # D % 64 != 0
+    h = sffn.SparseFFN(256, 512, 0, "relu", "int4")
+    q = torch.zeros(512, 256, dtype=torch.int8, device="cuda")
+    q[3, 7] = 8                                                # outside [-7, 7]
+    s = torch.ones(512, 4, device="cuda")
+    with pytest.raises(sffn.SffnError) as e:
+        h.set_weights_int8(q, s, torch.zeros_like(q), s, torch.zeros(256, 512, dtype=torch.int8, device="cuda"),
+                           torch.ones(256, device="cuda"))
+    assert e.value.code == sffn.SFFN_ERR_ARG
+    with pytest.raises(sffn.SffnError) as e:                   # and the handle has no weights
+        h(torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda"))
     assert e.value.code == sffn.SFFN_ERR_STATE
