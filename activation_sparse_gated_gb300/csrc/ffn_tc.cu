@@ -8,7 +8,8 @@
 // it -- the union of the live sets, which the pages warn grows with the batch
 // (at 90 % sparsity it holds 57 % of the units at B = 8 and 82 % at B = 16).
 // From a handful of tokens up, this path therefore streams every unit slice
-// and lets the gate decide, per token and unit, what reaches y:
+// and lets the gate decide, per token and unit, what reaches y (the union-skip
+// kernels of ffn_tcg.cu take small batches whose union is small):
 //
 //   gate-up kernel, one block per slice of NU units:
 //     [Z ; P][slice, :] = [W1 ; W3][slice, :] X^T   one pass; the W1 and W3 rows
@@ -22,17 +23,19 @@
 //   down kernel, one block per (128-wide slice of y, range of units):
 //     y^T[d-slice, :] += W2^T[units, d-slice]^T h   MN-major A (W2^T rows as
 //               stored), h the N = NB operand (one TMA box of NB rows);
-//               fp32 atomics into an accumulator; the last block of a y slice
-//               (a ticket per slice) rounds it into y and clears it, and block
-//               0 publishes the per-token live counts.
+//               the blocks of a y slice form a thread-block cluster and sum
+//               their partial tiles through distributed shared memory, each
+//               rounding its share of the tokens into y (where the clusters do
+//               not fit: fp32 atomics into an accumulator and a last block per
+//               slice, found by a ticket); block 0 publishes the live counts.
 //
 // Low-rank gate ("LoPA Gating: moving the ceiling", W1 = UV), three kernels:
 //   t kernel: the gate-up kernel's low-rank form with no U chunks and V in
 //             place of W3, so it computes T = V X^T; its blocks split K: one
-//             block per (128 rows of V, range of D), partial sums added into
-//             an fp32 accumulator, and the last block of a row tile (a
-//             ticket) stores t_b as a bf16 pair, t_hi in rows [0, NB) and
-//             t_lo in rows [NB, 2 NB) of one buffer, and clears the sums;
+//             block per (128 rows of V, range of D), the splits of a row tile
+//             one cluster summing through distributed shared memory (else
+//             fp32 atomics and a last block), which store t_b as a bf16 pair,
+//             t_hi in rows [0, NB) and t_lo in rows [NB, 2 NB) of one buffer;
 //   gate-up:  the first K chunk groups run over the r columns of U, two MMAs
 //             per K step into the Z accumulator (U t_hi, then U t_lo), the
 //             remaining groups over the D columns of W3 into the P accumulator;
