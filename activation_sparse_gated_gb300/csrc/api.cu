@@ -528,7 +528,7 @@ int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* 
 
 namespace {
 // Batches of 3..16 tokens (bf16) read only the union of the live sets when that pays: the expected
-// union u = 1 - (1 - rho)^B is at most a quarter of the units and the W3 and W2 bytes of the other units
+// union u = 1 - (1 - rho)^B is at most 30 % of the units and the W3 and W2 bytes of the other units
 // come to at least 128 MB (standard gate) or 64 MB (low-rank gate, whose streaming form pays a t kernel
 // and whose union form streams only U before the union is known).  Below that the streaming kernels win
 // on this GPU: they stream every slice at close to the copy bandwidth, while the union's scattered rows
@@ -539,7 +539,7 @@ bool use_union_skip(const sffn_s* h, int B) {
   if (h->live_frac < 0.f || B > 16) return false;
   const double u = 1.0 - std::pow(1.0 - (double)h->live_frac, B);
   const double saved = (1.0 - u) * 2.0 * 2.0 * (double)h->H * (double)h->D;
-  return u <= 0.25 && saved >= (h->r > 0 ? 64e6 : 128e6);
+  return u <= 0.30 && saved >= (h->r > 0 ? 64e6 : 128e6);
 }
 }  // namespace
 

@@ -163,8 +163,8 @@ int sffn_set_live_threshold(sffn_t h, float thr);
  * batching).  The union-skip kernels read the gate (W1, or U after t = V x) in
  * full and then only the union's rows of W3 and W2^T; the streaming kernels
  * read every slice of W3 and W2 and let the gate zero the dead terms.  The
- * forward takes the union-skip kernels when the expected union is at most a
- * quarter of the units and the W3 and W2 bytes of the other units come to at
+ * forward takes the union-skip kernels when the expected union is at most 30 %
+ * of the units and the W3 and W2 bytes of the other units come to at
  * least 128 MB (64 MB for the low-rank gate), else the streaming kernels:
  * on this GPU a gathered row arrives at a fraction of the streaming bandwidth,
  * and the rows can only be requested once the gate is known.  Both compute the
