@@ -98,14 +98,17 @@ __device__ __forceinline__ void widen_i8x4(uint32_t word, float2& v01, float2& v
 }
 
 // 8 int4 codes (one 32-bit word, code j in bits 4j .. 4j + 3) -> 8 exact fp32
-// values, v[k] = (code 2k, code 2k + 1).
+// values, v[k] = (code 2k, code 2k + 1).  The biased even and odd codes are split
+// into the bytes of two words once (a mask, a shift and a mask); each code then
+// takes one byte permute into the low byte of 2^23, as in widen_i8x4.
 __device__ __forceinline__ void widen_i4x8(uint32_t word, float2 (&v)[4]) {
   const uint32_t w = word ^ 0x88888888u;
+  const uint32_t even = w & 0x0F0F0F0Fu, odd = (w >> 4) & 0x0F0F0F0Fu;
   const float2 bias = make_float2(-8388616.f, -8388616.f);
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    v[k] = fadd2(make_float2(__uint_as_float(((w >> (8 * k)) & 0xFu) | 0x4B000000u),
-                             __uint_as_float(((w >> (8 * k + 4)) & 0xFu) | 0x4B000000u)),
+    v[k] = fadd2(make_float2(__uint_as_float(__byte_perm(even, 0x4B000000u, 0x7540u + k)),
+                             __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7540u + k))),
                  bias);
 }
 
