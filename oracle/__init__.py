@@ -65,6 +65,8 @@ def _bind(path):
     lib.oracle_ffn_dense_q8.argtypes = [ip] * 5 + [ctypes.c_double] + [vp] * 10
     lib.oracle_ffn_dense_qg.restype = ip
     lib.oracle_ffn_dense_qg.argtypes = [ip] * 5 + [ctypes.c_double, ip] + [vp] * 10
+    lib.oracle_ffn_lopa_q8.restype = ip
+    lib.oracle_ffn_lopa_q8.argtypes = [ip] * 6 + [ctypes.c_double] + [vp] * 12
     return lib
 
 
@@ -101,6 +103,9 @@ class Variant:
 
     def quantize_rows(self, W, qmax=127, group=None):
         return _quantize_rows(W, self._lib, qmax, group)
+
+    def ffn_lopa_q8(self, D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, x, thr=0.0):
+        return _ffn_lopa_q8(D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, x, thr, self._lib)
 
     def ffn_dense_q8(self, D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, group=None):
         return _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr, self._lib, group)
@@ -235,6 +240,30 @@ def _ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, lib=None
     if rc != 0:
         raise RuntimeError(f"oracle_ffn_dense_qg failed with code {rc}")
     return y, z, n_live
+
+
+def _ffn_lopa_q8(D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, x, thr=0.0, lib=None):
+    i8 = lambda a, n: np.ascontiguousarray(a, dtype=np.int8).reshape(n)  # noqa: E731
+    f32 = lambda a, n: np.ascontiguousarray(a, dtype=np.float32).reshape(n)  # noqa: E731
+    qU, qV, q3, q2 = i8(qU, H * r), i8(qV, r * D), i8(q3, H * D), i8(q2, D * H)
+    sU, sV, s3, s2 = f32(sU, H), f32(sV, r), f32(s3, H), f32(s2, D)
+    x = _as_input(x, BF16)
+    B = x.size // D
+    y = np.zeros((B, D), dtype=np.float64)
+    z = np.zeros((B, H), dtype=np.float64)
+    n_live = np.zeros(B, dtype=np.int32)
+    rc = (lib or _load()).oracle_ffn_lopa_q8(D, H, r, act, B, flags, float(thr), _ptr(qU), _ptr(sU), _ptr(qV),
+                                             _ptr(sV), _ptr(q3), _ptr(s3), _ptr(q2), _ptr(s2), _ptr(x), _ptr(y),
+                                             _ptr(z), _ptr(n_live))
+    if rc != 0:
+        raise RuntimeError(f"oracle_ffn_lopa_q8 failed with code {rc}")
+    return y, z, n_live
+
+
+def ffn_lopa_q8(D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, x, thr=0.0):
+    """The low-rank gate z = U (V x) with int8 weights, one scale per row of each matrix (qU [H, r],
+    qV [r, D], q3 [H, D], q2 [D, H]); bf16 x.  flags: 0 or FLAG_DOUBLE_ACT.  Returns (y, z, n_live)."""
+    return _ffn_lopa_q8(D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, x, thr)
 
 
 def ffn_dense_q8(D, H, act, flags, q1, s1, q3, s3, q2, s2, x, thr=0.0, group=None):

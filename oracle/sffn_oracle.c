@@ -460,3 +460,52 @@ int oracle_ffn_dense_q8(int D, int H, int act, int B, int flags, double thr,
                         double* y, double* z, int* n_live) {
   return oracle_ffn_dense_qg(D, H, act, B, flags, thr, D, q1, s1, q3, s3, q2, s2, x, y, z, n_live);
 }
+
+/*
+ * The low-rank gate ("LoPA Gating: moving the ceiling", the plain form
+ * z = U (V x)) with weight-only int8 weights, one scale per row of every
+ * matrix: qU [H, r] with sU [H], qV [r, D] with sV [r], q3 [H, D] with s3 [H],
+ * q2 [D, H] with s2 [D]; x [B, D] bf16 bits.
+ *     t = dequant(V) x,  z_i = dequant(U)[i, :] . t,  then as oracle_ffn_dense_q8.
+ * flags may only hold OR_FLAG_DOUBLE_ACT.  Outputs as oracle_ffn_dense_ex.
+ */
+int oracle_ffn_lopa_q8(int D, int H, int r, int act, int B, int flags, double thr,
+                       const int8_t* qU, const float* sU, const int8_t* qV, const float* sV,
+                       const int8_t* q3, const float* s3, const int8_t* q2, const float* s2, const void* x,
+                       double* y, double* z, int* n_live) {
+  if (check_args(D, H, r, act, OR_BF16, B, flags, 0.0, thr) || r <= 0) return -1;
+  if (flags & ~OR_FLAG_DOUBLE_ACT) return -1;
+  double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+  double* t = (double*)malloc(sizeof(double) * (size_t)r);
+  double* zb = (double*)malloc(sizeof(double) * (size_t)H);
+  double* g = (double*)malloc(sizeof(double) * (size_t)H);
+  double* row = (double*)malloc(sizeof(double) * (size_t)(D > H ? D : H));
+  if (!xd || !t || !zb || !g || !row) {
+    free(xd); free(t); free(zb); free(g); free(row);
+    return -2;
+  }
+  for (int b = 0; b < B; ++b) {
+    widen_row(x, OR_BF16, (size_t)b * D, D, xd);
+    for (int k = 0; k < r; ++k) {  /* t = V x */
+      dequant_row(qV, sV, (size_t)k, D, row);
+      t[k] = dot(row, xd, D);
+    }
+    for (int i = 0; i < H; ++i) {  /* z = U t, u = W3 x, g = A(z) u */
+      dequant_row(qU, sU, (size_t)i, r, row);
+      zb[i] = dot(row, t, r);
+      dequant_row(q3, s3, (size_t)i, D, row);
+      const double u = dot(row, xd, D);
+      g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);
+    }
+    for (int m = 0; m < D; ++m) {  /* y_m = sum_i (q2[m, i] s2[m]) g_i, i ascending */
+      dequant_row(q2, s2, (size_t)m, H, row);
+      y[(size_t)b * D + m] = dot(row, g, H);
+    }
+    int cnt = 0;
+    for (int i = 0; i < H; ++i) cnt += (fabs(activation(act, zb[i])) > thr);
+    if (n_live) n_live[b] = cnt;
+    if (z) memcpy(z + (size_t)b * H, zb, sizeof(double) * (size_t)H);
+  }
+  free(xd); free(t); free(zb); free(g); free(row);
+  return 0;
+}

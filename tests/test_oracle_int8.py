@@ -241,3 +241,55 @@ def test_grouped_forward_hand_worked():
     # u = 1 (1 + 1) + 0.25 (0 + 1) = 2.25; h = 8.5 * 2.25 = 19.125
     assert z.tolist() == [[8.5]] and n.tolist() == [1]
     assert y.tolist() == [[19.125, 19.125, -38.25, 9.5625]]
+
+
+# The low-rank gate ("LoPA Gating: moving the ceiling", z = U (V x)) with int8 weights, one scale per
+# row of U, V, W3 and W2.
+
+@pytest.mark.parametrize("act,flags", [(RELU, 0), (RSP, oracle.FLAG_DOUBLE_ACT), (SILU, 0)])
+def test_lopa_q8_equals_float_oracle_on_exact_weights(act, flags):
+    """Codes with power-of-two scales: q * s is exact in binary32, so the int8 low-rank forward must equal
+    the pinned float32 low-rank oracle on the dequantised weights."""
+    D, H, r, B = 40, 70, 16, 3
+    rng = np.random.default_rng(9)
+
+    def mat(rows, cols):
+        q = rng.integers(-127, 128, size=(rows, cols)).astype(np.int8)
+        q[np.arange(rows), rng.integers(0, cols, size=rows)] = rng.choice([-127, 127], size=rows)
+        s = np.ldexp(1.0, -rng.integers(4, 9, size=rows)).astype(np.float32)
+        return q, s, (q.astype(np.float32) * s[:, None]).astype(np.float32)
+
+    (qU, sU, U), (qV, sV, V), (q3, s3, W3), (q2, s2, W2) = mat(H, r), mat(r, D), mat(H, D), mat(D, H)
+    for q, s, W in ((qU, sU, U), (qV, sV, V)):
+        qq, ss = oracle.quantize_rows(W)
+        assert np.array_equal(qq, q) and np.array_equal(ss, s)
+    xf = torch.from_numpy(rng.standard_normal((B, D)).astype(np.float32)).bfloat16().float().numpy()
+    thr = 0.05 if act == SILU else 0.0
+    y8, z8, n8 = oracle.ffn_lopa_q8(D, H, r, act, flags, qU, sU, qV, sV, q3, s3, q2, s2, bf16_bits(xf), thr=thr)
+    yf, zf, nf = oracle.ffn_dense_ex(D, H, r, act, F32, flags, None, U, V, W3, W2, xf, thr=thr)
+    np.testing.assert_allclose(z8, zf, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y8, yf, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(n8, nf)
+
+
+def test_lopa_q8_hand_worked():
+    """D = 2, H = 2, r = 1: t = 0.5 (2 * 3 - 1 * 1) = 2.5; z = (0.25 * 4, 0.25 * -2) t = (2.5, -1.25)."""
+    qV = np.array([[2, -1]], np.int8); sV = np.array([0.5], np.float32)
+    qU = np.array([[4], [-2]], np.int8); sU = np.array([0.25, 0.25], np.float32)
+    q3 = np.array([[1, 0], [0, 1]], np.int8); s3 = np.array([1.0, 1.0], np.float32)
+    q2 = np.array([[2, 1], [1, 1]], np.int8); s2 = np.array([0.5, 1.0], np.float32)
+    x = bf16_bits(np.array([[3.0, 1.0]], dtype=np.float32))
+    y, z, n = oracle.ffn_lopa_q8(2, 2, 1, RELU, 0, qU, sU, qV, sV, q3, s3, q2, s2, x)
+    # u = (3, 1); h = (2.5 * 3, 0) = (7.5, 0); y = (0.5 * 2 * 7.5, 1 * 1 * 7.5)
+    assert z.tolist() == [[2.5, -1.25]] and n.tolist() == [1]
+    assert y.tolist() == [[7.5, 7.5]]
+
+
+def test_lopa_q8_rejects_bad_arguments():
+    q = np.zeros((4, 8), dtype=np.int8)
+    s = np.ones(4, dtype=np.float32)
+    x = bf16_bits(np.ones((1, 8), dtype=np.float32))
+    with pytest.raises(RuntimeError):   # the tiled identity is not part of this form
+        oracle.ffn_lopa_q8(8, 4, 8, RELU, oracle.FLAG_TILED_G, np.zeros((4, 8), np.int8), s,
+                           np.zeros((8, 8), np.int8), np.ones(8, np.float32), q, s, q.T.copy(),
+                           np.ones(8, np.float32), x)

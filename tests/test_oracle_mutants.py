@@ -56,6 +56,9 @@ MUTANTS = {
     "group_amax_of_first_group": ("const float* w = W + (size_t)i * cols + (size_t)g * group;",
                                   "const float* w = W + (size_t)i * cols;"),
     "group_scale_of_row": ("s[(size_t)i * ng + g] = sc;", "s[(size_t)i * ng] = sc;"),
+    # the low-rank gate with int8 weights
+    "lopa_q8_gate_on_x": ("zb[i] = dot(row, t, r);", "zb[i] = dot(row, xd, r);"),
+    "lopa_q8_v_scaled_by_u": ("dequant_row(qV, sV, (size_t)k, D, row);", "dequant_row(qV, sU, (size_t)k, D, row);"),
 }
 
 
@@ -195,6 +198,12 @@ def _pins(mod):
                                   np.array([[1], [2], [-1], [4]], np.int8), f([1.0, 0.5, 2.0, 0.125]),
                                   _bf16_bits(f(np.ones((1, 4)))), 0.0, 2)
     check("q4g_hand_forward", zg.tolist() == [[8.5]] and yg.tolist() == [[19.125, 19.125, -38.25, 9.5625]])
+    # the low-rank gate with int8 weights (values derived in test_oracle_int8)
+    yl, zl, nl = mod.ffn_lopa_q8(2, 2, 1, oracle.RELU, 0, np.array([[4], [-2]], np.int8), f([0.25, 0.25]),
+                                 np.array([[2, -1]], np.int8), f([0.5]), np.array([[1, 0], [0, 1]], np.int8),
+                                 f([1.0, 1.0]), np.array([[2, 1], [1, 1]], np.int8), f([0.5, 1.0]),
+                                 _bf16_bits(f([[3.0, 1.0]])))
+    check("lopa_q8_hand", zl.tolist() == [[2.5, -1.25]] and yl.tolist() == [[7.5, 7.5]])
     return failed
 
 
