@@ -497,8 +497,8 @@ int oracle_ffn_lopa_q8(int D, int H, int r, int act, int B, int flags, double th
       const double u = dot(row, xd, D);
       g[i] = gate_value(act, thr, zb[i]) * up_value(act, flags, u);
     }
-    for (int m = 0; m < D; ++m) {  /* y_m = sum_i (q2[m, i] s2[m]) g_i, i ascending */
-      dequant_row(q2, s2, (size_t)m, H, row);
+    for (int m = 0; m < D; ++m) {  /* y_m = sum_i (q2[m, i] s2[m]) g_i, i ascending (one group per row) */
+      dequant_row_g(q2, s2, (size_t)m, H, H, row);
       y[(size_t)b * D + m] = dot(row, g, H);
     }
     int cnt = 0;
