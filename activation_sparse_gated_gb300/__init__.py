@@ -250,11 +250,13 @@ class SparseFFN:
 
     def int8_weights(self, device="cuda"):
         """The handle's codes (one per byte, also for int4) and scales as tensors: (W1q, s1, W3q, s3,
-        W2q, s2), W2q as [D, H]; s1, s3 [H], or [H, D // 64] on an int4 handle."""
+        W2q, s2), W2q as [D, H]; s1, s3 [H], or [H, D // 64] on an int4 handle; with the low-rank gate
+        (int8) W1q holds U's codes [H, r] and s1 its scales."""
         import torch
         D, H = self.D, self.H
         ss = (H,) if self.dtype != "int4" else (H, D // INT4_GROUP)
-        out = (torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(ss, device=device),
+        gk = self.r if self.r > 0 else D  # the low-rank gate: U's codes [H, r]
+        out = (torch.empty(H, gk, dtype=torch.int8, device=device), torch.empty(ss, device=device),
                torch.empty(H, D, dtype=torch.int8, device=device), torch.empty(ss, device=device),
                torch.empty(D, H, dtype=torch.int8, device=device), torch.empty(D, device=device))
         sffn_get_weights_int8(self.h, *out)

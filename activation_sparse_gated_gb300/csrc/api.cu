@@ -82,10 +82,12 @@ struct sffn_s {
   float* ypart = nullptr;     // deterministic option: [blocks, D] partial y rows of the single-token kernel
   uint16_t* tpair = nullptr;  // low-rank gate: [256, r] bf16 t pairs of a tensor-core batch
   float* tacc = nullptr;      // low-rank gate: [128, r] fp32 partial sums of the t kernel
-  // weight-only int8 (SFFN_I8W): per-output-channel scales of W1, W3 [H] and W2 [D]
+  // weight-only int8 / int4: per-output-channel scales of W1 (or U), W3 [H] and W2 [D]; of V [r]
+  // for the low-rank gate with int8 weights
   float* qs1 = nullptr;
   float* qs3 = nullptr;
   float* qs2 = nullptr;
+  float* qsv = nullptr;
   StreamPlan i8_plan;
   bool b1_bf16 = true;    // bf16 single tokens: ffn_b1_bf16.cu (false: the fp32 streaming kernel's bf16 form)
   StreamPlan bf16_plan;
@@ -114,6 +116,7 @@ void release(sffn_s* h) {
   cudaFree(h->qs1);
   cudaFree(h->qs3);
   cudaFree(h->qs2);
+  cudaFree(h->qsv);
   if (h->ev) cudaEventDestroy(h->ev);
 }
 
@@ -202,8 +205,8 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     fail(SFFN_ERR_ARG, "dtype %d unknown", dtype);
     return nullptr;
   }
-  if (dtype == SFFN_I8W && (r != 0 || D % 16 != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
-    fail(SFFN_ERR_DTYPE, "int8 weights need the standard gate (r = 0), D %% 16 == 0 and no low-rank option");
+  if (dtype == SFFN_I8W && (r % 16 != 0 || D % 16 != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
+    fail(SFFN_ERR_DTYPE, "int8 weights need D %% 16 == 0, r %% 16 == 0 and no option but the double activation");
     return nullptr;
   }
   if (dtype == SFFN_I4W && (r != 0 || D % INT4_GROUP != 0 || (flags & ~SFFN_DOUBLE_ACT))) {
@@ -256,6 +259,7 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
       {(void**)&h->qs1, i8 ? sizeof(float) * H * qscale_per_row(h) : 16},
       {(void**)&h->qs3, i8 ? sizeof(float) * H * qscale_per_row(h) : 16},
       {(void**)&h->qs2, i8 ? sizeof(float) * D : 16},
+      {(void**)&h->qsv, i8 && r > 0 ? sizeof(float) * r : 16},
       {(void**)&h->yacc, sizeof(float) * SFFN_MAX_BATCH * YACC_COPIES * D},
       {(void**)&h->tbuf, sizeof(float) * SFFN_MAX_BATCH * std::max(r, 8)},
       {(void**)&h->ctrl, sizeof(int) * CTRL_INTS},
@@ -316,7 +320,7 @@ sffn_t sffn_create_ex(int D, int H, int r, int act, int dtype, int flags) {
     }
     if ((e = ffn_batch_prepare(h->max_smem))) return bail(SFFN_ERR_CUDA, "cudaFuncSetAttribute", e);
     if (i8) {
-      h->i8_plan = plan_ffn_b1_i8(D, h->stream_rows_cap, h->qbits);
+      h->i8_plan = plan_ffn_b1_i8(D, (int)gate_k(h), h->stream_rows_cap, h->qbits, r > 0);
       if (h->i8_plan.smem > h->max_smem) {
         fail(SFFN_ERR_DTYPE, "shared-memory plan of the int8 / int4 kernel exceeds the device limit");
         char keep[sizeof g_msg];
@@ -399,18 +403,23 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
     auto store = [&](void* dst, const int8_t* src) {  // int4: pack the one-per-byte codes
       return i4 ? launch_pack_int4(src, dst, H * D, perr, s) : cudaSuccess;
     };
-    // W1 and W3: int8 one scale per row, int4 one per group of 64 columns
-    auto quant_rows = [&](int8_t* dst, float* sc) {
-      return i4 ? launch_quantize_groups4(stage, dst, sc, (int)H, (int)D, s)
-                : launch_quantize_rows(stage, dst, sc, (int)H, (int)D, s, qmax);
+    // W1 (or U [H, r]) and W3: int8 one scale per row, int4 one per group of 64 columns
+    const size_t gk = gate_k(h);
+    auto quant_rows = [&](int8_t* dst, float* sc, size_t cols) {
+      return i4 ? launch_quantize_groups4(stage, dst, sc, (int)H, (int)cols, s)
+                : launch_quantize_rows(stage, dst, sc, (int)H, (int)cols, s, qmax);
     };
     int8_t* c1 = i4 ? codes : static_cast<int8_t*>(h->gate_w);
-    if (!e) e = cudaMemcpyAsync(stage, W1_or_U, H * D * 2, cudaMemcpyDefault, s);
-    if (!e) e = quant_rows(c1, h->qs1);
+    if (!e) e = cudaMemcpyAsync(stage, W1_or_U, H * gk * 2, cudaMemcpyDefault, s);
+    if (!e) e = quant_rows(c1, h->qs1, gk);
     if (!e) e = store(h->gate_w, c1);
+    if (!e && h->r > 0) {  // the low-rank gate's V [r, D] (int8 only): one scale per row
+      e = cudaMemcpyAsync(stage, V, (size_t)h->r * D * 2, cudaMemcpyDefault, s);
+      if (!e) e = launch_quantize_rows(stage, static_cast<int8_t*>(h->V), h->qsv, h->r, (int)D, s, 127);
+    }
     int8_t* c3 = i4 ? codes : static_cast<int8_t*>(h->W3);
     if (!e) e = cudaMemcpyAsync(stage, W3, H * D * 2, cudaMemcpyDefault, s);
-    if (!e) e = quant_rows(c3, h->qs3);
+    if (!e) e = quant_rows(c3, h->qs3, D);
     if (!e) e = store(h->W3, c3);
     if (!e) e = cudaMemcpyAsync(stage, W2, D * H * 2, cudaMemcpyDefault, s);
     if (!e) e = launch_quantize_rows(stage, q2, h->qs2, (int)D, (int)H, s, qmax);
@@ -449,6 +458,8 @@ int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const in
                           const int8_t* W2q, const float* s2, void* stream) {
   if (!h) return fail(SFFN_ERR_ARG, "null handle");
   if (!h->qbits) return fail(SFFN_ERR_STATE, "the handle does not hold int8 or int4 weights");
+  if (h->r > 0)
+    return fail(SFFN_ERR_STATE, "a low-rank int8 handle takes bf16 weights through sffn_set_weights");
   if (!W1q || !s1 || !W3q || !s3 || !W2q || !s2) return fail(SFFN_ERR_ARG, "null weight pointer");
   if (int rc = check_device(h)) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -503,13 +514,13 @@ int sffn_get_weights_int8(sffn_t h, int8_t* W1q, float* s1, int8_t* W3q, float* 
   int8_t *q2 = nullptr, *codes = nullptr;
   if (i4) e = cudaMalloc(&codes, D * H);
   // int4: unpacked to one code per byte on the way out
-  auto get = [&](int8_t* dst, const void* src) {
-    if (!i4) return cudaMemcpyAsync(dst, src, H * D, cudaMemcpyDefault, s);
-    cudaError_t r = launch_unpack_int4(src, codes, H * D, s);
-    return r ? r : cudaMemcpyAsync(dst, codes, H * D, cudaMemcpyDefault, s);
+  auto get = [&](int8_t* dst, const void* src, size_t cols) {
+    if (!i4) return cudaMemcpyAsync(dst, src, H * cols, cudaMemcpyDefault, s);
+    cudaError_t r = launch_unpack_int4(src, codes, H * cols, s);
+    return r ? r : cudaMemcpyAsync(dst, codes, H * cols, cudaMemcpyDefault, s);
   };
-  if (!e && W1q) e = get(W1q, h->gate_w);
-  if (!e && W3q) e = get(W3q, h->W3);
+  if (!e && W1q) e = get(W1q, h->gate_w, (size_t)gate_k(h));  // the low-rank gate: U's codes [H, r]
+  if (!e && W3q) e = get(W3q, h->W3, D);
   if (!e && s1) e = cudaMemcpyAsync(s1, h->qs1, sizeof(float) * H * qscale_per_row(h), cudaMemcpyDefault, s);
   if (!e && s3) e = cudaMemcpyAsync(s3, h->qs3, sizeof(float) * H * qscale_per_row(h), cudaMemcpyDefault, s);
   if (!e && s2) e = cudaMemcpyAsync(s2, h->qs2, sizeof(float) * D, cudaMemcpyDefault, s);
@@ -603,9 +614,14 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
     SFFN_CUDA(ce);
   }
   if (h->qbits) {
-    // weight-only int8 / int4: one streaming pass per token
+    // weight-only int8 / int4: one streaming pass per token (the low-rank gate's t kernel first)
     for (int b = 0; b < B; ++b) {
       B1Params p;
+      if (lopa) {
+        float* tb = h->tbuf + (size_t)b * h->r;
+        SFFN_CUDA(launch_lopa_t_i8(h->V, h->qsv, static_cast<const uint8_t*>(x) + b * row, tb, h->r, h->D, s));
+        p.t = tb;
+      }
       p.gate_w = h->gate_w;
       p.W3 = h->W3;
       p.W2t = h->W2t;
@@ -617,7 +633,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       p.mask = h->mask + (size_t)b * h->H;
       p.D = h->D;
       p.H = h->H;
-      p.gate_k = h->D;
+      p.gate_k = gate_k(h);
       p.act = h->act;
       p.count_slot = b;
       p.rows_cap = h->stream_rows_cap;
@@ -632,7 +648,7 @@ int sffn_forward(sffn_t h, const void* x, void* y, int B, void* stream) {
       SFFN_CUDA(launch_finalize(h->yacc, p.y, h->ctrl, p.counts, b, h->D, 1, SFFN_BF16, s));
     }
   }
-  if (lopa && !tc_batch) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
+  if (lopa && !tc_batch && !h->qbits) SFFN_CUDA(launch_lopa_t(h->V, x, h->tbuf, h->r, h->D, B, h->dtype, s));
   // tokens in groups of up to 8: one pass over the weights per group
   for (int b = 0; b < B && !h->qbits && !tc_batch;) {
     const int nb = det ? 1 : std::min(8, B - b);

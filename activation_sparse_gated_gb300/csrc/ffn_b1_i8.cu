@@ -211,7 +211,7 @@ __device__ __forceinline__ void load_piece_i8(CT (&w)[QPIECE], const CT* row, in
   }
 }
 
-template <int BITS>
+template <int BITS, bool LOWRANK>
 __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   using CT = typename Piece<BITS>::type;
   extern __shared__ __align__(16) uint8_t smem[];
@@ -221,7 +221,11 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   const uint32_t row_bytes = (uint32_t)(D * BITS / 8);
   const int rq = (int)(row_bytes / 16);  // 16-byte units of a row (D % 64 == 0 for int4)
   const int ng = BITS == 4 ? D / G4 : 1;  // scales per row of W1 and of W3
-  const int npg = (ncw + 32 * QPIECE - 1) / (32 * QPIECE);
+  // the gate: rows of W1 over x, or (low-rank gate, int8) rows of U over t = V x, gcw pieces a row
+  constexpr bool lowrank = LOWRANK;  // p.t holds t
+  const int gcw = lowrank ? p.gate_k / 16 : ncw;              // the standard gate's rows are W1's
+  const int rqg = lowrank ? p.gate_k * BITS / 8 / 16 : rq;    // 16-byte units of a gate row
+  const int npg = (gcw + 32 * QPIECE - 1) / (32 * QPIECE);
   const int row0 = (int)(((long long)blockIdx.x * p.H) / gridDim.x);
   const int row1 = (int)(((long long)(blockIdx.x + 1) * p.H) / gridDim.x);
   const int cap = p.rows_cap;
@@ -230,6 +234,11 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   uint8_t* sp = smem;
   float4* xq = reinterpret_cast<float4*>(sp);  // x widened to fp32 once per block (interleaved)
   sp += a16((size_t)D * 4);
+  float4* gq = xq;  // the gate's vector in the same layout: x, or t for the low-rank gate
+  if (lowrank) {
+    gq = reinterpret_cast<float4*>(sp);
+    sp += a16((size_t)p.gate_k * 4);
+  }
   float* s2s = reinterpret_cast<float*>(sp);
   sp += a16((size_t)D * 4);
   float* s1s = reinterpret_cast<float*>(sp);  // [cap][ng] scales of the block's W1 rows, then of its W3 rows
@@ -261,8 +270,8 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   const int R = min(p.pref_rows, nrows);
   const int nreg = max(0, min(QW, nrows - R));
   auto copy_rows = [&](int first, int n) {
-    const uint4* src = reinterpret_cast<const uint4*>(G + (size_t)(row0 + first) * ncw);
-    for (int i = tid; i < n * rq; i += QT) cpa16(srows + i, src + i);
+    const uint4* src = reinterpret_cast<const uint4*>(G + (size_t)(row0 + first) * gcw);
+    for (int i = tid; i < n * rqg; i += QT) cpa16(srows + i, src + i);
     cpa_commit();
   };
   for (int i = tid; i < D / 4; i += QT) cpa16(s2s + 4 * i, p.s2 + 4 * i);  // committed with the rows
@@ -272,10 +281,10 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   }
   copy_rows(0, R);
   const int n_seq = warp < nreg ? npg : 0;
-  const CT* my_row = G + (size_t)(row0 + R + warp) * ncw;
+  const CT* my_row = G + (size_t)(row0 + R + warp) * gcw;
   CT wa[QPIECE], wb[QPIECE];
-  if (n_seq > 0) load_piece_i8(wa, my_row, 0, lane, ncw);
-  if (n_seq > 1) load_piece_i8(wb, my_row, 1, lane, ncw);
+  if (n_seq > 0) load_piece_i8(wa, my_row, 0, lane, gcw);
+  if (n_seq > 1) load_piece_i8(wb, my_row, 1, lane, gcw);
   if (tid == 0) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.x), "r"((uint32_t)nch * 16u)
                              : "memory");
 
@@ -287,6 +296,9 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
     xq[(f0 & 3) * ncw + (f0 >> 2)] = make_float4(v[0], v[1], v[2], v[3]);
     xq[(f1 & 3) * ncw + (f1 >> 2)] = make_float4(v[4], v[5], v[6], v[7]);
   }
+  if (lowrank)  // t [r] fp32 from the t kernel: word f = t[4f .. 4f + 4), piece f / 4, quarter f % 4
+    for (int f = tid; f < p.gate_k / 4; f += QT)
+      gq[(f & 3) * gcw + (f >> 2)] = __ldcg(reinterpret_cast<const float4*>(p.t) + f);
   cpa_wait();
   __syncthreads();
 
@@ -309,10 +321,10 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   };
   auto shared_rows = [&](int first, int n) {
     for (int i = warp; i < n; i += QW) {
-      const CT* r = srow_p + (size_t)i * ncw;
+      const CT* r = srow_p + (size_t)i * gcw;
       const float* gs = s1s + (size_t)(first + i) * ng;
       float2 acc = make_float2(0.f, 0.f);
-      for (int c = lane; c < ncw; c += 32) dot_piece<BITS>(lds_piece(r + c), xq, ncw, c, acc, gs);
+      for (int c = lane; c < gcw; c += 32) dot_piece<BITS>(lds_piece(r + c), gq, gcw, c, acc, gs);
       decide(row0 + first + i, warp_sum(acc.x + acc.y));
     }
   };
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
 #pragma unroll
     for (int k = 0; k < QPIECE; ++k) {
       const int c = pc * 32 * QPIECE + lane + 32 * k;
-      if (c < ncw) dot_piece<BITS>(w[k], xq, ncw, c, acc, my_gs);
+      if (c < gcw) dot_piece<BITS>(w[k], gq, gcw, c, acc, my_gs);
     }
     if (pc == npg - 1) {
       const float d = warp_sum(acc.x + acc.y);
@@ -338,10 +350,10 @@ __global__ void __launch_bounds__(QT, 2) ffn_b1_i8_kernel(const B1Params p) {
   };
   for (int pc = 0; pc < n_seq; pc += 2) {
     consume(wa, pc);
-    if (pc + 2 < n_seq) load_piece_i8(wa, my_row, pc + 2, lane, ncw);
+    if (pc + 2 < n_seq) load_piece_i8(wa, my_row, pc + 2, lane, gcw);
     if (pc + 1 < n_seq) {
       consume(wb, pc + 1);
-      if (pc + 3 < n_seq) load_piece_i8(wb, my_row, pc + 3, lane, ncw);
+      if (pc + 3 < n_seq) load_piece_i8(wb, my_row, pc + 3, lane, gcw);
     }
   }
   while (nb1 > 0) {
@@ -494,6 +506,44 @@ __global__ void __launch_bounds__(256) quantize_groups4_kernel(const uint16_t* _
   }
 }
 
+// Low-rank gate with int8 weights: t_k = sV_k (qV[k, :] . x), one warp per row of V (D % 16 == 0),
+// the row's 16-byte pieces requested before the dependency wait, x read from L2 after it.
+constexpr int TW = 8;  // warps (rows of V) per block
+__global__ void __launch_bounds__(TW * 32) lopa_t_i8_kernel(const int8_t* __restrict__ qV, const float* __restrict__ sV,
+                                                            const uint16_t* __restrict__ x, float* __restrict__ t,
+                                                            int r, int D) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, k = blockIdx.x * TW + warp;
+  const int npc = D / 16;
+  const uint4* row = reinterpret_cast<const uint4*>(qV + (size_t)min(k, r - 1) * D);
+  constexpr int PL = 8;  // pieces held per lane (D <= 4096)
+  uint4 w[PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) w[j] = (lane + 32 * j < npc && k < r) ? ldg_stream(row + lane + 32 * j) : make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();  // x follows stream order
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const int c = lane + 32 * j;
+    if (c >= npc) break;
+    float xa[8], xb[8];
+    Elt<bf16_tag>::unpack(__ldcg(reinterpret_cast<const uint4*>(x) + 2 * c), xa);
+    Elt<bf16_tag>::unpack(__ldcg(reinterpret_cast<const uint4*>(x) + 2 * c + 1), xb);
+    const float xv[16] = {xa[0], xa[1], xa[2], xa[3], xa[4], xa[5], xa[6], xa[7],
+                          xb[0], xb[1], xb[2], xb[3], xb[4], xb[5], xb[6], xb[7]};
+    const uint32_t words[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float2 v01, v23;
+      widen_i8x4(words[q], v01, v23);
+      ffma2(acc, v01, make_float2(xv[4 * q], xv[4 * q + 1]));
+      ffma2(acc, v23, make_float2(xv[4 * q + 2], xv[4 * q + 3]));
+    }
+  }
+  const float d = warp_sum(acc.x + acc.y);
+  if (lane == 0 && k < r) t[k] = sV[k] * d;
+}
+
 // int4 codes, one per byte in [-7, 7] -> two per byte (code 2i in the low nibble); a code
 // outside that range sets DEV_ERR_CHECK in *err and packs as 0.
 __global__ void pack_int4_kernel(const int8_t* __restrict__ codes, uint8_t* __restrict__ out, size_t n_bytes,
@@ -520,17 +570,19 @@ __global__ void unpack_int4_kernel(const uint8_t* __restrict__ in, int8_t* __res
 
 }  // namespace
 
-StreamPlan plan_ffn_b1_i8(int D, int rows_cap, int bits) {
+StreamPlan plan_ffn_b1_i8(int D, int gate_k, int rows_cap, int bits, bool lowrank) {
   StreamPlan pl;
-  const size_t row = (size_t)D * bits / 8;  // bytes of a code row
+  const size_t row = (size_t)D * bits / 8;        // bytes of a gathered W3 code row
+  const size_t grow = (size_t)gate_k * bits / 8;  // bytes of a gate code row (W1, or U of the low-rank gate)
   const size_t ng = bits == 4 ? (size_t)(D / G4) : 1;  // W1 and W3 scales per row
   // two blocks per SM (the next call's blocks prefetch while this call runs):
   // at most 110 KB per block, of which the gate-row area takes what is left
-  const size_t fixed = 2 * a16((size_t)D * 4) + a16((size_t)rows_cap * ng * 8) + a16((size_t)rows_cap * 13 + 16);
+  const size_t tq = lowrank ? a16((size_t)gate_k * 4) : 0;  // the staged t of the low-rank gate
+  const size_t fixed = 2 * a16((size_t)D * 4) + tq + a16((size_t)rows_cap * ng * 8) + a16((size_t)rows_cap * 13 + 16);
   const size_t budget = 110u * 1024u;
   const size_t free_area = budget > fixed ? budget - fixed : 0;
-  pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, std::max<size_t>(1, free_area / row));
-  const size_t area = std::max((size_t)pl.pref_rows * row, (size_t)std::min(rows_cap, 16) * row);
+  pl.pref_rows = (int)std::min<size_t>((size_t)rows_cap, std::max<size_t>(1, free_area / grow));
+  const size_t area = std::max((size_t)pl.pref_rows * grow, (size_t)std::min(rows_cap, 16) * row);
   pl.gather_rows = (int)std::max<size_t>(1, area / row);
   pl.smem = fixed + area;
   return pl;
@@ -538,7 +590,7 @@ StreamPlan plan_ffn_b1_i8(int D, int rows_cap, int bits) {
 
 cudaError_t ffn_b1_i8_prepare(size_t max_smem) {
   cudaError_t e = cudaSuccess;
-  for (auto k : {ffn_b1_i8_kernel<8>, ffn_b1_i8_kernel<4>}) {
+  for (auto k : {ffn_b1_i8_kernel<8, false>, ffn_b1_i8_kernel<4, false>, ffn_b1_i8_kernel<8, true>}) {
     if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
     if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
@@ -546,8 +598,12 @@ cudaError_t ffn_b1_i8_prepare(size_t max_smem) {
 }
 
 cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s, int bits) {
-  return bits == 4 ? launch_pdl(ffn_b1_i8_kernel<4>, dim3(grid), dim3(QT), smem, s, p)
-                   : launch_pdl(ffn_b1_i8_kernel<8>, dim3(grid), dim3(QT), smem, s, p);
+  if (p.t) {  // the low-rank gate: int8 only
+    if (bits != 8) return cudaErrorInvalidValue;
+    return launch_pdl(ffn_b1_i8_kernel<8, true>, dim3(grid), dim3(QT), smem, s, p);
+  }
+  return bits == 4 ? launch_pdl(ffn_b1_i8_kernel<4, false>, dim3(grid), dim3(QT), smem, s, p)
+                   : launch_pdl(ffn_b1_i8_kernel<8, false>, dim3(grid), dim3(QT), smem, s, p);
 }
 
 cudaError_t launch_quantize_rows(const void* src_bf16, int8_t* dst, float* scale, int rows, int cols, cudaStream_t s,
@@ -565,6 +621,12 @@ cudaError_t launch_quantize_groups4(const void* src_bf16, int8_t* dst, float* sc
   if (rows <= 0) return cudaSuccess;
   quantize_groups4_kernel<<<rows, 256, 0, s>>>(static_cast<const uint16_t*>(src_bf16), dst, scale, cols);
   return cudaGetLastError();
+}
+
+cudaError_t launch_lopa_t_i8(const void* qV, const float* sV, const void* x, float* t, int r, int D, cudaStream_t s) {
+  if (D % 16 || D > 32 * 8 * 16 || r < 1) return cudaErrorInvalidValue;
+  return launch_pdl(lopa_t_i8_kernel, dim3((r + TW - 1) / TW), dim3(TW * 32), 0, s, static_cast<const int8_t*>(qV),
+                    sV, static_cast<const uint16_t*>(x), t, r, D);
 }
 
 cudaError_t launch_pack_int4(const int8_t* codes, void* packed, size_t n_codes, int* err, cudaStream_t s) {

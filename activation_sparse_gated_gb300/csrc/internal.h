@@ -15,7 +15,7 @@ struct B1Params {
   const void* W3;         // [H, D]
   const void* W2t;        // [H, D]  (W2 transposed: the column of unit i is row i)
   const void* x;          // [D]
-  const float* t;         // [r] fp32 t = V x for the low-rank gate, else nullptr
+  const float* t = nullptr;  // [r] fp32 t = V x for the low-rank gate, else nullptr
   void* y;                // [D]
   float* yacc;            // [D] fp32 accumulator, all zero between calls
   int* ctrl;              // ticket / error word / live-count accumulator
@@ -181,7 +181,10 @@ cudaError_t launch_finalize(float* yacc, void* y, int* ctrl, int* counts, int co
 // row, code 2b in the low nibble of byte b); scales s1, s3 [H] (int4: [H, D / 64], one
 // per group of 64 columns), s2 [D] in the params (each block scales its partial y by
 // s2 before adding it up).
-StreamPlan plan_ffn_b1_i8(int D, int rows_cap, int bits);
+StreamPlan plan_ffn_b1_i8(int D, int gate_k, int rows_cap, int bits, bool lowrank);
+// Low-rank gate, int8 weights: t [r] fp32 = sV * (qV [r, D] . x) for one bf16 token x (D % 16 == 0,
+// D <= 4096); the int8 kernel then takes gate_k = r, gate_w = qU [H, r], t.
+cudaError_t launch_lopa_t_i8(const void* qV, const float* sV, const void* x, float* t, int r, int D, cudaStream_t s);
 cudaError_t ffn_b1_i8_prepare(size_t max_smem);
 cudaError_t launch_ffn_b1_i8(const B1Params& p, int grid, size_t smem, cudaStream_t s, int bits);
 // Per-row symmetric quantisation of a bf16 matrix [rows, cols] to one code per byte in

@@ -88,8 +88,8 @@ enum {
  *   act    SFFN_ACT_RELU, SFFN_ACT_RSP, or SFFN_ACT_SILU (z sigmoid(z) for every
  *          z: the smooth gate, never exactly zero; see sffn_set_live_threshold)
  *   dtype  SFFN_F32, SFFN_BF16, SFFN_I8W (int8 weights, bf16 x and y; needs
- *          r == 0 and D % 16 == 0; flags may only hold SFFN_DOUBLE_ACT), or
- *          SFFN_I4W (int4 weights, the same with D % 64 == 0)
+ *          D % 16 == 0 and r % 16 == 0; flags may only hold SFFN_DOUBLE_ACT), or
+ *          SFFN_I4W (int4 weights, standard gate, D % 64 == 0)
  * Returns NULL on error (see sffn_last_error()).  Allocates device memory:
  * 3*H*D (+ r*D + H*r) elements of weights plus O(B_max * (D + r + H)) bytes of
  * accumulators.
@@ -209,7 +209,9 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
  * likewise u_i) with fp32 sums and y rounded once to bf16.
  *
  * On such a handle sffn_set_weights takes bf16 W1[H, D], W3[H, D], W2[D, H]
- * (V ignored) and quantises them on the device.  sffn_set_weights_int8 loads
+ * (V ignored) and quantises them on the device.  With the low-rank gate (int8
+ * only, the plain form z = U (V x)) it takes bf16 U[H, r], V[r, D], W3, W2 and
+ * gives U and V one scale per row as well: t = sV (qV x), z = sU (qU t).  sffn_set_weights_int8 loads
  * codes and scales quantised elsewhere (a quantisation-aware-trained layer):
  *   W1q, W3q [H, D] int8 with s1, s3 [H] fp32;  W2q [D, H] int8 with s2 [D] fp32
  * (host or device pointers, any alignment).  On an SFFN_I4W handle the code
@@ -218,8 +220,10 @@ int sffn_set_weights(sffn_t h, const void* W1_or_U, const void* V, const void* W
  * handle without weights), and s1, s3 are [H, D / 64] (scale of row i, columns
  * 64 g .. 64 g + 63 at i * D / 64 + g).  sffn_get_weights_int8 copies the handle's codes (one per
  * byte) and scales out in the same layout (any pointer may be NULL to skip that
- * array).  Both return after `stream` has finished the copies, and return
- * SFFN_ERR_STATE on a handle of another dtype.
+ * array); on a low-rank int8 handle W1q and s1 receive U's codes [H, r] and
+ * scales [H], and sffn_set_weights_int8 returns SFFN_ERR_STATE (such a handle
+ * takes bf16 weights).  Both return after `stream` has finished the copies, and
+ * return SFFN_ERR_STATE on a handle of another dtype.
  */
 int sffn_set_weights_int8(sffn_t h, const int8_t* W1q, const float* s1, const int8_t* W3q, const float* s3,
                           const int8_t* W2q, const float* s2, void* stream);

@@ -237,7 +237,7 @@ def test_external_codes_and_round_trip(dtype):
 
 def test_int8_argument_errors():
     with pytest.raises(sffn.SffnError):
-        sffn.SparseFFN(256, 512, 32, "relu", "int8")          # low-rank gate
+        sffn.SparseFFN(256, 512, 40, "relu", "int8")          # low-rank gate with r % 16 != 0
     with pytest.raises(sffn.SffnError):
         sffn.SparseFFN(40, 512, 0, "relu", "int8")            # D % 16 != 0
     bf = sffn.SparseFFN(256, 512, 0, "relu", "bf16")
@@ -297,3 +297,87 @@ def test_int4_argument_errors():
     with pytest.raises(sffn.SffnError) as e:                   # and the handle has no weights
         h(torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda"))
     assert e.value.code == sffn.SFFN_ERR_STATE
+
+
+# The low-rank gate with int8 weights: z = sU (qU t), t = sV (qV x), one scale per row of U, V, W3, W2.
+
+def oracle_codes_lowrank(lw):
+    t = lw.tensors()
+    U, V, W3, W2 = (t[k].float().numpy() for k in ("U", "V", "W3", "W2"))
+    return oracle.quantize_rows(U) + oracle.quantize_rows(V) + oracle.quantize_rows(W3) + oracle.quantize_rows(W2)
+
+
+def make_lowrank_int8(lw, act="relu", flags=0, thr=0.0):
+    ffn = sffn.SparseFFN(lw.D, lw.H, lw.r, act, "int8", flags=flags)
+    t = lw.tensors()
+    ffn.set_weights(t["U"].cuda(), t["V"].cuda(), t["W3"].cuda(), t["W2"].cuda())
+    if thr:
+        ffn.set_live_threshold(thr)
+    return ffn
+
+
+def check_lowrank(lw, x, y, counts, masks, act="relu", flags=0, thr=0.0):
+    qU, sU, qV, sV, q3, s3, q2, s2 = oracle_codes_lowrank(lw)
+    yref, z, n = oracle.ffn_lopa_q8(lw.D, lw.H, lw.r, ACTS[act], flags, qU, sU, qV, sV, q3, s3, q2, s2,
+                                    syn.oracle_view(x), thr=thr)
+    A = act_abs(act, z)
+    W3 = q3.astype(np.float64) * np.asarray(s3, np.float64)[:, None]
+    W2 = q2.astype(np.float64) * np.asarray(s2, np.float64)[:, None]
+    xv = x.double().numpy()
+    for b in range(x.shape[0]):
+        den = np.linalg.norm(yref[b])
+        live = A[b] > thr
+        if den == 0:
+            assert (y[b] == 0).all(), f"token {b}: no live unit but y != 0"
+        else:
+            err = np.linalg.norm(y[b] - yref[b]) / den
+            assert err <= TOL, f"token {b}: relative L2 {err:.3e} > {TOL}"
+            ya = flip_adjusted(yref[b], z[b], masks[b].astype(bool), live, W3, W2, xv[b], act, flags)
+            rms = np.sqrt(np.mean(yref[b] ** 2))
+            worst = np.abs(y[b] - ya).max()
+            assert worst <= K_ELEM * TOL * rms, f"token {b}: element error {worst:.3e} > {K_ELEM * TOL * rms:.3e}"
+        sure = (np.abs(z[b]) > BAND) if thr == 0 else (np.abs(A[b] - thr) > 1e-3)
+        bad = np.nonzero(sure & (masks[b].astype(bool) != live))[0]
+        assert bad.size == 0, f"token {b}: live set differs at units {bad[:10]}"
+        assert counts[b] == masks[b].sum()
+    return yref, z, n
+
+
+@pytest.mark.parametrize("act,flags,thr", [("relu", 0, 0.0), ("rsp", 0, 0.0), ("relu", sffn.SFFN_DOUBLE_ACT, 0.0),
+                                           ("silu", 0, 0.3)])
+@pytest.mark.parametrize("B", [1, 3])
+def test_lowrank_int8_matches_oracle(act, flags, thr, B):
+    kw = {"shift": 0.0} if act == "silu" else {}
+    lw = syn.lopa_layer(512, 1500, 64, dtype="bf16", seed=92, **kw)
+    x = syn.tokens(2 * B, 512, dtype="bf16", seed=93)
+    ffn = make_lowrank_int8(lw, act, flags, thr)
+    y, c, m = run(ffn, x, B=B)
+    check_lowrank(lw, x, y, c, m, act, flags, thr)
+
+
+@pytest.mark.parametrize("D,H,r", [(64, 151, 16), (256, 700, 48), (2560, 9787, 400)])
+def test_lowrank_int8_shapes_and_codes(D, H, r):
+    """Ragged and full-size shapes; U's codes and scales read back bit-exact with the oracle's."""
+    lw = syn.lopa_layer(D, H, r, dtype="bf16", seed=94)
+    x = syn.tokens(3, D, dtype="bf16", seed=95)
+    ffn = make_lowrank_int8(lw)
+    y, c, m = run(ffn, x)
+    _, _, n = check_lowrank(lw, x, y, c, m)
+    qU, sU = oracle.quantize_rows(lw.tensors()["U"].float().numpy())
+    got = ffn.int8_weights()
+    assert np.array_equal(got[0].cpu().numpy(), qU) and np.array_equal(got[1].cpu().numpy(), sU)
+    if D == 2560:
+        assert 0.02 < n.mean() / H < 0.3
+
+
+def test_lowrank_int8_takes_bf16_weights_only():
+    lw = syn.lopa_layer(256, 700, 48, dtype="bf16", seed=96)
+    ffn = sffn.SparseFFN(256, 700, 48, "relu", "int8")
+    q = torch.zeros(700, 256, dtype=torch.int8, device="cuda")
+    s = torch.ones(700, device="cuda")
+    with pytest.raises(sffn.SffnError) as e:
+        ffn.set_weights_int8(q, s, q, s, torch.zeros(256, 700, dtype=torch.int8, device="cuda"),
+                             torch.ones(256, device="cuda"))
+    assert e.value.code == sffn.SFFN_ERR_STATE
+    with pytest.raises(sffn.SffnError):
+        sffn.SparseFFN(256, 700, 48, "relu", "int4")          # int4 is the standard gate only
