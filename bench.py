@@ -577,6 +577,21 @@ def run_gpu(args):
         del lg
         lopa_batched = lopa_batched_extras(lffns, lx, stream, args, peak, D, Hp, r)
         del lffns
+        # the low-rank gate with weight-only int8 weights (one scale per row of U, V, W3, W2)
+        l8ffns = build_ffns(llayers, dev, dtype="int8")
+        l8counts = live_counts(l8ffns, lx, stream)
+        l8bytes = sum(r * (D + Hp) + 4 * (r + Hp) + 2 * k * D + 4 * k + 2 * elt * D + 4 * D for k in l8counts)
+        l8g = capture_step(l8ffns, lx, ly, stream)
+        l8t = time_graph(l8g, stream, args.steps, args.warmup)
+        l8us = 1e6 * l8t / (args.steps * li["tokens"])
+        extras["lopa_int8_weights"] = {"workload": LOPA_WORKLOAD + ", weight-only int8 (one fp32 scale per row of "
+                                       "U, V, W3 and W2), bf16 x and y", "weight_sets": lsets,
+                                       "us_per_call": l8us, "tokens_per_s": 1e6 / l8us,
+                                       "mean_live": sum(l8counts) / len(l8counts),
+                                       "gbs": l8bytes * args.steps / (l8t * 1e9),
+                                       "frac_of_measured": l8bytes * args.steps / (l8t * 1e9) / peak,
+                                       "speedup_vs_dense_bf16": us_dense / l8us, "gpu_launches_per_call": 3}
+        del l8ffns, l8g
         # the pages' complete low-rank form: W1(x) = Gx + U RMSNorm(Vx), double activation
         import activation_sparse_gated_gb300 as sffn_mod
         full = sffn_mod.SFFN_GATE_TILED_G | sffn_mod.SFFN_GATE_RMSNORM | sffn_mod.SFFN_DOUBLE_ACT
