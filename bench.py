@@ -553,6 +553,19 @@ def run_gpu(args):
                                 "gbs": dense_bytes / (us_dense * 1e3), "speedup_sparse": us_dense / us_call,
                                 "forms_us": {k: 1e6 * v / (args.steps * n_tok) for k, v in dense_t.items()}}
         del ld, dg
+        # the tiny fp32 configuration (D=384, H=1024, B=1, 64 tokens, one weight set; its parity against
+        # the oracle is in the tests): the latency of one call, L2-resident
+        tname = "tiny-f32-D384-H1024"
+        tffns = build_ffns(syn.workload_layers(tname, sets=1), dev)
+        tx = syn.workload_tokens(tname, 64).to(dev)
+        ty = torch.empty_like(tx)
+        tg = capture_step(tffns, tx, ty, stream)
+        tt = time_graph(tg, stream, args.steps, args.warmup)
+        tus = 1e6 * tt / (args.steps * 64)
+        extras["tiny_f32"] = {"workload": tname + ": fp32, D=384, H=1024, B=1, 64 tokens, one weight set "
+                              "(L2-resident)", "us_per_call": tus, "tokens_per_s": 1e6 / tus,
+                              "gpu_launches_per_call": 2}
+        del tffns, tg
         # low-rank gate layer, 32 rotated sets: the gate weights (U, V) of all sets are 316 MB,
         # 2.5x the 129 MB L2, so the gate is read from HBM as in a real model's stack of layers
         li = syn.WORKLOADS[LOPA_WORKLOAD]
