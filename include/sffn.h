@@ -30,9 +30,12 @@
  *   - The handle owns all library memory (packed weights, accumulators,
  *     counters).  It is not thread-safe and must not be used by two streams
  *     at once; concurrent layers need separate handles.
- *   - Numerical sums over live units are accumulated across thread blocks with
- *     fp32 atomics, so y can differ from run to run in its last bits (unless
- *     the handle is created with SFFN_DETERMINISTIC); the live set and the
+ *   - Numerical sums over live units are accumulated across thread blocks.
+ *     The single-token and union-gather kernels add partial y with fp32
+ *     atomics, so there y can differ from run to run in its last bits (unless
+ *     the handle is created with SFFN_DETERMINISTIC); the tensor-core batched
+ *     down kernels sum their partial tiles inside a thread-block cluster in a
+ *     fixed order when the cluster fits (the default).  The live set and the
  *     counts are deterministic.
  */
 #ifndef SFFN_H
@@ -102,8 +105,14 @@ enum {
  * t runs on the CUDA cores, default 2), SFFN_TC_T_SPLIT_TOKENS (K ranges of
  * the tensor-core t kernel times padded tokens, default 1024),
  * SFFN_TC_GATE_KB / SFFN_TC_DOWN_KB (pipeline-stage bytes per block of the
- * tensor-core kernels, default 200), SFFN_TC_GATE_CHUNKS (64-wide K chunks per
- * gate-up stage, 1..4, default by batch).
+ * tensor-core kernels, default 200; 220 for the low-rank gate-up kernel),
+ * SFFN_TC_GATE_CHUNKS (64-wide K chunks per gate-up stage, 1..4, default by
+ * batch), SFFN_TC_DOWN_CLUSTER / SFFN_TC_T_CLUSTER (0: the down kernels and
+ * the low-rank t kernel sum their K splits with fp32 atomics and a last block
+ * instead of inside a thread-block cluster), SFFN_TCG_MAX_BATCH (batches of
+ * 3..N tokens always take the union-skip kernels, 0: never; unset: the
+ * live-fraction rule), SFFN_TCG_ACC (TMEM accumulators per MMA warp of the
+ * union-skip gate kernel, 1..4, default 1).
  */
 sffn_t sffn_create(int D, int H, int r, int act, int dtype);
 
@@ -124,9 +133,10 @@ enum { SFFN_GATE_TILED_G = 1, SFFN_GATE_RMSNORM = 2, SFFN_DOUBLE_ACT = 4 };
 
 /*
  * SFFN_DETERMINISTIC (bf16 handles): y is bitwise reproducible run to run.
- * The pages are silent on summation order; by default each thread block adds
- * its partial y into an fp32 accumulator with atomics, so the last bits of y
- * follow the order in which blocks finish.  With this option every token runs
+ * The pages are silent on summation order; by default the single-token and
+ * union-gather kernels add each thread block's partial y into an fp32
+ * accumulator with atomics, so the last bits of y follow the order in which
+ * blocks finish.  With this option every token runs
  * the single-token kernel, a block folds its live units in ascending unit
  * order and writes its partial y to a row of its own, and a finalize kernel
  * sums the rows in block order.  Costs a [blocks, D] fp32 buffer in the handle
