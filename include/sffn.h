@@ -51,8 +51,8 @@ extern "C" {
 typedef struct sffn_s* sffn_t;
 
 /* element type of W1/U, V, W3, W2, x and y.  SFFN_I8W: weight-only int8 --
-   W1, W3 and W2 are held as int8 codes with one fp32 scale per output channel,
-   x and y are bf16 (standard gate only; see sffn_set_weights_int8).  SFFN_I4W:
+   W1 (or U and V), W3 and W2 are held as int8 codes with one fp32 scale per
+   output channel, x and y are bf16 (see sffn_set_weights_int8).  SFFN_I4W:
    the same with int4 codes in [-7, 7], held two per byte, and one scale per
    group of 64 columns for W1 and W3 */
 enum { SFFN_F32 = 0, SFFN_BF16 = 1, SFFN_I8W = 2, SFFN_I4W = 3 };
