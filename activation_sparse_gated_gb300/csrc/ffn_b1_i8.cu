@@ -521,14 +521,23 @@ __global__ void __launch_bounds__(TW * 32) lopa_t_i8_kernel(const int8_t* __rest
   for (int j = 0; j < PL; ++j) w[j] = (lane + 32 * j < npc && k < r) ? ldg_stream(row + lane + 32 * j) : make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) pdl_launch_dependents();
   pdl_wait();  // x follows stream order
+  // every x piece requested at once: one L2 round trip, not one per piece
+  uint4 xr[PL][2];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const int c = lane + 32 * j;
+    const uint4* xp = reinterpret_cast<const uint4*>(x) + 2 * c;
+    xr[j][0] = c < npc ? __ldcg(xp) : make_uint4(0, 0, 0, 0);
+    xr[j][1] = c < npc ? __ldcg(xp + 1) : make_uint4(0, 0, 0, 0);
+  }
   float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < PL; ++j) {
     const int c = lane + 32 * j;
     if (c >= npc) break;
     float xa[8], xb[8];
-    Elt<bf16_tag>::unpack(__ldcg(reinterpret_cast<const uint4*>(x) + 2 * c), xa);
-    Elt<bf16_tag>::unpack(__ldcg(reinterpret_cast<const uint4*>(x) + 2 * c + 1), xb);
+    Elt<bf16_tag>::unpack(xr[j][0], xa);
+    Elt<bf16_tag>::unpack(xr[j][1], xb);
     const float xv[16] = {xa[0], xa[1], xa[2], xa[3], xa[4], xa[5], xa[6], xa[7],
                           xb[0], xb[1], xb[2], xb[3], xb[4], xb[5], xb[6], xb[7]};
     const uint32_t words[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
