@@ -898,7 +898,7 @@ def run_profile_case(args):
           f"last call: {ffn.active_counts(args.batch)}", flush=True)
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
@@ -921,7 +921,11 @@ def main():
                     help="--profile-case: handle dtype (default: the workload's; int8 / int4 quantise on the device)")
     ap.add_argument("--oracle-one-thread", type=float, default=0.0, metavar="SECONDS",
                     help="(internal) time the oracle on this process's OpenMP threads for SECONDS, print JSON")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     args.warmup = max(args.warmup, 3)   # at least three untimed warm-up steps
     if args.oracle_one_thread > 0:
         from activation_sparse_gated_gb300 import synthetic as syn
