@@ -125,3 +125,13 @@ def test_int4_handle_shape_rules_checked_on_host(lib, args):
     h = lib.sffn_create_ex(D, H, r, sffn.SFFN_ACT_RELU, sffn.SFFN_I4W, flags)
     assert not h
     assert "int4" in sffn.sffn_last_error()
+
+
+@pytest.mark.parametrize("args", [(512, 64, 24, 0), (512, 64, 64, sffn.SFFN_GATE_TILED_G),
+                                  (512, 64, 64, sffn.SFFN_GATE_RMSNORM), (520, 64, 0, 0)])
+def test_int8_handle_shape_rules_checked_on_host(lib, args):
+    """int8 weights: D and r multiples of 16 (16-code pieces), the low-rank gate in its plain form only."""
+    D, H, r, flags = args
+    h = lib.sffn_create_ex(D, H, r, sffn.SFFN_ACT_RELU, sffn.SFFN_I8W, flags)
+    assert not h
+    assert "int8" in sffn.sffn_last_error()
